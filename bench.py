@@ -1,0 +1,457 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged KV-cache hot path on one GB300 (or N replicas under torchrun).
+
+One step = one pass of the whole path over one batch: slot mapping of the step's new
+tokens, then for every layer the KV store of the new tokens and paged attention (decode,
+plus causal chunked prefill where the workload has chunks).  The default workload is
+decode batch 256 with lognormal contexts (median 1024, sigma 0.8, clipped to [1, 8192])
+and 16 layers of KV pools resident; other workloads are reachable with --config.
+
+Prints ONE JSON line (rank 0).  ``value`` is KV-read GB/s: the live K+V bytes the decode
+attention must read in a step (sum of context lengths x 2048 B x layers), divided by the
+device time of the whole step; tokens/s is batch / step time.
+
+``--impl reference`` times the CPU oracle (plain C, double precision) on a bounded sample
+of the same workload: the slow baseline arm, not a target.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attn: KV-read HBM GB/s (% of GB300 peak); tokens/s at batch 256"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per decode launch from an ncu capture (for roofline)")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def workload(cfg: int):
+    from paged_kv_cache_299_gb300 import workloads as wl
+    return wl.CONFIGS[cfg]()
+
+
+def describe(w) -> dict:
+    ctx = w.context_lens
+    d = {"workload": w.name, "batch": int(w.num_seqs), "layers": int(w.layers),
+         "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+         "block_size": w.block_size, "prefill_chunks": int(w.num_prefill),
+         "decode_seqs": int(w.num_decode), "context_min": int(ctx.min()),
+         "context_max": int(ctx.max()), "context_mean": round(float(ctx.mean()), 1),
+         "new_tokens_per_step": int(w.new_lens.sum()), "pool_blocks_per_layer": int(w.num_blocks),
+         "kv_read_bytes_per_step": int(w.decode_kv_bytes()),
+         "partition_tokens": int(w.partition_tokens)}
+    return d
+
+
+# ----------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ----------------------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------------------
+# the GB300 arm
+# ----------------------------------------------------------------------------------------
+class DeviceStep:
+    """Resident state of one workload: per-layer pools (history already stored through the
+    library), this step's inputs, outputs and workspaces."""
+
+    def __init__(self, w, dev):
+        import torch
+        from paged_kv_cache_299_gb300 import binding as pa
+        self.pa = pa
+        self.torch = torch
+        self.w = w
+        self.dev = dev
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
+        self.bt = i32(w.block_tables)
+        self.ctx = i32(w.context_lens)
+        self.new_qsl = i32(w.new_start_loc)
+        self.one_token_each = bool((w.new_lens == 1).all())
+        self.n_new = int(w.new_lens.sum())
+        self.bt_dec = self.bt[w.num_prefill:].contiguous()
+        self.ctx_dec = self.ctx[w.num_prefill:].contiguous()
+        self.bt_pre = self.bt[: w.num_prefill].contiguous()
+        self.ctx_pre = self.ctx[: w.num_prefill].contiguous()
+        self.pre_qsl = i32(w.prefill_query_start_loc)
+        self.max_ctx_dec = int(w.decode_context_lens.max()) if w.num_decode else 0
+        self.max_q_pre = int(w.new_lens[: w.num_prefill].max()) if w.num_prefill else 0
+        self.status = pa.new_device_status(dev)
+        self.slots = torch.empty(self.n_new, dtype=torch.int64, device=dev)
+        shape = (w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim)
+        self.layers = []
+        hist_ctx = i32(w.hist_lens)
+        hist_qsl = i32(w.hist_start_loc)
+        n_hist = int(w.hist_lens.sum())
+        for layer in range(w.layers):
+            vals = w.values(layer, dev)
+            kc = torch.full(shape, float("nan"), dtype=torch.bfloat16, device=dev)
+            vc = torch.full(shape, float("nan"), dtype=torch.bfloat16, device=dev)
+            if n_hist:
+                hs = pa.pa_compute_slot_mapping(self.bt, hist_ctx, hist_qsl, n_hist, kc,
+                                                device_status=self.status)
+                pa.pa_reshape_and_cache(vals["hist_k"], vals["hist_v"], hs, kc, vc,
+                                        device_status=self.status)
+                del hs
+            self.layers.append({
+                "kc": kc, "vc": vc, "new_k": vals["new_k"], "new_v": vals["new_v"],
+                "q_dec": vals["q_decode"], "q_pre": vals["q_prefill"],
+                "out_dec": torch.empty_like(vals["q_decode"]),
+                "out_pre": torch.empty_like(vals["q_prefill"]),
+            })
+            del vals
+            torch.cuda.synchronize(dev)
+        if w.num_decode:
+            need = pa.pa_decode_workspace_size(w.num_decode, w.num_kv_heads, w.num_q_heads,
+                                               self.max_ctx_dec, w.partition_tokens)
+            self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        assert pa.pa_check_device_status(self.status) == pa.PA_OK
+
+    def launches_per_step(self) -> int:
+        w = self.w
+        per_layer = 1 + (2 if w.num_decode else 0) + (1 if w.num_prefill else 0)
+        return 1 + per_layer * w.layers
+
+    def step(self, dec_events=None):
+        pa, w = self.pa, self.w
+        pa.pa_compute_slot_mapping(self.bt, self.ctx, None if self.one_token_each else self.new_qsl,
+                                   self.n_new, self.layers[0]["kc"], slot_mapping=self.slots)
+        for li, L in enumerate(self.layers):
+            pa.pa_reshape_and_cache(L["new_k"], L["new_v"], self.slots, L["kc"], L["vc"])
+            if w.num_prefill:
+                pa.pa_prefill_chunk(L["out_pre"], L["q_pre"], self.pre_qsl, self.max_q_pre,
+                                    L["kc"], L["vc"], self.bt_pre, self.ctx_pre, w.scale)
+            if w.num_decode:
+                if dec_events is not None:
+                    dec_events[li][0].record()
+                pa.pa_decode(L["out_dec"], L["q_dec"], L["kc"], L["vc"], self.bt_dec,
+                             self.ctx_dec, w.scale, self.max_ctx_dec, w.partition_tokens,
+                             workspace=self.ws)
+                if dec_events is not None:
+                    dec_events[li][1].record()
+
+
+def run_gpu(args, rank, world):
+    import torch
+    import torch.distributed as dist
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workload(args.config)
+    if world > 1:  # weak scaling: every rank serves its own batch (seed offset)
+        from paged_kv_cache_299_gb300 import workloads as wl
+        w = wl.CONFIGS[args.config](seed=w.seed + 100 * rank)
+    st = DeviceStep(w, dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    kv_bytes = w.decode_kv_bytes()
+    flush = kv_bytes < 4 * l2
+    flush_buf = torch.empty(2 * l2 // 4 + 1024, dtype=torch.int32, device=dev) if flush else None
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        st.step()
+    torch.cuda.synchronize(dev)
+    barrier()
+
+    K = args.steps
+    dec_ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+               for _ in range(w.layers)] for _ in range(K)]
+    step_ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+               for _ in range(K)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize(dev)
+    barrier()
+    t_wall = time.perf_counter()
+    for k in range(K):
+        if flush:
+            flush_buf.fill_(k)  # rewrite a buffer of twice the L2 size between steps
+        step_ev[k][0].record()
+        st.step(dec_ev[k] if w.num_decode else None)
+        step_ev[k][1].record()
+    torch.cuda.synchronize(dev)
+    barrier()
+    wall = time.perf_counter() - t_wall
+    clocks = sampler.stop()
+    step_ms = sum(a.elapsed_time(b) for a, b in step_ev) / K
+    dec_ms = None
+    if w.num_decode:
+        dec_ms = sum(a.elapsed_time(b) for row in dec_ev for a, b in row) / (K * w.layers)
+    if world > 1:
+        t = torch.tensor([step_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(st, max(3, min(K, 50)), dev)
+        if world > 1:
+            t = torch.tensor([e2e["step_ms"]], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e["step_ms"] = float(t.item())
+
+    if rank != 0:
+        return
+    peak, peak_src = measured_peaks()
+    value = kv_bytes * world / (step_ms * 1e-3) / 1e9
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": dict(describe(w), parallelism=f"replicas{world}" if world > 1 else "single",
+                       accumulate="f32",
+                       l2=("flushed between steps (2x L2 rewrite)" if flush
+                           else "inputs larger than L2 (%.1f GB KV per step)" % (kv_bytes / 1e9)),
+                       launch="eager (one C-ABI call per kernel group)"),
+        "tokens_per_s": round(w.num_decode * world / (step_ms * 1e-3), 1),
+        "pct_of_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "gpu_launches": st.launches_per_step() * K,
+        "wall_s_timed": round(wall, 3),
+        "clocks": clocks,
+    }
+    if dec_ms:
+        per_launch = kv_bytes / w.layers
+        achieved = per_launch / (dec_ms * 1e-3) / 1e9
+        res["roofline"] = {
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": args.traffic,
+            "kernel": "pa_decode (paged_decode_kernel + merge_partials_kernel)",
+            "peak_source": f"{peak_src} hbm_gbs", "pct_of_8tbs": round(100 * achieved / 8000, 2),
+            "launch_ms": round(dec_ms, 5), "algorithmic_bytes_per_launch": int(per_launch)}
+    if e2e:
+        res["e2e"] = {"value": round(kv_bytes * world / (e2e["step_ms"] * 1e-3) / 1e9, 1),
+                      "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
+                      "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e["step_ms"], 4)}
+    if not args.no_cpu_baseline and world == 1:
+        res["cpu_baseline"] = cpu_baseline(w, args.config, target_s=10.0)
+    print(json.dumps(res), flush=True)
+
+
+def run_e2e(st: DeviceStep, steps: int, dev) -> dict:
+    """Each step: pinned host -> device copy of the step's inputs (queries, new K/V, block
+    tables, context lengths), the step through the C ABI, device -> host copy of the
+    attention outputs.  Timed on the device with events around the whole loop."""
+    import torch
+    w = st.w
+    pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+    host_in, host_out = [], []
+    for L in st.layers:
+        for key in ("q_dec", "q_pre", "new_k", "new_v"):
+            if L[key].numel():
+                host_in.append((pin(L[key]), L[key]))
+        for key in ("out_dec", "out_pre"):
+            if L[key].numel():
+                host_out.append((torch.empty(L[key].shape, dtype=L[key].dtype, pin_memory=True),
+                                 L[key]))
+    for t in (st.bt, st.ctx):
+        host_in.append((pin(t), t))
+    h2d = sum(h.numel() * h.element_size() for h, _ in host_in)
+    d2h = sum(h.numel() * h.element_size() for h, _ in host_out)
+
+    def one():
+        for h, d in host_in:
+            d.copy_(h, non_blocking=True)
+        st.step()
+        for h, d in host_out:
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize(dev)
+    return {"step_ms": a.elapsed_time(b) / steps, "h2d": h2d, "d2h": d2h}
+
+
+# ----------------------------------------------------------------------------------------
+# the CPU oracle (baseline leg and --impl reference)
+# ----------------------------------------------------------------------------------------
+def oracle_sample(w, max_seqs: int):
+    """A bounded sample of the workload: its first sequences (same length law), one layer,
+    drawn on the host; returns a callable doing one oracle step and its KV bytes."""
+    import oracle
+    from paged_kv_cache_299_gb300 import workloads as wl
+
+    n = min(max_seqs, w.num_seqs)
+    npre = min(w.num_prefill, n)
+    sw = wl.make_workload(w.name + f"_sample{n}", w.hist_lens[:n], w.new_lens[:n],
+                          num_prefill=npre, seed=w.seed,
+                          big_key_fraction=w.big_key_fraction)
+    vals = sw.values(0, "cpu")
+    kc, vc = wl.nan_pool(sw.num_blocks), wl.nan_pool(sw.num_blocks)
+    hs, err = oracle.slot_mapping(sw.block_tables, sw.hist_lens, sw.hist_start_loc, sw.num_blocks)
+    oracle.reshape_and_cache(wl.bf16_bits(vals["hist_k"]), wl.bf16_bits(vals["hist_v"]), hs,
+                             kc, vc)
+    new_k, new_v = wl.bf16_bits(vals["new_k"]), wl.bf16_bits(vals["new_v"])
+    qd, qp = wl.bf16_bits(vals["q_decode"]), wl.bf16_bits(vals["q_prefill"])
+
+    def step():
+        slots, _ = oracle.slot_mapping(sw.block_tables, sw.context_lens, sw.new_start_loc,
+                                       sw.num_blocks)
+        oracle.reshape_and_cache(new_k, new_v, slots, kc, vc)
+        if sw.num_prefill:
+            oracle.prefill_chunk(qp, sw.prefill_query_start_loc, kc, vc,
+                                 sw.block_tables[:npre], sw.context_lens[:npre], sw.scale)
+        if sw.num_decode:
+            oracle.decode(qd, kc, vc, sw.decode_block_tables, sw.decode_context_lens, sw.scale)
+
+    return sw, step, sw.decode_kv_bytes()
+
+
+def cpu_baseline(w, cfg: int, target_s: float) -> dict:
+    sw, step, kv = oracle_sample(w, 32)
+    step()  # warm
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        step()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= target_s:
+            break
+    gbs = kv * reps / el / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"one layer of the first {sw.num_seqs} sequences of {w.name} "
+                      f"({int(sw.context_lens.sum())} cached tokens), {reps} repetitions, "
+                      f"{el:.1f} s single-threaded",
+            "tokens_per_s": round(sw.num_decode * reps / el, 3)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = workload(args.config)
+    sw, step, kv = oracle_sample(w, 4)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    ms = el * 1e3 / args.steps
+    value = kv / (ms * 1e-3) / 1e9
+    res = {
+        "metric": METRIC, "impl": "reference", "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": describe(w),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: one layer of the first {sw.num_seqs} sequences "
+                                   f"of {w.name} ({int(sw.context_lens.sum())} cached tokens)"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl")
+    try:
+        run_gpu(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,161 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv.so, the GB300 (sm_103a) paged KV cache.
+ *
+ * What it computes (from the four web pages this library restates):
+ *   - "vLLM" (blog.rlaisqls.com), section PagedAttention: the KV cache is cut into
+ *     fixed blocks of 16 tokens; a per-sequence block table maps logical positions to
+ *     physical blocks, which need not be contiguous.
+ *   - "Tiny-vLLM" (trendpick100.com), Q&A on how Tiny-vLLM splits complexity:
+ *     prepare_prefill / prepare_decode publish a slot_mapping, and a store kernel writes
+ *     each token's key/value vector to its slot.
+ *   - "vLLM", section Flash Attention: attention S = Q K^T, P = softmax(S), O = P V,
+ *     evaluated block by block with a running max and running sum (online softmax), so
+ *     the score matrix never reaches HBM.
+ *   - "tiny-vllm (1)" (geonuchoi.com), section 2 (GQA): consecutive groups of query
+ *     heads share one K/V head (query head h reads K/V head h / (Hq / Hkv)); section 1:
+ *     causal decoding, position t sees positions <= t.
+ *
+ * Conventions shared by every call:
+ *   - All pointers are DEVICE pointers on the current CUDA device, 16-byte aligned,
+ *     to contiguous row-major arrays.  The caller owns every buffer; the library never
+ *     allocates, frees or synchronises on these paths (pa_check_device_status aside).
+ *   - bf16 tensors: key/value [T][Hkv][D], q / out [rows][Hq][D].
+ *   - Cache pools: key_cache and value_cache are separate pools, each
+ *     [num_blocks][Hkv][block_size][D] bf16, so one (block, kv head) tile is a
+ *     contiguous block_size * D * 2 = 2 KiB run.
+ *   - slot = physical_block * block_size + offset_in_block (int64); slot < 0 = skip.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
+ *   - Supported shapes: head_dim == 64, block_size == 16, num_q_heads / num_kv_heads in
+ *     {1, 2, 4}.  Other values return PA_ERR_UNSUPPORTED.
+ *
+ * Errors: a call whose arguments are wrong on the host returns a negative pa_status and
+ * launches nothing; pa_last_error() then holds a one-line reason.  Problems only the
+ * device can see (a block id outside [0, num_blocks), a slot beyond the pool, a context
+ * longer than its block-table row, a pipeline wait that timed out) never trap: the
+ * kernel ORs a PA_DEVFLAG_* bit into *device_status (if non-NULL), skips the affected
+ * work and returns; results of the affected rows are undefined.  Read the word with
+ * pa_check_device_status().
+ */
+#ifndef PAGEDKV_H_
+#define PAGEDKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* pa_stream_t; /* same type as cudaStream_t */
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = -1,   /* null/misaligned pointer, negative size, bad desc */
+  PA_ERR_UNSUPPORTED = -2,   /* a shape these kernels do not implement */
+  PA_ERR_CUDA = -3,          /* a CUDA runtime call failed (launch, query, copy) */
+  PA_ERR_WORKSPACE = -4,     /* workspace missing or smaller than required */
+  PA_ERR_DEVICE_INDEX = -5,  /* device_status reports a bad block id / slot / length */
+  PA_ERR_DEVICE_TIMEOUT = -6 /* device_status reports a pipeline wait that timed out */
+} pa_status;
+
+/* Bits a kernel ORs into *device_status. */
+#define PA_DEVFLAG_BAD_BLOCK 0x1   /* block-table entry outside [0, num_blocks) */
+#define PA_DEVFLAG_BAD_SLOT 0x2    /* slot >= num_blocks * block_size */
+#define PA_DEVFLAG_BAD_CONTEXT 0x4 /* context length < 0, beyond its table row, or beyond
+                                      the host bound max_context_len */
+#define PA_DEVFLAG_TIMEOUT 0x8     /* an mbarrier wait exceeded its time limit */
+
+/* Geometry of one layer's pair of cache pools; validated on every call. */
+typedef struct pa_cache_desc {
+  int32_t num_blocks;   /* physical blocks in each pool */
+  int32_t num_kv_heads; /* Hkv (8 for Llama-3.2-1B) */
+  int32_t head_dim;     /* D, must be 64 */
+  int32_t block_size;   /* tokens per block, must be 16 */
+} pa_cache_desc;
+
+/* Slot mapping (the step prepare_prefill / prepare_decode perform on the "Tiny-vLLM" page,
+ * run here as a kernel).  Sequence s appends the tokens query_start_loc[s] ..
+ * query_start_loc[s+1]-1, which are the last q_len of its context_lens[s] tokens; the
+ * token at logical position p gets slot block_tables[s][p / 16] * 16 + p % 16.
+ *   block_tables    int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens    int32 [num_seqs], token count AFTER this append
+ *   query_start_loc int32 [num_seqs + 1] prefix sums of appended counts, or NULL for
+ *                   exactly one appended token per sequence (then num_tokens == num_seqs)
+ *   num_tokens      == query_start_loc[num_seqs] (host-known; sizes the grid)
+ *   slot_mapping    int64 [num_tokens] output; -1 where the device saw a bad entry
+ * num_tokens == 0 is a no-op. */
+pa_status pa_compute_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* context_lens,
+                                  const int32_t* query_start_loc, int32_t num_seqs,
+                                  int32_t num_tokens, pa_cache_desc cd,
+                                  int64_t* slot_mapping, int32_t* device_status,
+                                  pa_stream_t stream);
+
+/* KV store ("reshape_and_cache"): for every token t with slot_mapping[t] >= 0, copy
+ * key[t][h][:] to key_cache[slot / 16][h][slot % 16][:] and value likewise, for all
+ * heads h.  A bit-exact copy.  key/value bf16 [num_tokens][Hkv][D]; num_tokens == 0 is a
+ * no-op.  Duplicate slots within one call are a caller error (the winner is undefined). */
+pa_status pa_reshape_and_cache(const void* key, const void* value,
+                               const int64_t* slot_mapping, int32_t num_tokens,
+                               void* key_cache, void* value_cache, pa_cache_desc cd,
+                               int32_t* device_status, pa_stream_t stream);
+
+/* Bytes of device workspace pa_decode needs for these sizes on the current device
+ * (0 when the sizes are invalid).  The workspace holds the split-KV partial results and
+ * the per-sequence block offsets; it needs no initialisation. */
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_heads,
+                                int32_t max_context_len, int32_t partition_tokens);
+
+/* Paged decode attention: one query per sequence (its newest token, already stored)
+ * over all context_lens[s] cached tokens:
+ *   out[s][h][:] = sum_j softmax_j(scale * q[s][h] . K_s[j][h / group]) V_s[j][h / group]
+ * where K_s[j] / V_s[j] is the token at logical position j found through block_tables.
+ * The (sequence, K/V head, block) tiles are split evenly over the SMs (or into runs of
+ * partition_tokens tokens); runs that end inside a sequence leave (running max, running
+ * sum, unnormalised output) partials that a second kernel merges.
+ *   out              bf16 [num_seqs][num_q_heads][D] output
+ *   q                bf16 [num_seqs][num_q_heads][D]
+ *   block_tables     int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens     int32 [num_seqs]; 0 gives a zero output row
+ *   max_context_len  host-known upper bound of context_lens (sizes the grid)
+ *   partition_tokens 0 = split evenly over the device; else a multiple of 16 giving
+ *                    the run length in tokens
+ *   workspace        device buffer of >= pa_decode_workspace_size(...) bytes
+ * num_seqs == 0 is a no-op.  At most 8192 sequences per call. */
+pa_status pa_decode(void* out, const void* q, const void* key_cache, const void* value_cache,
+                    pa_cache_desc cd, const int32_t* block_tables,
+                    int32_t max_blocks_per_seq, const int32_t* context_lens,
+                    int32_t num_seqs, int32_t num_q_heads, float scale,
+                    int32_t max_context_len, int32_t partition_tokens, void* workspace,
+                    size_t workspace_bytes, int32_t* device_status, pa_stream_t stream);
+
+/* Causal chunked-prefill attention over a paged prefix.  Sequence s has q_len =
+ * query_start_loc[s+1] - query_start_loc[s] query rows, the last q_len of its
+ * context_lens[s] tokens (already stored); row i sits at position L - q_len + i and
+ * attends keys 0 .. L - q_len + i.  QK^T and PV run on tcgen05 tensor cores.
+ *   out / q          bf16 [query_start_loc[num_seqs]][num_q_heads][D]
+ *   max_query_len    host-known upper bound of q_len (sizes the grid)
+ * Requires num_q_heads / num_kv_heads == 4.  num_seqs == 0 is a no-op. */
+pa_status pa_prefill_chunk(void* out, const void* q, const int32_t* query_start_loc,
+                           int32_t max_query_len, const void* key_cache,
+                           const void* value_cache, pa_cache_desc cd,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* context_lens, int32_t num_seqs,
+                           int32_t num_q_heads, float scale, int32_t* device_status,
+                           pa_stream_t stream);
+
+/* Synchronise `stream`, read *device_status and translate it: PA_OK when zero,
+ * PA_ERR_DEVICE_TIMEOUT when the timeout bit is set, else PA_ERR_DEVICE_INDEX. */
+pa_status pa_check_device_status(const int32_t* device_status, pa_stream_t stream);
+
+/* Static description of a status code (never NULL). */
+const char* pa_status_string(pa_status status);
+
+/* One-line detail of this thread's last non-OK return ("" if none). */
+const char* pa_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H_ */

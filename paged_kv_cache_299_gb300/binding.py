@@ -1,0 +1,223 @@
+"""Python binding of libpagedkv.so: the C-ABI calls of include/pagedkv.h under the same
+names, taking torch CUDA tensors.
+
+This module only marshals arguments (dtype / shape / device checks, data pointers, the
+current CUDA stream) and raises ``PagedKVError`` on a non-OK status; every step of the
+path runs in the library's kernels.  There is no fallback: if the library is missing or
+fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+_lib = None
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32)]
+
+
+PA_OK = 0
+PA_ERR_INVALID_ARG = -1
+PA_ERR_UNSUPPORTED = -2
+PA_ERR_CUDA = -3
+PA_ERR_WORKSPACE = -4
+PA_ERR_DEVICE_INDEX = -5
+PA_ERR_DEVICE_TIMEOUT = -6
+DEVFLAG_BAD_BLOCK, DEVFLAG_BAD_SLOT, DEVFLAG_BAD_CONTEXT, DEVFLAG_TIMEOUT = 1, 2, 4, 8
+
+# Every symbol include/pagedkv.h declares.
+EXPORTED = ("pa_compute_slot_mapping", "pa_reshape_and_cache", "pa_decode_workspace_size",
+            "pa_decode", "pa_prefill_chunk", "pa_check_device_status", "pa_status_string",
+            "pa_last_error")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Load (building first if the sources are newer) and bind the library."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    if path is None:
+        path = _build.build()
+    if not os.path.exists(path):
+        raise PagedKVError(PA_ERR_CUDA, f"libpagedkv.so not found at {path}")
+    lib = ctypes.CDLL(path)
+    P, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
+    st = ctypes.c_int
+    lib.pa_compute_slot_mapping.argtypes = [P, i32, P, P, i32, i32, CacheDesc, P, P, P]
+    lib.pa_compute_slot_mapping.restype = st
+    lib.pa_reshape_and_cache.argtypes = [P, P, P, i32, P, P, CacheDesc, P, P]
+    lib.pa_reshape_and_cache.restype = st
+    lib.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    lib.pa_decode_workspace_size.restype = sz
+    lib.pa_decode.argtypes = [P, P, P, P, CacheDesc, P, i32, P, i32, i32, f32, i32, i32, P, sz,
+                              P, P]
+    lib.pa_decode.restype = st
+    lib.pa_prefill_chunk.argtypes = [P, P, P, i32, P, P, CacheDesc, P, i32, P, i32, i32, f32, P,
+                                     P]
+    lib.pa_prefill_chunk.restype = st
+    lib.pa_check_device_status.argtypes = [P, P]
+    lib.pa_check_device_status.restype = st
+    lib.pa_status_string.argtypes = [st]
+    lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_last_error.argtypes = []
+    lib.pa_last_error.restype = ctypes.c_char_p
+    if path == _build.LIB:
+        _lib = lib
+    return lib
+
+
+def _check(status: int, what: str):
+    if status != PA_OK:
+        lib = load()
+        msg = lib.pa_last_error().decode()
+        name = lib.pa_status_string(status).decode()
+        raise PagedKVError(status, f"{what}: {name} ({msg})")
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, name, dtype, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+
+
+def cache_desc(key_cache: torch.Tensor) -> CacheDesc:
+    nb, hkv, bs, d = key_cache.shape
+    return CacheDesc(nb, hkv, d, bs)
+
+
+def new_device_status(device=None) -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def pa_compute_slot_mapping(block_tables, context_lens, query_start_loc, num_tokens,
+                            key_cache, slot_mapping=None, device_status=None, stream=None):
+    """int64 slot of every appended token (see include/pagedkv.h)."""
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    if query_start_loc is not None:
+        _need(query_start_loc, "query_start_loc", torch.int32, 1)
+    if slot_mapping is None:
+        slot_mapping = torch.empty(num_tokens, dtype=torch.int64, device=block_tables.device)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    st = load().pa_compute_slot_mapping(
+        _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), _ptr(query_start_loc),
+        context_lens.shape[0], int(num_tokens), cache_desc(key_cache), _ptr(slot_mapping),
+        _ptr(device_status), _stream(stream))
+    _check(st, "pa_compute_slot_mapping")
+    return slot_mapping
+
+
+def pa_reshape_and_cache(key, value, slot_mapping, key_cache, value_cache, device_status=None,
+                         stream=None):
+    """Store key/value [T, Hkv, D] into the paged pools at slot_mapping[T]."""
+    _need(key, "key", torch.bfloat16, 3)
+    _need(value, "value", torch.bfloat16, 3)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    _need(key_cache, "key_cache", torch.bfloat16, 4)
+    _need(value_cache, "value_cache", torch.bfloat16, 4)
+    if key.shape != value.shape or key_cache.shape != value_cache.shape:
+        raise ValueError("key/value or cache shapes differ")
+    if key.shape[0] != slot_mapping.shape[0] or key.shape[1:] != (key_cache.shape[1],
+                                                                   key_cache.shape[3]):
+        raise ValueError("key shape does not match slot_mapping / cache")
+    st = load().pa_reshape_and_cache(_ptr(key), _ptr(value), _ptr(slot_mapping), key.shape[0],
+                                     _ptr(key_cache), _ptr(value_cache), cache_desc(key_cache),
+                                     _ptr(device_status), _stream(stream))
+    _check(st, "pa_reshape_and_cache")
+
+
+def pa_decode_workspace_size(num_seqs, num_kv_heads, num_q_heads, max_context_len,
+                             partition_tokens=0) -> int:
+    return int(load().pa_decode_workspace_size(num_seqs, num_kv_heads, num_q_heads,
+                                               max_context_len, partition_tokens))
+
+
+def pa_decode(out, q, key_cache, value_cache, block_tables, context_lens, scale,
+              max_context_len, partition_tokens=0, workspace=None, device_status=None,
+              stream=None):
+    """Paged decode attention; writes out [S, Hq, D] (bf16)."""
+    _need(out, "out", torch.bfloat16, 3)
+    _need(q, "q", torch.bfloat16, 3)
+    _need(key_cache, "key_cache", torch.bfloat16, 4)
+    _need(value_cache, "value_cache", torch.bfloat16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    num_seqs, hq, _ = q.shape
+    if out.shape != q.shape or block_tables.shape[0] != num_seqs or \
+            context_lens.shape[0] != num_seqs:
+        raise ValueError("q/out/block_tables/context_lens disagree on the sequence count")
+    if workspace is None:
+        need = pa_decode_workspace_size(num_seqs, key_cache.shape[1], hq, max_context_len,
+                                        partition_tokens)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _need(workspace, "workspace", torch.uint8, 1)
+    st = load().pa_decode(_ptr(out), _ptr(q), _ptr(key_cache), _ptr(value_cache),
+                          cache_desc(key_cache), _ptr(block_tables), block_tables.shape[1],
+                          _ptr(context_lens), num_seqs, hq, float(scale), int(max_context_len),
+                          int(partition_tokens), _ptr(workspace), workspace.numel(),
+                          _ptr(device_status), _stream(stream))
+    _check(st, "pa_decode")
+    return out
+
+
+def pa_prefill_chunk(out, q, query_start_loc, max_query_len, key_cache, value_cache,
+                     block_tables, context_lens, scale, device_status=None, stream=None):
+    """Causal chunked-prefill attention; writes out [Tq, Hq, D] (bf16)."""
+    _need(out, "out", torch.bfloat16, 3)
+    _need(q, "q", torch.bfloat16, 3)
+    _need(query_start_loc, "query_start_loc", torch.int32, 1)
+    _need(key_cache, "key_cache", torch.bfloat16, 4)
+    _need(value_cache, "value_cache", torch.bfloat16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    num_seqs = context_lens.shape[0]
+    if out.shape != q.shape or query_start_loc.shape[0] != num_seqs + 1 or \
+            block_tables.shape[0] != num_seqs:
+        raise ValueError("prefill argument shapes disagree")
+    st = load().pa_prefill_chunk(_ptr(out), _ptr(q), _ptr(query_start_loc), int(max_query_len),
+                                 _ptr(key_cache), _ptr(value_cache), cache_desc(key_cache),
+                                 _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+                                 num_seqs, q.shape[1], float(scale), _ptr(device_status),
+                                 _stream(stream))
+    _check(st, "pa_prefill_chunk")
+    return out
+
+
+def pa_check_device_status(device_status, stream=None) -> int:
+    """Synchronise and translate the device status word; returns the pa_status code."""
+    _need(device_status, "device_status", torch.int32, 1)
+    return int(load().pa_check_device_status(_ptr(device_status), _stream(stream)))

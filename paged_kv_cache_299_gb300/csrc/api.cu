@@ -1,0 +1,246 @@
+// C-ABI entry points of libpagedkv.so: host-side argument checks, then kernel launches.
+// Declarations and the contract of every call are in include/pagedkv.h.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+int decode_max_seqs();
+}  // namespace pkv
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+pa_status fail(pa_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+pa_status ok() {
+  g_last_error[0] = '\0';
+  return PA_OK;
+}
+
+pa_status from_cuda(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return ok();
+  return fail(PA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+pa_status check_desc(const pa_cache_desc& cd) {
+  if (cd.num_blocks <= 0 || cd.num_kv_heads <= 0 || cd.num_kv_heads > 64)
+    return fail(PA_ERR_INVALID_ARG, "cache desc: num_blocks %d, num_kv_heads %d",
+                cd.num_blocks, cd.num_kv_heads);
+  if (cd.head_dim != pkv::kHeadDim)
+    return fail(PA_ERR_UNSUPPORTED, "head_dim %d (only 64 is implemented)", cd.head_dim);
+  if (cd.block_size != pkv::kBlockSize)
+    return fail(PA_ERR_UNSUPPORTED, "block_size %d (only 16 is implemented)", cd.block_size);
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_compute_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* context_lens,
+                                  const int32_t* query_start_loc, int32_t num_seqs,
+                                  int32_t num_tokens, pa_cache_desc cd,
+                                  int64_t* slot_mapping, int32_t* device_status,
+                                  pa_stream_t stream) {
+  pa_status st = check_desc(cd);
+  if (st != PA_OK) return st;
+  if (num_tokens < 0 || num_seqs < 0 || max_blocks_per_seq <= 0)
+    return fail(PA_ERR_INVALID_ARG, "num_tokens %d, num_seqs %d, max_blocks_per_seq %d",
+                num_tokens, num_seqs, max_blocks_per_seq);
+  if (num_tokens == 0) return ok();
+  if (num_seqs == 0) return fail(PA_ERR_INVALID_ARG, "tokens without sequences");
+  if (query_start_loc == nullptr && num_tokens != num_seqs)
+    return fail(PA_ERR_INVALID_ARG, "query_start_loc NULL needs num_tokens == num_seqs");
+  if (!block_tables || !context_lens || !slot_mapping)
+    return fail(PA_ERR_INVALID_ARG, "null pointer");
+  return from_cuda(pkv::launch_slot_mapping(block_tables, max_blocks_per_seq, context_lens,
+                                            query_start_loc, num_seqs, num_tokens,
+                                            cd.num_blocks, slot_mapping, device_status,
+                                            reinterpret_cast<cudaStream_t>(stream)),
+                   "slot mapping launch");
+}
+
+pa_status pa_reshape_and_cache(const void* key, const void* value,
+                               const int64_t* slot_mapping, int32_t num_tokens,
+                               void* key_cache, void* value_cache, pa_cache_desc cd,
+                               int32_t* device_status, pa_stream_t stream) {
+  pa_status st = check_desc(cd);
+  if (st != PA_OK) return st;
+  if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens %d", num_tokens);
+  if (num_tokens == 0) return ok();
+  if (!key || !value || !slot_mapping || !key_cache || !value_cache)
+    return fail(PA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache))
+    return fail(PA_ERR_INVALID_ARG, "key/value/cache pointers must be 16-byte aligned");
+  return from_cuda(pkv::launch_reshape_and_cache(key, value, slot_mapping, num_tokens,
+                                                 key_cache, value_cache, cd.num_blocks,
+                                                 cd.num_kv_heads, device_status,
+                                                 reinterpret_cast<cudaStream_t>(stream)),
+                   "reshape_and_cache launch");
+}
+
+static pa_status check_decode_sizes(int32_t num_seqs, int32_t num_kv_heads,
+                                    int32_t num_q_heads, int32_t max_context_len,
+                                    int32_t partition_tokens) {
+  if (num_seqs < 0 || num_seqs > pkv::decode_max_seqs())
+    return fail(num_seqs < 0 ? PA_ERR_INVALID_ARG : PA_ERR_UNSUPPORTED,
+                "num_seqs %d (0..%d supported)", num_seqs, pkv::decode_max_seqs());
+  if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
+    return fail(PA_ERR_INVALID_ARG, "num_q_heads %d not a multiple of num_kv_heads %d",
+                num_q_heads, num_kv_heads);
+  const int group = num_q_heads / num_kv_heads;
+  if (group != 1 && group != 2 && group != 4)
+    return fail(PA_ERR_UNSUPPORTED, "query heads per kv head %d (1, 2, 4 implemented)", group);
+  if (max_context_len < 0) return fail(PA_ERR_INVALID_ARG, "max_context_len %d", max_context_len);
+  if (partition_tokens < 0 || partition_tokens % pkv::kBlockSize != 0)
+    return fail(PA_ERR_INVALID_ARG, "partition_tokens %d (0 or a multiple of 16)",
+                partition_tokens);
+  return PA_OK;
+}
+
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_heads,
+                                int32_t max_context_len, int32_t partition_tokens) {
+  if (check_decode_sizes(num_seqs, num_kv_heads, num_q_heads, max_context_len,
+                         partition_tokens) != PA_OK)
+    return 0;
+  if (num_seqs == 0) return 0;
+  pkv::DecodePlan plan;
+  if (pkv::plan_decode(num_seqs, num_kv_heads, num_q_heads, max_context_len, partition_tokens,
+                       &plan) != cudaSuccess)
+    return 0;
+  return plan.workspace_bytes;
+}
+
+pa_status pa_decode(void* out, const void* q, const void* key_cache, const void* value_cache,
+                    pa_cache_desc cd, const int32_t* block_tables,
+                    int32_t max_blocks_per_seq, const int32_t* context_lens,
+                    int32_t num_seqs, int32_t num_q_heads, float scale,
+                    int32_t max_context_len, int32_t partition_tokens, void* workspace,
+                    size_t workspace_bytes, int32_t* device_status, pa_stream_t stream) {
+  pa_status st = check_desc(cd);
+  if (st != PA_OK) return st;
+  st = check_decode_sizes(num_seqs, cd.num_kv_heads, num_q_heads, max_context_len,
+                          partition_tokens);
+  if (st != PA_OK) return st;
+  if (num_seqs == 0) return ok();
+  if (max_blocks_per_seq <= 0)
+    return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq %d", max_blocks_per_seq);
+  if (!out || !q || !key_cache || !value_cache || !block_tables || !context_lens)
+    return fail(PA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
+    return fail(PA_ERR_INVALID_ARG, "out/q/cache pointers must be 16-byte aligned");
+  if (!(scale > 0.f) || !isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale %g", scale);
+  pkv::DecodePlan plan;
+  cudaError_t e = pkv::plan_decode(num_seqs, cd.num_kv_heads, num_q_heads, max_context_len,
+                                   partition_tokens, &plan);
+  if (e != cudaSuccess) return from_cuda(e, "decode plan");
+  if (!workspace || workspace_bytes < plan.workspace_bytes || !aligned16(workspace))
+    return fail(PA_ERR_WORKSPACE, "workspace %zu bytes at %p, need %zu (16-byte aligned)",
+                workspace_bytes, workspace, plan.workspace_bytes);
+  pkv::DecodeArgs a;
+  a.out = out;
+  a.q = q;
+  a.key_cache = key_cache;
+  a.value_cache = value_cache;
+  a.block_tables = block_tables;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.context_lens = context_lens;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = cd.num_kv_heads;
+  a.num_blocks = cd.num_blocks;
+  a.scale = scale;
+  a.workspace = workspace;
+  a.status = device_status;
+  return from_cuda(pkv::launch_decode(a, plan, reinterpret_cast<cudaStream_t>(stream)),
+                   "decode launch");
+}
+
+pa_status pa_prefill_chunk(void* out, const void* q, const int32_t* query_start_loc,
+                           int32_t max_query_len, const void* key_cache,
+                           const void* value_cache, pa_cache_desc cd,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* context_lens, int32_t num_seqs,
+                           int32_t num_q_heads, float scale, int32_t* device_status,
+                           pa_stream_t stream) {
+  pa_status st = check_desc(cd);
+  if (st != PA_OK) return st;
+  if (num_seqs < 0 || max_query_len < 0 || max_blocks_per_seq <= 0)
+    return fail(PA_ERR_INVALID_ARG, "num_seqs %d, max_query_len %d, max_blocks_per_seq %d",
+                num_seqs, max_query_len, max_blocks_per_seq);
+  if (num_seqs == 0 || max_query_len == 0) return ok();
+  if (num_q_heads != 4 * cd.num_kv_heads)
+    return fail(PA_ERR_UNSUPPORTED, "prefill needs 4 query heads per kv head (got %d / %d)",
+                num_q_heads, cd.num_kv_heads);
+  if (!out || !q || !query_start_loc || !key_cache || !value_cache || !block_tables ||
+      !context_lens)
+    return fail(PA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
+    return fail(PA_ERR_INVALID_ARG, "out/q/cache pointers must be 16-byte aligned");
+  if (!(scale > 0.f) || !isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale %g", scale);
+  pkv::PrefillArgs a;
+  a.out = out;
+  a.q = q;
+  a.query_start_loc = query_start_loc;
+  a.max_query_len = max_query_len;
+  a.key_cache = key_cache;
+  a.value_cache = value_cache;
+  a.num_blocks = cd.num_blocks;
+  a.num_kv_heads = cd.num_kv_heads;
+  a.block_tables = block_tables;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.context_lens = context_lens;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.scale = scale;
+  a.status = device_status;
+  return from_cuda(pkv::launch_prefill(a, reinterpret_cast<cudaStream_t>(stream)),
+                   "prefill launch");
+}
+
+pa_status pa_check_device_status(const int32_t* device_status, pa_stream_t stream) {
+  if (!device_status) return fail(PA_ERR_INVALID_ARG, "null status pointer");
+  int32_t word = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(&word, device_status, sizeof word, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return from_cuda(e, "reading device status");
+  if (word == 0) return ok();
+  if (word & PA_DEVFLAG_TIMEOUT)
+    return fail(PA_ERR_DEVICE_TIMEOUT, "device status 0x%x: a pipeline wait timed out", word);
+  return fail(PA_ERR_DEVICE_INDEX, "device status 0x%x:%s%s%s", word,
+              (word & PA_DEVFLAG_BAD_BLOCK) ? " bad block id" : "",
+              (word & PA_DEVFLAG_BAD_SLOT) ? " slot beyond pool" : "",
+              (word & PA_DEVFLAG_BAD_CONTEXT) ? " bad context length" : "");
+}
+
+const char* pa_status_string(pa_status status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported shape";
+    case PA_ERR_CUDA: return "CUDA runtime error";
+    case PA_ERR_WORKSPACE: return "workspace missing or too small";
+    case PA_ERR_DEVICE_INDEX: return "device reported a bad index";
+    case PA_ERR_DEVICE_TIMEOUT: return "device reported a wait timeout";
+  }
+  return "unknown status";
+}
+
+const char* pa_last_error(void) { return g_last_error; }
+
+}  // extern "C"

@@ -1,0 +1,697 @@
+// Paged decode attention with online softmax and a balanced split-KV merge.
+//
+// What is computed ("vLLM", blog.rlaisqls.com, sections PagedAttention and Flash
+// Attention; "tiny-vllm (1)", geonuchoi.com, section 2 GQA): for every sequence s and
+// query head h, out = softmax(scale * q K^T) V over the context_lens[s] cached tokens,
+// where K/V are reached through the block table and query head h reads K/V head
+// h / GROUP.  Blocks are processed one at a time with a running max and running sum, so
+// no score vector is ever stored.
+//
+// GB300 design (decode is HBM-bound: each (block, kv head) tile of 2 KiB of K + 2 KiB of
+// V is read once and feeds 4 query heads):
+//   * The flattened space of (sequence, kv head, block) tiles is cut into one contiguous
+//     run per CTA, of equal length (or of `chunk` tiles when the caller fixes the
+//     partition), so every SM streams the same number of bytes whatever the length mix.
+//   * One producer warp walks the run, reads the block-table entries 32 at a time and
+//     issues cp.async.bulk (TMA, non-tensor) copies of each K and V tile into an NSTAGES
+//     ring in shared memory, completing on per-stage mbarriers; consumer warps take tiles
+//     round-robin.
+//   * Consumer lane (tg, dq) owns token tg and tg+8 of a tile and a quarter of the 64
+//     dims; q for all GROUP heads stays in registers (pre-scaled by scale*log2 e), the
+//     4-lane dot product is finished with two shuffles, and each lane keeps its own
+//     online-softmax state (max, sum, output slice), rescaled only when the max grows by
+//     more than 2^8, so the per-token cost is FMAs, one exp2 and no cross-lane reduction.
+//   * At the end of a run piece the lanes and warps are merged (log-sum-exp weights) and
+//     either the final bf16 row is written (whole sequence in one CTA) or an unnormalised
+//     (o, max, sum) partial, which merge_partials_kernel combines.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kNumConsumerWarps = 4;
+constexpr int kNumStages = 8;
+constexpr int kPartialFloats = kHeadDim + 2;  // o[64], max (log2 units), sum
+constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale when max grows > 2^8
+constexpr int kMinTilesPerCta = 4;
+constexpr int kMaxSeqs = 8192;
+constexpr int kMergeThreads = 256;
+
+struct KParams {
+  __nv_bfloat16* out;
+  const __nv_bfloat16* q;
+  const uint8_t* key_cache;
+  const uint8_t* value_cache;
+  const int32_t* block_tables;
+  int32_t max_blocks_per_seq;
+  const int32_t* context_lens;
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t num_blocks;
+  float q_scale;  // scale * log2(e): scores come out in log2 units
+  int32_t grid;
+  int32_t chunk;  // tiles per CTA, 0 = balanced split
+  int64_t* ws_total;    // total tiles, written by CTA 0
+  int32_t* ws_seq_base; // [num_seqs + 1] blocks-per-head prefix, written by CTA 0
+  float* partials;      // [grid][2][GROUP][kPartialFloats]
+  int32_t* status;
+};
+
+__device__ __forceinline__ int64_t run_start(int64_t c, int64_t total, int32_t grid,
+                                             int32_t chunk) {
+  if (chunk > 0) return c * chunk < total ? c * chunk : total;
+  return c * total / grid;
+}
+
+// CTA whose run contains tile x (x < total).  Runs are [run_start(c), run_start(c+1)).
+__device__ __forceinline__ int64_t run_of(int64_t x, int64_t total, int32_t grid,
+                                          int32_t chunk) {
+  if (chunk > 0) return x / chunk;
+  return ((x + 1) * grid - 1) / total;
+}
+
+// Largest s in [0, num_seqs) with kv * base[s] <= y (y < kv * base[num_seqs]).
+__device__ __forceinline__ int find_seq(const int32_t* base, int num_seqs, int64_t y, int kv) {
+  int lo = 0, hi = num_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (static_cast<int64_t>(base[mid]) * kv <= y) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+struct Piece {
+  int s, g, b0, b1, nb;
+};
+
+__device__ __forceinline__ Piece piece_at(const int32_t* base, int num_seqs, int kv, int64_t y,
+                                          int64_t run_end) {
+  Piece pc;
+  pc.s = find_seq(base, num_seqs, y, kv);
+  pc.nb = base[pc.s + 1] - base[pc.s];
+  const int64_t off = y - static_cast<int64_t>(base[pc.s]) * kv;
+  pc.g = static_cast<int>(off / pc.nb);
+  pc.b0 = static_cast<int>(off % pc.nb);
+  const int64_t left = run_end - y;
+  pc.b1 = (pc.nb - pc.b0 <= left) ? pc.nb : pc.b0 + static_cast<int>(left);
+  return pc;
+}
+
+// Process one 16-token tile pair held in shared memory.  Lane (tg, dq) handles tokens tg
+// and tg + 8; its 16 dims are the 16-byte chunks c0 (set 0) and c1 (set 1) of each row.
+template <int GROUP, bool TAIL>
+__device__ __forceinline__ void attend_tile(const uint8_t* __restrict__ kt,
+                                            const uint8_t* __restrict__ vt, int tg, int c0,
+                                            int c1, int valid_tokens,
+                                            const float2 (&qf)[GROUP][8], float (&m)[GROUP],
+                                            float (&l)[GROUP], float2 (&o)[GROUP][8]) {
+#pragma unroll
+  for (int step = 0; step < 2; ++step) {
+    const int t = tg + 8 * step;
+    const uint8_t* krow = kt + t * kRowBytes;
+    const uint4 ka = lds128(krow + c0 * 16);
+    const uint4 kb = lds128(krow + c1 * 16);
+    const float2 kf[8] = {bf16x2_to_float2(ka.x), bf16x2_to_float2(ka.y),
+                          bf16x2_to_float2(ka.z), bf16x2_to_float2(ka.w),
+                          bf16x2_to_float2(kb.x), bf16x2_to_float2(kb.y),
+                          bf16x2_to_float2(kb.z), bf16x2_to_float2(kb.w)};
+    float sc[GROUP];
+#pragma unroll
+    for (int h = 0; h < GROUP; ++h) {
+      float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc = __ffma2_rn(qf[h][i], kf[i], acc);
+      sc[h] = acc.x + acc.y;
+    }
+#pragma unroll
+    for (int h = 0; h < GROUP; ++h) sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], 1);
+#pragma unroll
+    for (int h = 0; h < GROUP; ++h) sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], 2);
+    const bool valid = !TAIL || t < valid_tokens;
+    float dlt[GROUP];
+    bool grow = false;
+#pragma unroll
+    for (int h = 0; h < GROUP; ++h) {
+      if (TAIL && !valid) sc[h] = -INFINITY;
+      dlt[h] = sc[h] - m[h];
+      grow |= dlt[h] > kRescaleThreshold;
+    }
+    if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+      for (int h = 0; h < GROUP; ++h) {
+        if (dlt[h] > kRescaleThreshold) {
+          const float a = fast_exp2(m[h] - sc[h]);
+          l[h] *= a;
+          const float2 aa = make_float2(a, a);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) o[h][i] = __fmul2_rn(o[h][i], aa);
+          m[h] = sc[h];
+          dlt[h] = 0.f;
+        }
+      }
+    }
+    float pr[GROUP];
+#pragma unroll
+    for (int h = 0; h < GROUP; ++h) {
+      pr[h] = fast_exp2(dlt[h]);
+      if (TAIL && !valid) pr[h] = 0.f;
+      l[h] += pr[h];
+    }
+    const uint8_t* vrow = vt + t * kRowBytes;
+    uint4 va = lds128(vrow + c0 * 16);
+    uint4 vb = lds128(vrow + c1 * 16);
+    if (TAIL && !valid) {  // unused slots may hold anything (NaN included): never multiply
+      va = make_uint4(0, 0, 0, 0);
+      vb = make_uint4(0, 0, 0, 0);
+    }
+    const float2 vf[8] = {bf16x2_to_float2(va.x), bf16x2_to_float2(va.y),
+                          bf16x2_to_float2(va.z), bf16x2_to_float2(va.w),
+                          bf16x2_to_float2(vb.x), bf16x2_to_float2(vb.y),
+                          bf16x2_to_float2(vb.z), bf16x2_to_float2(vb.w)};
+#pragma unroll
+    for (int h = 0; h < GROUP; ++h) {
+      const float2 pp = make_float2(pr[h], pr[h]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[h][i] = __ffma2_rn(pp, vf[i], o[h][i]);
+    }
+  }
+}
+
+template <int GROUP>
+constexpr size_t decode_smem_fixed() {
+  return static_cast<size_t>(kNumStages) * 2 * kTileBytes  // K+V ring
+         + 2 * kNumStages * sizeof(uint64_t)               // full / empty barriers
+         + sizeof(float) * kNumConsumerWarps * GROUP * (2 + kHeadDim);  // merge scratch
+}
+
+template <int GROUP>
+__global__ void __launch_bounds__((kNumConsumerWarps + 1) * 32, 1)
+paged_decode_kernel(const KParams p) {
+  static_assert(kNumStages % kNumConsumerWarps == 0, "stage ring must cycle per warp");
+  constexpr int kThreads = (kNumConsumerWarps + 1) * 32;
+  constexpr int kConsumerThreads = kNumConsumerWarps * 32;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kNumStages * 2 * kTileBytes);
+  uint64_t* empty_bar = full_bar + kNumStages;
+  float* red_m = reinterpret_cast<float*>(empty_bar + kNumStages);  // [W][GROUP]
+  float* red_l = red_m + kNumConsumerWarps * GROUP;                  // [W][GROUP]
+  float* red_o = red_l + kNumConsumerWarps * GROUP;                  // [W][GROUP][64]
+  int32_t* seq_base = reinterpret_cast<int32_t*>(red_o + kNumConsumerWarps * GROUP * kHeadDim);
+  __shared__ int64_t warp_sums[kThreads / 32];
+  __shared__ volatile int abort_flag;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int S = p.num_seqs;
+  const int KV = p.num_kv_heads;
+
+  if (tid == 0) {
+    for (int i = 0; i < kNumStages; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    fence_barrier_init();
+    abort_flag = 0;
+  }
+
+  // ---- per-sequence block counts and their exclusive prefix (the tile index space) ----
+  for (int i = tid; i < S; i += kThreads) {
+    const int32_t L = p.context_lens[i];
+    int32_t nb = 0;
+    if (L < 0 || static_cast<int64_t>(L) > static_cast<int64_t>(p.max_blocks_per_seq) * kBlockSize) {
+      if (blockIdx.x == 0) flag_error(p.status, PA_DEVFLAG_BAD_CONTEXT);
+    } else {
+      nb = (L + kBlockSize - 1) / kBlockSize;
+    }
+    seq_base[i] = nb;
+  }
+  __syncthreads();
+  {
+    const int per = (S + kThreads - 1) / kThreads;
+    const int beg = min(tid * per, S);
+    const int end = min(beg + per, S);
+    int64_t local = 0;
+    for (int i = beg; i < end; ++i) local += seq_base[i];
+    int64_t incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int64_t v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    int64_t run = incl - local;
+    int64_t grand = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      if (w < warp) run += warp_sums[w];
+      grand += warp_sums[w];
+    }
+    const bool overflow = grand * KV > 0x7fffffffLL;
+    for (int i = beg; i < end; ++i) {
+      const int32_t v = seq_base[i];
+      seq_base[i] = static_cast<int32_t>(overflow ? 0 : run);
+      run += v;
+    }
+    if (tid == 0) seq_base[S] = static_cast<int32_t>(overflow ? 0 : grand);
+    if (overflow && tid == 0 && blockIdx.x == 0) flag_error(p.status, PA_DEVFLAG_BAD_CONTEXT);
+  }
+  __syncthreads();
+
+  const int64_t total = static_cast<int64_t>(seq_base[S]) * KV;
+  if (blockIdx.x == 0) {
+    for (int i = tid; i <= S; i += kThreads) p.ws_seq_base[i] = seq_base[i];
+    if (tid == 0) {
+      *p.ws_total = total;
+      if (p.chunk > 0 && static_cast<int64_t>(p.grid) * p.chunk < total)
+        flag_error(p.status, PA_DEVFLAG_BAD_CONTEXT);  // contexts beyond max_context_len
+    }
+  }
+  const int64_t start = run_start(blockIdx.x, total, p.grid, p.chunk);
+  const int64_t stop = run_start(static_cast<int64_t>(blockIdx.x) + 1, total, p.grid, p.chunk);
+  if (start >= stop) return;
+
+  if (warp == kNumConsumerWarps) {
+    // =============================== producer warp ===============================
+    const uint64_t policy = l2_evict_first_policy();
+    int64_t y = start;
+    int64_t rc = 0;  // tiles issued so far by this CTA
+    bool ok = true;
+    while (y < stop && ok) {
+      const Piece pc = piece_at(seq_base, S, KV, y, stop);
+      const int32_t* row = p.block_tables + static_cast<int64_t>(pc.s) * p.max_blocks_per_seq;
+      for (int bb = pc.b0; bb < pc.b1 && ok; bb += 32) {
+        const int n = min(32, pc.b1 - bb);
+        const int32_t phys = lane < n ? __ldg(row + bb + lane) : 0;
+        const bool bad = lane < n && (phys < 0 || phys >= p.num_blocks);
+        if (__any_sync(0xffffffffu, bad) && lane == 0) flag_error(p.status, PA_DEVFLAG_BAD_BLOCK);
+        for (int j = 0; j < n; ++j, ++rc) {
+          const int32_t pj = __shfl_sync(0xffffffffu, phys, j);
+          if (lane == 0) {
+            const int st = static_cast<int>(rc % kNumStages);
+            const uint32_t parity = static_cast<uint32_t>((rc / kNumStages) & 1) ^ 1u;
+            if (abort_flag || !mbar_wait(&empty_bar[st], parity)) {
+              if (!abort_flag) flag_error(p.status, PA_DEVFLAG_TIMEOUT);
+              abort_flag = 1;
+              ok = false;
+            } else if (pj < 0 || pj >= p.num_blocks) {
+              mbar_arrive(&full_bar[st]);  // release the stage; its data is stale
+            } else {
+              mbar_arrive_expect_tx(&full_bar[st], 2 * kTileBytes);
+              const size_t off = (static_cast<size_t>(pj) * KV + pc.g) * kTileBytes;
+              uint8_t* dst = ring + st * 2 * kTileBytes;
+              bulk_copy_g2s(dst, p.key_cache + off, kTileBytes, &full_bar[st], policy);
+              bulk_copy_g2s(dst + kTileBytes, p.value_cache + off, kTileBytes, &full_bar[st],
+                            policy);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+        }
+      }
+      y += pc.b1 - pc.b0;
+    }
+    // Do not leave copies in flight into shared memory: wait (bounded) for the most
+    // recent fill of every stage that was issued.
+    if (lane == 0) {
+      for (int st = 0; st < kNumStages; ++st) {
+        if (rc <= st) break;
+        const int64_t last = st + ((rc - 1 - st) / kNumStages) * kNumStages;
+        if (!mbar_wait(&full_bar[st], static_cast<uint32_t>((last / kNumStages) & 1))) {
+          flag_error(p.status, PA_DEVFLAG_TIMEOUT);
+        }
+      }
+    }
+    return;
+  }
+
+  // =============================== consumer warps ================================
+  const int tg = lane >> 2;
+  const int dq = lane & 3;
+  const int par = tg & 1;
+  const int c0 = dq + 4 * par;        // 16-byte chunk held in register set 0
+  const int c1 = dq + 4 * (par ^ 1);  // 16-byte chunk held in register set 1
+  int64_t y = start;
+  while (y < stop) {
+    const Piece pc = piece_at(seq_base, S, KV, y, stop);
+    const int32_t L = p.context_lens[pc.s];
+    const bool whole = pc.b0 == 0 && pc.b1 == pc.nb;
+    const bool first_piece = y == start;
+    const int64_t rc0 = y - start;
+    const int ntiles = pc.b1 - pc.b0;
+
+    float2 qf[GROUP][8];
+#pragma unroll
+    for (int h = 0; h < GROUP; ++h) {
+      const __nv_bfloat16* qrow =
+          p.q + (static_cast<int64_t>(pc.s) * p.num_q_heads + pc.g * GROUP + h) * kHeadDim;
+      const uint4 a = ldg_nc128(qrow + c0 * 8);
+      const uint4 b = ldg_nc128(qrow + c1 * 8);
+      const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float2 f = bf16x2_to_float2(w[i]);
+        qf[h][i] = make_float2(f.x * p.q_scale, f.y * p.q_scale);
+      }
+    }
+    float m[GROUP], l[GROUP];
+    float2 o[GROUP][8];
+#pragma unroll
+    for (int h = 0; h < GROUP; ++h) {
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[h][i] = make_float2(0.f, 0.f);
+    }
+
+    const int first_k = static_cast<int>(((warp - rc0) % kNumConsumerWarps + kNumConsumerWarps) %
+                                         kNumConsumerWarps);
+    for (int k = first_k; k < ntiles; k += kNumConsumerWarps) {
+      const int64_t rc = rc0 + k;
+      const int st = static_cast<int>(rc % kNumStages);
+      if (abort_flag) break;
+      if (!mbar_wait(&full_bar[st], static_cast<uint32_t>((rc / kNumStages) & 1))) {
+        if (lane == 0) flag_error(p.status, PA_DEVFLAG_TIMEOUT);
+        abort_flag = 1;
+        break;
+      }
+      const uint8_t* kt = ring + st * 2 * kTileBytes;
+      const uint8_t* vt = kt + kTileBytes;
+      const int b = pc.b0 + k;
+      const int valid = L - b * kBlockSize;
+      if (valid >= kBlockSize) {
+        attend_tile<GROUP, false>(kt, vt, tg, c0, c1, kBlockSize, qf, m, l, o);
+      } else {
+        attend_tile<GROUP, true>(kt, vt, tg, c0, c1, valid, qf, m, l, o);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[st]);
+    }
+
+    // ---- merge the 32 (warp, token-group) online-softmax states of this piece ----
+    float mx[GROUP];
+#pragma unroll
+    for (int h = 0; h < GROUP; ++h) {
+      mx[h] = m[h];
+      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 4));
+      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 8));
+      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 16));
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int h = 0; h < GROUP; ++h) red_m[warp * GROUP + h] = mx[h];
+    }
+    named_barrier_sync(1, kConsumerThreads);
+    float M[GROUP];
+#pragma unroll
+    for (int h = 0; h < GROUP; ++h) {
+      M[h] = red_m[h];
+#pragma unroll
+      for (int w = 1; w < kNumConsumerWarps; ++w) M[h] = fmaxf(M[h], red_m[w * GROUP + h]);
+      const float f = m[h] == -INFINITY ? 0.f : fast_exp2(m[h] - M[h]);
+      l[h] *= f;
+      const float2 ff = make_float2(f, f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[h][i] = __fmul2_rn(o[h][i], ff);
+      if (par) {  // odd token groups hold chunk dq+4 in set 0: align before summing
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 tmp = o[h][i];
+          o[h][i] = o[h][i + 4];
+          o[h][i + 4] = tmp;
+        }
+      }
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          o[h][i].x += __shfl_xor_sync(0xffffffffu, o[h][i].x, off);
+          o[h][i].y += __shfl_xor_sync(0xffffffffu, o[h][i].y, off);
+        }
+      }
+    }
+    if (tg == 0) {
+#pragma unroll
+      for (int h = 0; h < GROUP; ++h) {
+        float* dst = red_o + (warp * GROUP + h) * kHeadDim;
+        float4* lo = reinterpret_cast<float4*>(dst + 8 * dq);
+        float4* hi = reinterpret_cast<float4*>(dst + 8 * (dq + 4));
+        lo[0] = make_float4(o[h][0].x, o[h][0].y, o[h][1].x, o[h][1].y);
+        lo[1] = make_float4(o[h][2].x, o[h][2].y, o[h][3].x, o[h][3].y);
+        hi[0] = make_float4(o[h][4].x, o[h][4].y, o[h][5].x, o[h][5].y);
+        hi[1] = make_float4(o[h][6].x, o[h][6].y, o[h][7].x, o[h][7].y);
+        if (dq == 0) red_l[warp * GROUP + h] = l[h];
+      }
+    }
+    named_barrier_sync(1, kConsumerThreads);
+    for (int e = tid; e < GROUP * kHeadDim; e += kConsumerThreads) {
+      const int h = e / kHeadDim;
+      const int d = e % kHeadDim;
+      float acc = 0.f, lsum = 0.f;
+#pragma unroll
+      for (int w = 0; w < kNumConsumerWarps; ++w) {
+        acc += red_o[(w * GROUP + h) * kHeadDim + d];
+        lsum += red_l[w * GROUP + h];
+      }
+      if (whole) {
+        const int64_t row = static_cast<int64_t>(pc.s) * p.num_q_heads + pc.g * GROUP + h;
+        p.out[row * kHeadDim + d] = __float2bfloat16_rn(acc / lsum);
+      } else {
+        const int slot = first_piece ? 0 : 1;
+        float* dst = p.partials +
+                     ((static_cast<int64_t>(blockIdx.x) * 2 + slot) * GROUP + h) * kPartialFloats;
+        dst[d] = acc;
+        if (d == 0) {
+          dst[kHeadDim] = M[h];
+          dst[kHeadDim + 1] = lsum;
+        }
+      }
+    }
+    named_barrier_sync(1, kConsumerThreads);  // scratch is reused by the next piece
+    y += ntiles;
+  }
+}
+
+// Combines the partials of every (sequence, kv head) whose tiles were split across CTAs,
+// and writes zero rows for empty contexts.  One CTA per (kv head, sequence).
+template <int GROUP>
+__global__ void __launch_bounds__(kMergeThreads)
+merge_partials_kernel(const KParams p) {
+  constexpr int kWarps = kMergeThreads / 32;
+  __shared__ float red_m[kWarps][GROUP];
+  __shared__ float red_l[kWarps][GROUP];
+  __shared__ float red_o[kWarps][GROUP][kHeadDim];
+  __shared__ float s_M[GROUP];
+  const int g = blockIdx.x;
+  const int s = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int KV = p.num_kv_heads;
+  __nv_bfloat16* out = p.out + (static_cast<int64_t>(s) * p.num_q_heads + g * GROUP) * kHeadDim;
+  const int32_t base = p.ws_seq_base[s];
+  const int nb = p.ws_seq_base[s + 1] - base;
+  if (nb == 0) {
+    for (int e = tid; e < GROUP * kHeadDim; e += kMergeThreads) out[e] = __float2bfloat16_rn(0.f);
+    return;
+  }
+  const int64_t total = *p.ws_total;
+  const int64_t x0 = static_cast<int64_t>(base) * KV + static_cast<int64_t>(g) * nb;
+  const int64_t x1 = x0 + nb;
+  const int64_t c_first = run_of(x0, total, p.grid, p.chunk);
+  const int64_t c_last = run_of(x1 - 1, total, p.grid, p.chunk);
+  if (c_last >= p.grid) {  // tiles beyond the grid (contexts above max_context_len)
+    if (tid == 0) flag_error(p.status, PA_DEVFLAG_BAD_CONTEXT);
+    return;
+  }
+  if (c_first == c_last) return;  // written directly by the attention kernel
+  const int n = static_cast<int>(c_last - c_first + 1);
+  const int first_slot = x0 == run_start(c_first, total, p.grid, p.chunk) ? 0 : 1;
+
+  auto record = [&](int k, int h) -> const float* {
+    const int64_t c = c_first + k;
+    const int slot = k == 0 ? first_slot : 0;
+    return p.partials + ((c * 2 + slot) * GROUP + h) * kPartialFloats;
+  };
+  auto empty_run = [&](int k) -> bool {
+    const int64_t c = c_first + k;
+    return run_start(c, total, p.grid, p.chunk) == run_start(c + 1, total, p.grid, p.chunk);
+  };
+
+  float mloc[GROUP];
+#pragma unroll
+  for (int h = 0; h < GROUP; ++h) mloc[h] = -INFINITY;
+  for (int k = tid; k < n; k += kMergeThreads) {
+    if (empty_run(k)) continue;
+#pragma unroll
+    for (int h = 0; h < GROUP; ++h) mloc[h] = fmaxf(mloc[h], record(k, h)[kHeadDim]);
+  }
+#pragma unroll
+  for (int h = 0; h < GROUP; ++h) {
+    for (int off = 16; off > 0; off >>= 1)
+      mloc[h] = fmaxf(mloc[h], __shfl_xor_sync(0xffffffffu, mloc[h], off));
+    if (lane == 0) red_m[warp][h] = mloc[h];
+  }
+  __syncthreads();
+  if (tid < GROUP) {
+    float v = red_m[0][tid];
+    for (int w = 1; w < kWarps; ++w) v = fmaxf(v, red_m[w][tid]);
+    s_M[tid] = v;
+  }
+  __syncthreads();
+
+  float2 acc[GROUP];
+  float lacc[GROUP];
+#pragma unroll
+  for (int h = 0; h < GROUP; ++h) {
+    acc[h] = make_float2(0.f, 0.f);
+    lacc[h] = 0.f;
+  }
+  for (int k = warp; k < n; k += kWarps) {
+    if (empty_run(k)) continue;
+#pragma unroll
+    for (int h = 0; h < GROUP; ++h) {
+      const float* r = record(k, h);
+      const float wgt = fast_exp2(r[kHeadDim] - s_M[h]);
+      lacc[h] += wgt * r[kHeadDim + 1];
+      const float2 v = *reinterpret_cast<const float2*>(r + 2 * lane);
+      acc[h].x += wgt * v.x;
+      acc[h].y += wgt * v.y;
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < GROUP; ++h) {
+    red_o[warp][h][2 * lane] = acc[h].x;
+    red_o[warp][h][2 * lane + 1] = acc[h].y;
+    if (lane == 0) red_l[warp][h] = lacc[h];
+  }
+  __syncthreads();
+  for (int e = tid; e < GROUP * kHeadDim; e += kMergeThreads) {
+    const int h = e / kHeadDim;
+    const int d = e % kHeadDim;
+    float o = 0.f, lsum = 0.f;
+    for (int w = 0; w < kWarps; ++w) {
+      o += red_o[w][h][d];
+      lsum += red_l[w][h];
+    }
+    out[e] = __float2bfloat16_rn(o / lsum);
+  }
+}
+
+template <int GROUP>
+size_t smem_bytes(int num_seqs) {
+  return decode_smem_fixed<GROUP>() + sizeof(int32_t) * (num_seqs + 1);
+}
+
+template <int GROUP>
+cudaError_t prepare_kernel() {
+  static bool done = false;  // benign race: the attribute call is idempotent
+  if (done) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<GROUP>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem_bytes<GROUP>(kMaxSeqs)));
+  if (e == cudaSuccess) done = true;
+  return e;
+}
+
+template <int GROUP>
+cudaError_t occupancy(int num_seqs, int* ctas_per_sm) {
+  cudaError_t e = prepare_kernel<GROUP>();
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      ctas_per_sm, paged_decode_kernel<GROUP>, (kNumConsumerWarps + 1) * 32,
+      smem_bytes<GROUP>(num_seqs));
+}
+
+template <int GROUP>
+cudaError_t launch(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
+  cudaError_t e = prepare_kernel<GROUP>();
+  if (e != cudaSuccess) return e;
+  KParams p;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.key_cache = static_cast<const uint8_t*>(a.key_cache);
+  p.value_cache = static_cast<const uint8_t*>(a.value_cache);
+  p.block_tables = a.block_tables;
+  p.max_blocks_per_seq = a.max_blocks_per_seq;
+  p.context_lens = a.context_lens;
+  p.num_seqs = a.num_seqs;
+  p.num_q_heads = a.num_q_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.num_blocks = a.num_blocks;
+  p.q_scale = a.scale * 1.4426950408889634f;
+  p.grid = plan.grid;
+  p.chunk = plan.chunk;
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  p.ws_total = reinterpret_cast<int64_t*>(ws);
+  p.ws_seq_base = reinterpret_cast<int32_t*>(ws + 16);
+  p.partials = reinterpret_cast<float*>(ws + plan.ws_meta_bytes);
+  p.status = a.status;
+  paged_decode_kernel<GROUP><<<plan.grid, (kNumConsumerWarps + 1) * 32, plan.smem_bytes, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  merge_partials_kernel<GROUP><<<dim3(a.num_kv_heads, a.num_seqs), kMergeThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t plan_decode(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_heads,
+                        int32_t max_context_len, int32_t partition_tokens, DecodePlan* plan) {
+  const int group = num_q_heads / num_kv_heads;
+  plan->group = group;
+  int ctas_per_sm = 0;
+  cudaError_t e;
+  switch (group) {
+    case 1: e = occupancy<1>(num_seqs, &ctas_per_sm); plan->smem_bytes = smem_bytes<1>(num_seqs); break;
+    case 2: e = occupancy<2>(num_seqs, &ctas_per_sm); plan->smem_bytes = smem_bytes<2>(num_seqs); break;
+    case 4: e = occupancy<4>(num_seqs, &ctas_per_sm); plan->smem_bytes = smem_bytes<4>(num_seqs); break;
+    default: return cudaErrorInvalidValue;
+  }
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (ctas_per_sm < 1) return cudaErrorInvalidConfiguration;
+  const int64_t blocks_max = (static_cast<int64_t>(max_context_len) + kBlockSize - 1) / kBlockSize;
+  const int64_t tiles_upper = static_cast<int64_t>(num_seqs) * num_kv_heads * blocks_max;
+  int64_t grid;
+  if (partition_tokens > 0) {
+    plan->chunk = partition_tokens / kBlockSize;
+    grid = (tiles_upper + plan->chunk - 1) / plan->chunk;
+  } else {
+    plan->chunk = 0;
+    grid = static_cast<int64_t>(sms) * ctas_per_sm;
+    const int64_t by_size = (tiles_upper + kMinTilesPerCta - 1) / kMinTilesPerCta;
+    if (by_size < grid) grid = by_size;
+  }
+  if (grid < 1) grid = 1;
+  if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+  plan->grid = static_cast<int>(grid);
+  plan->ws_meta_bytes = (16 + sizeof(int32_t) * (num_seqs + 1) + 255) / 256 * 256;
+  plan->workspace_bytes = plan->ws_meta_bytes +
+                          static_cast<size_t>(grid) * 2 * group * kPartialFloats * sizeof(float);
+  return cudaSuccess;
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
+  switch (plan.group) {
+    case 1: return launch<1>(a, plan, stream);
+    case 2: return launch<2>(a, plan, stream);
+    case 4: return launch<4>(a, plan, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int decode_max_seqs() { return kMaxSeqs; }
+
+}  // namespace pkv

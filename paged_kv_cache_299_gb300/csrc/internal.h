@@ -1,0 +1,76 @@
+// Host-side launchers shared between the C-ABI entry points (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pagedkv.h"
+
+namespace pkv {
+
+cudaError_t launch_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* context_lens, const int32_t* query_start_loc,
+                                int32_t num_seqs, int32_t num_tokens, int32_t num_blocks,
+                                int64_t* slot_mapping, int32_t* status, cudaStream_t stream);
+
+cudaError_t launch_reshape_and_cache(const void* key, const void* value,
+                                     const int64_t* slot_mapping, int32_t num_tokens,
+                                     void* key_cache, void* value_cache, int32_t num_blocks,
+                                     int32_t num_kv_heads, int32_t* status,
+                                     cudaStream_t stream);
+
+// Work decomposition of one pa_decode call (identical in the size query and the call).
+struct DecodePlan {
+  int group;          // q heads per kv head
+  int grid;           // CTAs of the attention kernel
+  int chunk;          // tiles per CTA (fixed mode), 0 = balanced split of the real total
+  size_t smem_bytes;  // dynamic shared memory of the attention kernel
+  size_t ws_meta_bytes;      // offset of the partials inside the workspace
+  size_t workspace_bytes;    // total workspace
+};
+
+// Returns cudaSuccess and fills `plan`, or an error (e.g. no device).
+cudaError_t plan_decode(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_heads,
+                        int32_t max_context_len, int32_t partition_tokens, DecodePlan* plan);
+
+struct DecodeArgs {
+  void* out;
+  const void* q;
+  const void* key_cache;
+  const void* value_cache;
+  const int32_t* block_tables;
+  int32_t max_blocks_per_seq;
+  const int32_t* context_lens;
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t num_blocks;
+  float scale;
+  void* workspace;
+  int32_t* status;
+};
+
+cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream);
+
+struct PrefillArgs {
+  void* out;
+  const void* q;
+  const int32_t* query_start_loc;
+  int32_t max_query_len;
+  const void* key_cache;
+  const void* value_cache;
+  int32_t num_blocks;
+  int32_t num_kv_heads;
+  const int32_t* block_tables;
+  int32_t max_blocks_per_seq;
+  const int32_t* context_lens;
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  float scale;
+  int32_t* status;
+};
+
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+
+}  // namespace pkv

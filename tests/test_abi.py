@@ -1,0 +1,87 @@
+"""The C-ABI library builds for sm_103a, loads, exports every symbol the header declares,
+and rejects bad arguments on the host (these calls return before any CUDA call, so they
+run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_299_gb300 import binding as pa
+from paged_kv_cache_299_gb300 import build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "pagedkv.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_library_builds_and_exports_every_declared_symbol():
+    lib = pa.load()
+    names = declared_functions()
+    assert set(names) == set(pa.EXPORTED)
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings():
+    lib = pa.load()
+    for code in range(-6, 1):
+        assert lib.pa_status_string(code)
+    assert lib.pa_status_string(-99) == b"unknown status"
+
+
+def _desc(nb=4, hkv=8, d=64, bs=16):
+    return pa.CacheDesc(nb, hkv, d, bs)
+
+
+def test_host_rejects_bad_arguments_without_touching_the_device():
+    lib = pa.load()
+    P = ctypes.c_void_p
+    fake = P(0x1000)  # never dereferenced: every call below fails its host checks first
+    # unsupported head_dim / block_size
+    assert lib.pa_reshape_and_cache(fake, fake, fake, 1, fake, fake, _desc(d=128), None,
+                                    None) == pa.PA_ERR_UNSUPPORTED
+    assert b"head_dim" in lib.pa_last_error()
+    assert lib.pa_reshape_and_cache(fake, fake, fake, 1, fake, fake, _desc(bs=32), None,
+                                    None) == pa.PA_ERR_UNSUPPORTED
+    # null pointers, misalignment, negative sizes
+    assert lib.pa_reshape_and_cache(None, fake, fake, 1, fake, fake, _desc(), None,
+                                    None) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_reshape_and_cache(P(0x1008), fake, fake, 1, fake, fake, _desc(), None,
+                                    None) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_reshape_and_cache(fake, fake, fake, -1, fake, fake, _desc(), None,
+                                    None) == pa.PA_ERR_INVALID_ARG
+    # empty calls succeed without launching
+    assert lib.pa_reshape_and_cache(None, None, None, 0, None, None, _desc(), None,
+                                    None) == pa.PA_OK
+    assert lib.pa_compute_slot_mapping(None, 1, None, None, 0, 0, _desc(), None, None,
+                                       None) == pa.PA_OK
+    assert lib.pa_compute_slot_mapping(fake, 1, fake, None, 2, 3, _desc(), fake, None,
+                                       None) == pa.PA_ERR_INVALID_ARG
+    # decode: group of 3 unsupported, partition not a multiple of 16, too many sequences
+    args = [fake, fake, fake, fake, _desc(), fake, 4, fake]
+    assert lib.pa_decode(*args, 2, 24, ctypes.c_float(0.125), 64, 0, fake, 1 << 20, None,
+                         None) == pa.PA_ERR_UNSUPPORTED
+    assert lib.pa_decode(*args, 2, 32, ctypes.c_float(0.125), 64, 24, fake, 1 << 20, None,
+                         None) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_decode(*args, 10000, 32, ctypes.c_float(0.125), 64, 0, fake, 1 << 20, None,
+                         None) == pa.PA_ERR_UNSUPPORTED
+    assert lib.pa_decode(*args, 0, 32, ctypes.c_float(0.125), 64, 0, None, 0, None,
+                         None) == pa.PA_OK
+    assert lib.pa_decode(*args, 2, 32, ctypes.c_float(-1.0), 64, 0, fake, 1 << 20, None,
+                         None) == pa.PA_ERR_INVALID_ARG
+    # prefill needs group 4
+    assert lib.pa_prefill_chunk(fake, fake, fake, 8, fake, fake, _desc(), fake, 4, fake, 2, 8,
+                                ctypes.c_float(0.125), None, None) == pa.PA_ERR_UNSUPPORTED
+    assert lib.pa_decode_workspace_size(2, 8, 24, 64, 0) == 0
+    assert lib.pa_check_device_status(None, None) == pa.PA_ERR_INVALID_ARG
+
+
+def test_build_targets_sm103a_only():
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    assert os.path.exists(build.build())
