@@ -133,11 +133,14 @@ pa_status pa_decode(void* out, const void* q, const void* key_cache, const void*
  * query_start_loc[s+1] - query_start_loc[s] query rows, the last q_len of its
  * context_lens[s] tokens (already stored); row i sits at position L - q_len + i and
  * attends keys 0 .. L - q_len + i.  QK^T and PV run on tcgen05 tensor cores.
- *   out / q          bf16 [query_start_loc[num_seqs]][num_q_heads][D]
+ *   out / q          bf16 [num_query_tokens][num_q_heads][D]
+ *   num_query_tokens == query_start_loc[num_seqs], the rows of q and out (host-known;
+ *                    bounds the tensor-memory-access box reads of q)
  *   max_query_len    host-known upper bound of q_len (sizes the grid)
  * Requires num_q_heads / num_kv_heads == 4.  num_seqs == 0 is a no-op. */
 pa_status pa_prefill_chunk(void* out, const void* q, const int32_t* query_start_loc,
-                           int32_t max_query_len, const void* key_cache,
+                           int32_t num_query_tokens, int32_t max_query_len,
+                           const void* key_cache,
                            const void* value_cache, pa_cache_desc cd,
                            const int32_t* block_tables, int32_t max_blocks_per_seq,
                            const int32_t* context_lens, int32_t num_seqs,

@@ -69,8 +69,8 @@ def load(path: str | None = None):
     lib.pa_decode.argtypes = [P, P, P, P, CacheDesc, P, i32, P, i32, i32, f32, i32, i32, P, sz,
                               P, P]
     lib.pa_decode.restype = st
-    lib.pa_prefill_chunk.argtypes = [P, P, P, i32, P, P, CacheDesc, P, i32, P, i32, i32, f32, P,
-                                     P]
+    lib.pa_prefill_chunk.argtypes = [P, P, P, i32, i32, P, P, CacheDesc, P, i32, P, i32, i32,
+                                     f32, P, P]
     lib.pa_prefill_chunk.restype = st
     lib.pa_check_device_status.argtypes = [P, P]
     lib.pa_check_device_status.restype = st
@@ -208,7 +208,8 @@ def pa_prefill_chunk(out, q, query_start_loc, max_query_len, key_cache, value_ca
     if out.shape != q.shape or query_start_loc.shape[0] != num_seqs + 1 or \
             block_tables.shape[0] != num_seqs:
         raise ValueError("prefill argument shapes disagree")
-    st = load().pa_prefill_chunk(_ptr(out), _ptr(q), _ptr(query_start_loc), int(max_query_len),
+    st = load().pa_prefill_chunk(_ptr(out), _ptr(q), _ptr(query_start_loc), q.shape[0],
+                                 int(max_query_len),
                                  _ptr(key_cache), _ptr(value_cache), cache_desc(key_cache),
                                  _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
                                  num_seqs, q.shape[1], float(scale), _ptr(device_status),

@@ -171,7 +171,8 @@ pa_status pa_decode(void* out, const void* q, const void* key_cache, const void*
 }
 
 pa_status pa_prefill_chunk(void* out, const void* q, const int32_t* query_start_loc,
-                           int32_t max_query_len, const void* key_cache,
+                           int32_t num_query_tokens, int32_t max_query_len,
+                           const void* key_cache,
                            const void* value_cache, pa_cache_desc cd,
                            const int32_t* block_tables, int32_t max_blocks_per_seq,
                            const int32_t* context_lens, int32_t num_seqs,
@@ -179,10 +180,14 @@ pa_status pa_prefill_chunk(void* out, const void* q, const int32_t* query_start_
                            pa_stream_t stream) {
   pa_status st = check_desc(cd);
   if (st != PA_OK) return st;
-  if (num_seqs < 0 || max_query_len < 0 || max_blocks_per_seq <= 0)
-    return fail(PA_ERR_INVALID_ARG, "num_seqs %d, max_query_len %d, max_blocks_per_seq %d",
-                num_seqs, max_query_len, max_blocks_per_seq);
-  if (num_seqs == 0 || max_query_len == 0) return ok();
+  if (num_seqs < 0 || max_query_len < 0 || num_query_tokens < 0 || max_blocks_per_seq <= 0)
+    return fail(PA_ERR_INVALID_ARG,
+                "num_seqs %d, num_query_tokens %d, max_query_len %d, max_blocks_per_seq %d",
+                num_seqs, num_query_tokens, max_query_len, max_blocks_per_seq);
+  if (num_seqs == 0 || max_query_len == 0 || num_query_tokens == 0) return ok();
+  if (max_query_len > num_query_tokens)
+    return fail(PA_ERR_INVALID_ARG, "max_query_len %d > num_query_tokens %d", max_query_len,
+                num_query_tokens);
   if (num_q_heads != 4 * cd.num_kv_heads)
     return fail(PA_ERR_UNSUPPORTED, "prefill needs 4 query heads per kv head (got %d / %d)",
                 num_q_heads, cd.num_kv_heads);
@@ -196,6 +201,7 @@ pa_status pa_prefill_chunk(void* out, const void* q, const int32_t* query_start_
   a.out = out;
   a.q = q;
   a.query_start_loc = query_start_loc;
+  a.num_query_tokens = num_query_tokens;
   a.max_query_len = max_query_len;
   a.key_cache = key_cache;
   a.value_cache = value_cache;

@@ -33,8 +33,8 @@ namespace pkv {
 
 namespace {
 
-constexpr int kNumConsumerWarps = 4;
-constexpr int kNumStages = 8;
+constexpr int kNumConsumerWarps = 7;  // + 1 producer = 8 warps, 2 per SM sub-partition
+constexpr int kNumStages = 28;     // multiple of kNumConsumerWarps; 112 KiB in flight
 constexpr int kPartialFloats = kHeadDim + 2;  // o[64], max (log2 units), sum
 constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale when max grows > 2^8
 constexpr int kMinTilesPerCta = 4;
@@ -54,11 +54,11 @@ struct KParams {
   int32_t num_kv_heads;
   int32_t num_blocks;
   float q_scale;  // scale * log2(e): scores come out in log2 units
-  int32_t grid;
-  int32_t chunk;  // tiles per CTA, 0 = balanced split
+  int32_t grid;      // runs of the decomposition (balanced mode: one per CTA)
+  int32_t chunk;     // tiles per run, 0 = balanced split into `grid` runs
   int64_t* ws_total;    // total tiles, written by CTA 0
   int32_t* ws_seq_base; // [num_seqs + 1] blocks-per-head prefix, written by CTA 0
-  float* partials;      // [grid][2][GROUP][kPartialFloats]
+  float* partials;      // [runs][2][GROUP][kPartialFloats]
   int32_t* status;
 };
 
@@ -68,7 +68,7 @@ __device__ __forceinline__ int64_t run_start(int64_t c, int64_t total, int32_t g
   return c * total / grid;
 }
 
-// CTA whose run contains tile x (x < total).  Runs are [run_start(c), run_start(c+1)).
+// Run containing tile x (x < total).  Runs are [run_start(c), run_start(c+1)).
 __device__ __forceinline__ int64_t run_of(int64_t x, int64_t total, int32_t grid,
                                           int32_t chunk) {
   if (chunk > 0) return x / chunk;
@@ -273,17 +273,18 @@ paged_decode_kernel(const KParams p) {
         flag_error(p.status, PA_DEVFLAG_BAD_CONTEXT);  // contexts beyond max_context_len
     }
   }
-  const int64_t start = run_start(blockIdx.x, total, p.grid, p.chunk);
-  const int64_t stop = run_start(static_cast<int64_t>(blockIdx.x) + 1, total, p.grid, p.chunk);
-  if (start >= stop) return;
+  // This CTA serves runs blockIdx.x, blockIdx.x + gridDim.x, ... (persistent); the
+  // producer and the consumers walk the same sequence of runs and pieces.
+  if (run_start(blockIdx.x, total, p.grid, p.chunk) >= total) return;
 
   if (warp == kNumConsumerWarps) {
     // =============================== producer warp ===============================
     const uint64_t policy = l2_evict_first_policy();
-    int64_t y = start;
     int64_t rc = 0;  // tiles issued so far by this CTA
     bool ok = true;
-    while (y < stop && ok) {
+    for (int64_t run = blockIdx.x; run < p.grid && ok; run += gridDim.x) {
+    const int64_t stop = run_start(run + 1, total, p.grid, p.chunk);
+    for (int64_t y = run_start(run, total, p.grid, p.chunk); y < stop && ok;) {
       const Piece pc = piece_at(seq_base, S, KV, y, stop);
       const int32_t* row = p.block_tables + static_cast<int64_t>(pc.s) * p.max_blocks_per_seq;
       for (int bb = pc.b0; bb < pc.b1 && ok; bb += 32) {
@@ -317,6 +318,7 @@ paged_decode_kernel(const KParams p) {
       }
       y += pc.b1 - pc.b0;
     }
+    }
     // Do not leave copies in flight into shared memory: wait (bounded) for the most
     // recent fill of every stage that was issued.
     if (lane == 0) {
@@ -337,13 +339,16 @@ paged_decode_kernel(const KParams p) {
   const int par = tg & 1;
   const int c0 = dq + 4 * par;        // 16-byte chunk held in register set 0
   const int c1 = dq + 4 * (par ^ 1);  // 16-byte chunk held in register set 1
-  int64_t y = start;
-  while (y < stop) {
+  int64_t done = 0;  // tiles consumed so far by this CTA (the producer's running count)
+  for (int64_t run = blockIdx.x; run < p.grid; run += gridDim.x) {
+  const int64_t start = run_start(run, total, p.grid, p.chunk);
+  const int64_t stop = run_start(run + 1, total, p.grid, p.chunk);
+  for (int64_t y = start; y < stop;) {
     const Piece pc = piece_at(seq_base, S, KV, y, stop);
     const int32_t L = p.context_lens[pc.s];
     const bool whole = pc.b0 == 0 && pc.b1 == pc.nb;
     const bool first_piece = y == start;
-    const int64_t rc0 = y - start;
+    const int64_t rc0 = done;
     const int ntiles = pc.b1 - pc.b0;
 
     float2 qf[GROUP][8];
@@ -375,9 +380,12 @@ paged_decode_kernel(const KParams p) {
     for (int k = first_k; k < ntiles; k += kNumConsumerWarps) {
       const int64_t rc = rc0 + k;
       const int st = static_cast<int>(rc % kNumStages);
-      if (abort_flag) break;
-      if (!mbar_wait(&full_bar[st], static_cast<uint32_t>((rc / kNumStages) & 1))) {
-        if (lane == 0) flag_error(p.status, PA_DEVFLAG_TIMEOUT);
+      // warp-uniform decision: every lane must take the same path into the shuffles below
+      const bool was_aborted = __any_sync(0xffffffffu, abort_flag != 0);
+      const bool ready = !was_aborted &&
+                         mbar_wait(&full_bar[st], static_cast<uint32_t>((rc / kNumStages) & 1));
+      if (!__all_sync(0xffffffffu, ready)) {
+        if (lane == 0 && !was_aborted) flag_error(p.status, PA_DEVFLAG_TIMEOUT);
         abort_flag = 1;
         break;
       }
@@ -465,8 +473,7 @@ paged_decode_kernel(const KParams p) {
         p.out[row * kHeadDim + d] = __float2bfloat16_rn(acc / lsum);
       } else {
         const int slot = first_piece ? 0 : 1;
-        float* dst = p.partials +
-                     ((static_cast<int64_t>(blockIdx.x) * 2 + slot) * GROUP + h) * kPartialFloats;
+        float* dst = p.partials + ((run * 2 + slot) * GROUP + h) * kPartialFloats;
         dst[d] = acc;
         if (d == 0) {
           dst[kHeadDim] = M[h];
@@ -476,6 +483,8 @@ paged_decode_kernel(const KParams p) {
     }
     named_barrier_sync(1, kConsumerThreads);  // scratch is reused by the next piece
     y += ntiles;
+    done += ntiles;
+  }
   }
 }
 
@@ -597,6 +606,10 @@ cudaError_t prepare_kernel() {
   cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<GROUP>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem_bytes<GROUP>(kMaxSeqs)));
+  if (e == cudaSuccess)  // the ring needs the full shared-memory carveout
+    e = cudaFuncSetAttribute(paged_decode_kernel<GROUP>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess) done = true;
   return e;
 }
@@ -627,7 +640,7 @@ cudaError_t launch(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t str
   p.num_kv_heads = a.num_kv_heads;
   p.num_blocks = a.num_blocks;
   p.q_scale = a.scale * 1.4426950408889634f;
-  p.grid = plan.grid;
+  p.grid = plan.runs;
   p.chunk = plan.chunk;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   p.ws_total = reinterpret_cast<int64_t*>(ws);
@@ -664,22 +677,24 @@ cudaError_t plan_decode(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_he
   if (ctas_per_sm < 1) return cudaErrorInvalidConfiguration;
   const int64_t blocks_max = (static_cast<int64_t>(max_context_len) + kBlockSize - 1) / kBlockSize;
   const int64_t tiles_upper = static_cast<int64_t>(num_seqs) * num_kv_heads * blocks_max;
-  int64_t grid;
+  const int64_t resident = static_cast<int64_t>(sms) * ctas_per_sm;
+  int64_t runs;
   if (partition_tokens > 0) {
     plan->chunk = partition_tokens / kBlockSize;
-    grid = (tiles_upper + plan->chunk - 1) / plan->chunk;
+    runs = (tiles_upper + plan->chunk - 1) / plan->chunk;
   } else {
     plan->chunk = 0;
-    grid = static_cast<int64_t>(sms) * ctas_per_sm;
+    runs = resident;
     const int64_t by_size = (tiles_upper + kMinTilesPerCta - 1) / kMinTilesPerCta;
-    if (by_size < grid) grid = by_size;
+    if (by_size < runs) runs = by_size;
   }
-  if (grid < 1) grid = 1;
-  if (grid > 0x7fffffff) return cudaErrorInvalidValue;
-  plan->grid = static_cast<int>(grid);
+  if (runs < 1) runs = 1;
+  if (runs > 0x7fffffff) return cudaErrorInvalidValue;
+  plan->runs = static_cast<int>(runs);
+  plan->grid = static_cast<int>(runs < resident ? runs : resident);
   plan->ws_meta_bytes = (16 + sizeof(int32_t) * (num_seqs + 1) + 255) / 256 * 256;
   plan->workspace_bytes = plan->ws_meta_bytes +
-                          static_cast<size_t>(grid) * 2 * group * kPartialFloats * sizeof(float);
+                          static_cast<size_t>(runs) * 2 * group * kPartialFloats * sizeof(float);
   return cudaSuccess;
 }
 

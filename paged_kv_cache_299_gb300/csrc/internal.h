@@ -23,8 +23,9 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value,
 // Work decomposition of one pa_decode call (identical in the size query and the call).
 struct DecodePlan {
   int group;          // q heads per kv head
-  int grid;           // CTAs of the attention kernel
-  int chunk;          // tiles per CTA (fixed mode), 0 = balanced split of the real total
+  int grid;           // CTAs of the attention kernel (persistent, <= resident capacity)
+  int runs;           // units of the tile decomposition; CTA c serves runs c, c + grid, ...
+  int chunk;          // tiles per run (fixed mode), 0 = balanced split of the real total
   size_t smem_bytes;  // dynamic shared memory of the attention kernel
   size_t ws_meta_bytes;      // offset of the partials inside the workspace
   size_t workspace_bytes;    // total workspace
@@ -57,6 +58,7 @@ struct PrefillArgs {
   void* out;
   const void* q;
   const int32_t* query_start_loc;
+  int32_t num_query_tokens;
   int32_t max_query_len;
   const void* key_cache;
   const void* value_cache;

@@ -1,13 +1,452 @@
-// Causal chunked-prefill attention over a paged prefix (tcgen05 version in progress).
+// Causal chunked-prefill attention over a paged prefix, on tcgen05 tensor cores.
+//
+// What is computed ("vLLM", blog.rlaisqls.com, sections PagedAttention and Flash
+// Attention; "tiny-vllm (1)", geonuchoi.com, sections 1 and 2): a sequence appends a chunk
+// of q_len tokens to a context of L tokens (the chunk's own K/V already stored); chunk row
+// i sits at position L - q_len + i and attends keys 0 .. L - q_len + i (causal mask) of
+// its query head's K/V head (query head h reads K/V head h / 4), with an online softmax
+// over key tiles so no score matrix reaches HBM.
+//
+// GB300 design.  QK^T and PV are dense contractions, so they run on the 5th-generation
+// tensor cores with accumulators in tensor memory:
+//   * One CTA per (32-token query tile, K/V head, sequence).  Its 128 MMA rows are the
+//     32 tokens x 4 query heads that share the K/V head (row = 4 * token + head), so each
+//     K/V tile feeds four heads.
+//   * Warp 5 loads the Q tile with one 3-D TMA box and gathers every 128-key K/V tile as
+//     eight 16-row TMA boxes at the physical blocks named by the block table (128-byte
+//     swizzle), into a 2-stage ring.
+//   * Warp 4 (one thread) issues S = Q K^T (M128 N128 K64, fp32 in TMEM columns 0..127)
+//     and O += P V (M128 N64 K128, TMEM columns 128..191, V read N-major) and commits
+//     them to mbarriers.
+//   * Warps 0-3 own one TMEM lane = one query row each: they read S, mask by absolute
+//     position, keep the running max / sum in registers (O in TMEM is rescaled only when
+//     the max grows by more than 2^8), write P as bf16 into a swizzled K-major smem tile,
+//     and finally normalise O and store bf16 rows.
+// Every mbarrier wait is bounded; on timeout the CTA records PA_DEVFLAG_TIMEOUT, drains
+// its own copies and MMAs, frees its tensor memory and returns.
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "internal.h"
+#include "tcgen05.cuh"
 
 namespace pkv {
 
+namespace {
+
+constexpr int kGroup = 4;                         // query heads per K/V head
+constexpr int kTokensPerTile = 32;
+constexpr int kTileM = kTokensPerTile * kGroup;   // 128 MMA rows
+constexpr int kTileN = 128;                       // keys per K/V tile
+constexpr int kBlocksPerTile = kTileN / kBlockSize;
+constexpr int kStages = 2;
+constexpr int kQBytes = kTileM * kRowBytes;       // 16 KiB
+constexpr int kKVBytes = kTileN * kRowBytes;      // 16 KiB per K (or V) tile
+constexpr int kPRegionBytes = kTileM * 128;       // 64 keys x 128 rows of bf16
+constexpr int kPBytes = 2 * kPRegionBytes;        // 32 KiB
+constexpr int kSmemBytes = 1024 + kQBytes + 2 * kStages * kKVBytes + kPBytes + 8 * 16 + 16;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kSCol = 0;
+constexpr uint32_t kOCol = 128;
+constexpr int kThreads = 192;
+constexpr float kRescaleThreshold = 8.0f;
+
+struct PParams {
+  __nv_bfloat16* out;
+  const int32_t* query_start_loc;
+  const int32_t* block_tables;
+  int32_t max_blocks_per_seq;
+  const int32_t* context_lens;
+  int32_t num_blocks;
+  int32_t num_kv_heads;
+  int32_t num_q_heads;
+  float qk_scale;  // scale * log2(e)
+  int32_t* status;
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
+                                              volatile int* abort_flag, int32_t* status) {
+  if (*abort_flag) return false;
+  if (mbar_wait(bar, parity)) return true;
+  flag_error(status, PA_DEVFLAG_TIMEOUT);
+  *abort_flag = 1;
+  return false;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                     const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_v, const PParams p) {
+  const int tile = blockIdx.x;
+  const int g = blockIdx.y;
+  const int s = blockIdx.z;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  const int q0 = p.query_start_loc[s];
+  const int q_len = p.query_start_loc[s + 1] - q0;
+  const int tok0 = tile * kTokensPerTile;
+  if (tok0 >= q_len) return;
+  const int L = p.context_lens[s];
+  if (L < q_len || static_cast<int64_t>(L) > static_cast<int64_t>(p.max_blocks_per_seq) * kBlockSize) {
+    if (tid == 0) flag_error(p.status, PA_DEVFLAG_BAD_CONTEXT);
+    return;
+  }
+  const int ntok = min(kTokensPerTile, q_len - tok0);
+  const int keys = L - q_len + tok0 + ntok;  // this tile needs keys 0 .. keys-1
+  const int n_kv = (keys + kTileN - 1) / kTileN;
+  const int blocks_needed = (keys + kBlockSize - 1) / kBlockSize;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sq = smem;
+  uint8_t* sk = sq + kQBytes;
+  uint8_t* sv = sk + kStages * kKVBytes;
+  uint8_t* sp = sv + kStages * kKVBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sp + kPBytes);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = kv_full + kStages;
+  uint64_t* s_ready = kv_empty + kStages;
+  uint64_t* p_ready = s_ready + 1;
+  uint64_t* o_done = p_ready + 1;
+  uint64_t* drain = o_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  __shared__ volatile int abort_flag;
+
+  if (tid == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    mbar_init(s_ready, 1);
+    mbar_init(p_ready, kTileM);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    fence_barrier_init();
+    abort_flag = 0;
+  }
+  if (warp == 4) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 5 && lane == 0) {
+    prefetch_tensormap(&tmap_q);
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 5) {
+    // ================================ TMA producer ================================
+    const int32_t* row = p.block_tables + static_cast<int64_t>(s) * p.max_blocks_per_seq;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, kQBytes);
+      tma_load_3d(sq, &tmap_q, 0, g * kGroup, q0 + tok0, q_full);
+    }
+    int issued = 0;
+    for (int j = 0; j < n_kv; ++j) {
+      const int st = j % kStages;
+      const int lb = j * kBlocksPerTile + lane;
+      const bool need = lane < kBlocksPerTile && lb < blocks_needed;
+      const int32_t phys = need ? __ldg(row + lb) : 0;
+      const bool bad = need && (phys < 0 || phys >= p.num_blocks);
+      const bool load = need && !bad;
+      const unsigned mask = __ballot_sync(0xffffffffu, load);
+      const unsigned bad_mask = __ballot_sync(0xffffffffu, bad);
+      if (lane == 0 && bad_mask != 0) flag_error(p.status, PA_DEVFLAG_BAD_BLOCK);
+      int ok = 1;
+      if (lane == 0) {
+        ok = wait_or_abort(&kv_empty[st], static_cast<uint32_t>((j / kStages) & 1) ^ 1u,
+                           &abort_flag, p.status);
+        if (ok) mbar_arrive_expect_tx(&kv_full[st], __popc(mask) * 2u * kTileBytes);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (load) {
+        const int y = (phys * p.num_kv_heads + g) * kBlockSize;
+        tma_load_2d(sk + st * kKVBytes + lane * kTileBytes, &tmap_k, 0, y, &kv_full[st]);
+        tma_load_2d(sv + st * kKVBytes + lane * kTileBytes, &tmap_v, 0, y, &kv_full[st]);
+      }
+      ++issued;
+    }
+    // leave no copy in flight: wait (bounded) for the Q tile and the last fill per stage
+    if (lane == 0) {
+      if (!mbar_wait(q_full, 0)) flag_error(p.status, PA_DEVFLAG_TIMEOUT);
+      for (int st = 0; st < kStages && st < issued; ++st) {
+        const int last = st + ((issued - 1 - st) / kStages) * kStages;
+        if (!mbar_wait(&kv_full[st], static_cast<uint32_t>((last / kStages) & 1)))
+          flag_error(p.status, PA_DEVFLAG_TIMEOUT);
+      }
+    }
+  } else if (warp == 4) {
+    // ================================ MMA issuer ==================================
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = idesc_bf16_f32(kTileM, kTileN, false);
+      constexpr uint32_t kIdescO = idesc_bf16_f32(kTileM, kHeadDim, true);
+      const uint32_t s_tmem = tmem + kSCol;
+      const uint32_t o_tmem = tmem + kOCol;
+      const uint32_t q_base = smem_addr(sq);
+      const uint32_t p_base = smem_addr(sp);
+      auto issue_pv = [&](int t) {
+        const uint32_t v_base = smem_addr(sv + (t % kStages) * kKVBytes);
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk) {
+          const uint64_t a = sw128_desc(p_base + (kk / 4) * kPRegionBytes + (kk % 4) * 32, 16, 1024);
+          const uint64_t b = sw128_desc(v_base + kk * 16 * kRowBytes, 16, 1024);
+          umma_bf16(o_tmem, a, b, kIdescO, (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(o_done);
+        umma_commit(&kv_empty[t % kStages]);
+      };
+      bool ok = wait_or_abort(q_full, 0, &abort_flag, p.status);
+      int j = 0;
+      for (; ok && j < n_kv; ++j) {
+        const int st = j % kStages;
+        if (!wait_or_abort(&kv_full[st], static_cast<uint32_t>((j / kStages) & 1), &abort_flag,
+                           p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        if (j > 0) {
+          if (!wait_or_abort(p_ready, static_cast<uint32_t>((j - 1) & 1), &abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          issue_pv(j - 1);
+        }
+        const uint32_t k_base = smem_addr(sk + st * kKVBytes);
+#pragma unroll
+        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+          umma_bf16(s_tmem, sw128_desc(q_base + kk * 32, 16, 1024),
+                    sw128_desc(k_base + kk * 32, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(s_ready);
+      }
+      if (ok && wait_or_abort(p_ready, static_cast<uint32_t>((n_kv - 1) & 1), &abort_flag,
+                              p.status)) {
+        tc_fence_after_sync();
+        issue_pv(n_kv - 1);
+      }
+      // wait (bounded) until every MMA issued above has completed
+      umma_commit(drain);
+      if (!mbar_wait(drain, 0)) flag_error(p.status, PA_DEVFLAG_TIMEOUT);
+    }
+  } else {
+    // ============================ softmax / epilogue (warps 0-3) ============================
+    const int r = tid;  // MMA row == TMEM lane
+    const int tt = r >> 2;
+    const int hh = r & 3;
+    const int token = tok0 + tt;
+    const bool row_ok = token < q_len;
+    const int pos = L - q_len + min(token, q_len - 1);
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    float m = -INFINITY;
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      ok = wait_or_abort(s_ready, static_cast<uint32_t>(j & 1), &abort_flag, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const int kb = j * kTileN;
+      uint32_t v[32];
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(lane_addr + kSCol + 32 * c, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float x = kb + 32 * c + i <= pos ? __uint_as_float(v[i]) * p.qk_scale : -INFINITY;
+          mt = fmaxf(mt, x);
+        }
+      }
+      const float m_new = fmaxf(m, mt);
+      const bool grow = m_new - m > kRescaleThreshold;  // true on the first tile (m = -inf)
+      float alpha = 1.f;
+      if (grow) {
+        alpha = fast_exp2(m - m_new);
+        m = m_new;
+      }
+      if (j > 0) {
+        // the previous P.V must be done: P is overwritten below and O may be rescaled
+        ok = wait_or_abort(o_done, static_cast<uint32_t>((j - 1) & 1), &abort_flag, p.status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after_sync();
+        if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            tmem_ld32(lane_addr + kOCol + 32 * c, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tmem_st32(lane_addr + kOCol + 32 * c, v);
+          }
+          tmem_wait_st();
+        }
+      }
+      if (j == n_kv - 1 && kb + r >= keys) {
+        // V rows past the last needed key are never weighted, but may hold NaN (unused
+        // slots) or stale data: zero them so 0 * V stays 0 in the tensor core.
+        uint4* vrow = reinterpret_cast<uint4*>(sv + (j % kStages) * kKVBytes + r * kRowBytes);
+#pragma unroll
+        for (int i = 0; i < kRowBytes / 16; ++i) vrow[i] = make_uint4(0, 0, 0, 0);
+      }
+      float psum = 0.f;
+      __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the row-local branch
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(lane_addr + kSCol + 32 * c, v);
+        tmem_wait_ld();
+        uint32_t packed[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int k0 = kb + 32 * c + 2 * i;
+          const float p0 = k0 <= pos ? fast_exp2(__uint_as_float(v[2 * i]) * p.qk_scale - m) : 0.f;
+          const float p1 = k0 + 1 <= pos ? fast_exp2(__uint_as_float(v[2 * i + 1]) * p.qk_scale - m) : 0.f;
+          psum += p0 + p1;
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+          packed[i] = *reinterpret_cast<const uint32_t*>(&b2);
+        }
+        uint8_t* region = sp + (c >> 1) * kPRegionBytes + r * 128;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int chunk = ((c & 1) * 4 + q4) ^ (r & 7);
+          *reinterpret_cast<uint4*>(region + chunk * 16) =
+              make_uint4(packed[4 * q4], packed[4 * q4 + 1], packed[4 * q4 + 2], packed[4 * q4 + 3]);
+        }
+      }
+      l = l * alpha + psum;
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      mbar_arrive(p_ready);
+    }
+    if (ok) {
+      ok = wait_or_abort(o_done, static_cast<uint32_t>((n_kv - 1) & 1), &abort_flag, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after_sync();
+      __syncwarp();
+      uint32_t o[2][32];
+      tmem_ld32(lane_addr + kOCol, o[0]);
+      tmem_ld32(lane_addr + kOCol + 32, o[1]);
+      tmem_wait_ld();
+      if (row_ok) {
+        const float inv = 1.f / l;
+        __nv_bfloat16* dst = p.out + (static_cast<int64_t>(q0 + token) * p.num_q_heads +
+                                      g * kGroup + hh) * kHeadDim;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int i = q4 * 8 + 2 * e;
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(o[c][i]) * inv,
+                                                              __uint_as_float(o[c][i + 1]) * inv);
+              w[e] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            *reinterpret_cast<uint4*>(dst + 32 * c + 8 * q4) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 4) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    cudaDriverEntryPointQueryResult q;
+    void* ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// [rows][64] bf16 tensor read in boxes of `box_rows` rows (128-byte swizzle).
+bool encode_rows(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), rows};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kRowBytes)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kHeadDim), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// q as [tokens][heads][64]; one box = 32 tokens x 4 heads (the 128 MMA rows of a tile).
+bool encode_q(CUtensorMap* map, const void* base, uint64_t tokens, uint64_t heads) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), heads, tokens};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kRowBytes), heads * kRowBytes};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), kGroup, kTokensPerTile};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
-  (void)a;
-  (void)stream;
-  return cudaErrorNotSupported;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(paged_prefill_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(paged_prefill_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const uint64_t pool_rows = static_cast<uint64_t>(a.num_blocks) * a.num_kv_heads * kBlockSize;
+  if (pool_rows >= (1ull << 31)) return cudaErrorInvalidValue;
+  CUtensorMap tq, tk, tv;
+  if (!encode_q(&tq, a.q, static_cast<uint64_t>(a.num_query_tokens), a.num_q_heads) ||
+      !encode_rows(&tk, a.key_cache, pool_rows, kBlockSize) ||
+      !encode_rows(&tv, a.value_cache, pool_rows, kBlockSize))
+    return cudaErrorInvalidValue;
+  PParams p;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.query_start_loc = a.query_start_loc;
+  p.block_tables = a.block_tables;
+  p.max_blocks_per_seq = a.max_blocks_per_seq;
+  p.context_lens = a.context_lens;
+  p.num_blocks = a.num_blocks;
+  p.num_kv_heads = a.num_kv_heads;
+  p.num_q_heads = a.num_q_heads;
+  p.qk_scale = a.scale * 1.4426950408889634f;
+  p.status = a.status;
+  dim3 grid((a.max_query_len + kTokensPerTile - 1) / kTokensPerTile, a.num_kv_heads, a.num_seqs);
+  paged_prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
 }
 
 }  // namespace pkv

@@ -76,8 +76,10 @@ def test_host_rejects_bad_arguments_without_touching_the_device():
     assert lib.pa_decode(*args, 2, 32, ctypes.c_float(-1.0), 64, 0, fake, 1 << 20, None,
                          None) == pa.PA_ERR_INVALID_ARG
     # prefill needs group 4
-    assert lib.pa_prefill_chunk(fake, fake, fake, 8, fake, fake, _desc(), fake, 4, fake, 2, 8,
-                                ctypes.c_float(0.125), None, None) == pa.PA_ERR_UNSUPPORTED
+    assert lib.pa_prefill_chunk(fake, fake, fake, 16, 8, fake, fake, _desc(), fake, 4, fake, 2,
+                                8, ctypes.c_float(0.125), None, None) == pa.PA_ERR_UNSUPPORTED
+    assert lib.pa_prefill_chunk(fake, fake, fake, 4, 8, fake, fake, _desc(), fake, 4, fake, 2,
+                                32, ctypes.c_float(0.125), None, None) == pa.PA_ERR_INVALID_ARG
     assert lib.pa_decode_workspace_size(2, 8, 24, 64, 0) == 0
     assert lib.pa_check_device_status(None, None) == pa.PA_ERR_INVALID_ARG
 
