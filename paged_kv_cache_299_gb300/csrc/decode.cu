@@ -193,16 +193,19 @@ template <int GROUP>
 __global__ void __launch_bounds__((kNumConsumerWarps + 1) * 32, 1)
 paged_decode_kernel(const KParams p) {
   static_assert(kNumStages % kNumConsumerWarps == 0, "stage ring must cycle per warp");
+  static_assert((kNumStages * 2 * kTileBytes + 2 * kNumStages * sizeof(uint64_t)) % 16 == 0,
+                "merge scratch must start on a 16-byte boundary");
   constexpr int kThreads = (kNumConsumerWarps + 1) * 32;
   constexpr int kConsumerThreads = kNumConsumerWarps * 32;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kNumStages * 2 * kTileBytes);
   uint64_t* empty_bar = full_bar + kNumStages;
-  float* red_m = reinterpret_cast<float*>(empty_bar + kNumStages);  // [W][GROUP]
-  float* red_l = red_m + kNumConsumerWarps * GROUP;                  // [W][GROUP]
-  float* red_o = red_l + kNumConsumerWarps * GROUP;                  // [W][GROUP][64]
-  int32_t* seq_base = reinterpret_cast<int32_t*>(red_o + kNumConsumerWarps * GROUP * kHeadDim);
+  // red_o first: it is written with 16-byte stores (offset = ring + barriers, a multiple of 16)
+  float* red_o = reinterpret_cast<float*>(empty_bar + kNumStages);   // [W][GROUP][64]
+  float* red_m = red_o + kNumConsumerWarps * GROUP * kHeadDim;        // [W][GROUP]
+  float* red_l = red_m + kNumConsumerWarps * GROUP;                   // [W][GROUP]
+  int32_t* seq_base = reinterpret_cast<int32_t*>(red_l + kNumConsumerWarps * GROUP);
   __shared__ int64_t warp_sums[kThreads / 32];
   __shared__ volatile int abort_flag;
 
