@@ -35,6 +35,7 @@ namespace {
 
 constexpr int kNumConsumerWarps = 7;  // + 1 producer = 8 warps, 2 per SM sub-partition
 constexpr int kNumStages = 28;     // multiple of kNumConsumerWarps; 112 KiB in flight
+constexpr int kProducerBatch = kNumStages < 32 ? kNumStages : 32;  // tiles issued in parallel
 constexpr int kPartialFloats = kHeadDim + 2;  // o[64], max (log2 units), sum
 constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale when max grows > 2^8
 constexpr int kMinTilesPerCta = 4;
@@ -290,34 +291,42 @@ paged_decode_kernel(const KParams p) {
     for (int64_t y = run_start(run, total, p.grid, p.chunk); y < stop && ok;) {
       const Piece pc = piece_at(seq_base, S, KV, y, stop);
       const int32_t* row = p.block_tables + static_cast<int64_t>(pc.s) * p.max_blocks_per_seq;
-      for (int bb = pc.b0; bb < pc.b1 && ok; bb += 32) {
-        const int n = min(32, pc.b1 - bb);
-        const int32_t phys = lane < n ? __ldg(row + bb + lane) : 0;
-        const bool bad = lane < n && (phys < 0 || phys >= p.num_blocks);
+      // Batches of up to kProducerBatch tiles: lane j owns tile bb + j, waits for its stage to
+      // be released and issues its two copies, so the barrier round trips of a batch overlap.
+      // A batch never holds two tiles of the same stage (kProducerBatch <= kNumStages), and
+      // every earlier tile is already issued, so each lane waits on its stage's current phase.
+      for (int bb = pc.b0; bb < pc.b1 && ok; bb += kProducerBatch) {
+        const int n = min(kProducerBatch, pc.b1 - bb);
+        const bool mine = lane < n;
+        const int32_t phys = mine ? __ldg(row + bb + lane) : 0;
+        const bool bad = mine && (phys < 0 || phys >= p.num_blocks);
         if (__any_sync(0xffffffffu, bad) && lane == 0) flag_error(p.status, PA_DEVFLAG_BAD_BLOCK);
-        for (int j = 0; j < n; ++j, ++rc) {
-          const int32_t pj = __shfl_sync(0xffffffffu, phys, j);
-          if (lane == 0) {
-            const int st = static_cast<int>(rc % kNumStages);
-            const uint32_t parity = static_cast<uint32_t>((rc / kNumStages) & 1) ^ 1u;
-            if (abort_flag || !mbar_wait(&empty_bar[st], parity)) {
-              if (!abort_flag) flag_error(p.status, PA_DEVFLAG_TIMEOUT);
-              abort_flag = 1;
-              ok = false;
-            } else if (pj < 0 || pj >= p.num_blocks) {
-              mbar_arrive(&full_bar[st]);  // release the stage; its data is stale
-            } else {
-              mbar_arrive_expect_tx(&full_bar[st], 2 * kTileBytes);
-              const size_t off = (static_cast<size_t>(pj) * KV + pc.g) * kTileBytes;
-              uint8_t* dst = ring + st * 2 * kTileBytes;
-              bulk_copy_g2s(dst, p.key_cache + off, kTileBytes, &full_bar[st], policy);
-              bulk_copy_g2s(dst + kTileBytes, p.value_cache + off, kTileBytes, &full_bar[st],
-                            policy);
-            }
-          }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
+        const int64_t my_rc = rc + lane;
+        const int st = static_cast<int>(my_rc % kNumStages);
+        bool freed = true;
+        if (mine) {
+          freed = abort_flag == 0 &&
+                  mbar_wait(&empty_bar[st], static_cast<uint32_t>((my_rc / kNumStages) & 1) ^ 1u);
         }
+        if (!__all_sync(0xffffffffu, freed)) {
+          if (lane == 0 && !abort_flag) flag_error(p.status, PA_DEVFLAG_TIMEOUT);
+          abort_flag = 1;
+          ok = false;
+          break;
+        }
+        if (mine) {
+          if (bad) {
+            mbar_arrive(&full_bar[st]);  // release the stage; its data is stale
+          } else {
+            mbar_arrive_expect_tx(&full_bar[st], 2 * kTileBytes);
+            const size_t off = (static_cast<size_t>(phys) * KV + pc.g) * kTileBytes;
+            uint8_t* dst = ring + st * 2 * kTileBytes;
+            bulk_copy_g2s(dst, p.key_cache + off, kTileBytes, &full_bar[st], policy);
+            bulk_copy_g2s(dst + kTileBytes, p.value_cache + off, kTileBytes, &full_bar[st],
+                          policy);
+          }
+        }
+        rc += n;
       }
       y += pc.b1 - pc.b0;
     }
