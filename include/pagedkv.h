@@ -147,6 +147,35 @@ pa_status pa_prefill_chunk(void* out, const void* q, const int32_t* query_start_
                            int32_t num_q_heads, float scale, int32_t* device_status,
                            pa_stream_t stream);
 
+/* Paged decode attention that needs no workspace from the caller.  The paper has no
+ * counterpart for this call.  It exists for callers that cannot allocate device memory
+ * themselves: code embedded in a host program that owns every device allocation (its
+ * memory pool is not reachable from here), or code that must not call cudaMalloc at run
+ * time because that call can stall the whole device.  It computes exactly what pa_decode
+ * computes, with the same arguments minus the workspace; the split-KV partials and
+ * per-sequence offsets live instead in one library-owned device array of
+ * PA_DECODE_STATIC_SCRATCH_BYTES bytes, which every GPU that loads the library keeps until
+ * the process exits.
+ *   - Sizes whose pa_decode_workspace_size() exceeds that limit are rejected with
+ *     PA_ERR_WORKSPACE before anything is launched (pa_last_error() names both sizes).
+ *     Balanced splits (partition_tokens 0) fit for every supported sequence count;
+ *     short fixed partitions over very long contexts may not.
+ *   - The first call on a device looks up the array's device address (once per device,
+ *     with that device current); make that first call before any stream capture.
+ *   - All calls share the array and it keeps the last call's contents.  Nothing in it has
+ *     to start at zero (each call writes every entry it later reads), but calls that can
+ *     overlap on the GPU (different streams, or different host threads) race on it: order
+ *     them on one stream.
+ *   - No allocation of any kind happens inside this call. */
+#define PA_DECODE_STATIC_SCRATCH_BYTES ((size_t)4 << 20)
+pa_status pa_decode_static_scratch(void* out, const void* q, const void* key_cache,
+                                   const void* value_cache, pa_cache_desc cd,
+                                   const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t* context_lens, int32_t num_seqs,
+                                   int32_t num_q_heads, float scale, int32_t max_context_len,
+                                   int32_t partition_tokens, int32_t* device_status,
+                                   pa_stream_t stream);
+
 /* Synchronise `stream`, read *device_status and translate it: PA_OK when zero,
  * PA_ERR_DEVICE_TIMEOUT when the timeout bit is set, else PA_ERR_DEVICE_INDEX. */
 pa_status pa_check_device_status(const int32_t* device_status, pa_stream_t stream);

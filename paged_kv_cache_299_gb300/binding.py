@@ -41,7 +41,7 @@ DEVFLAG_BAD_BLOCK, DEVFLAG_BAD_SLOT, DEVFLAG_BAD_CONTEXT, DEVFLAG_TIMEOUT = 1, 2
 # Every symbol include/pagedkv.h declares.
 EXPORTED = ("pa_compute_slot_mapping", "pa_reshape_and_cache", "pa_decode_workspace_size",
             "pa_decode", "pa_prefill_chunk", "pa_check_device_status", "pa_status_string",
-            "pa_last_error")
+            "pa_last_error", "pa_decode_static_scratch")
 
 
 def library_path() -> str:
@@ -72,6 +72,9 @@ def load(path: str | None = None):
     lib.pa_prefill_chunk.argtypes = [P, P, P, i32, i32, P, P, CacheDesc, P, i32, P, i32, i32,
                                      f32, P, P]
     lib.pa_prefill_chunk.restype = st
+    lib.pa_decode_static_scratch.argtypes = [P, P, P, P, CacheDesc, P, i32, P, i32, i32, f32,
+                                             i32, i32, P, P]
+    lib.pa_decode_static_scratch.restype = st
     lib.pa_check_device_status.argtypes = [P, P]
     lib.pa_check_device_status.restype = st
     lib.pa_status_string.argtypes = [st]
@@ -191,6 +194,31 @@ def pa_decode(out, q, key_cache, value_cache, block_tables, context_lens, scale,
                           int(partition_tokens), _ptr(workspace), workspace.numel(),
                           _ptr(device_status), _stream(stream))
     _check(st, "pa_decode")
+    return out
+
+
+def pa_decode_static_scratch(out, q, key_cache, value_cache, block_tables, context_lens, scale,
+                             max_context_len, partition_tokens=0, device_status=None,
+                             stream=None):
+    """Paged decode attention without a workspace argument: for callers that cannot
+    allocate device memory, the library uses its own fixed device scratch (see
+    include/pagedkv.h for the size limit and the rules on overlapping calls)."""
+    _need(out, "out", torch.bfloat16, 3)
+    _need(q, "q", torch.bfloat16, 3)
+    _need(key_cache, "key_cache", torch.bfloat16, 4)
+    _need(value_cache, "value_cache", torch.bfloat16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    num_seqs, hq, _ = q.shape
+    if out.shape != q.shape or block_tables.shape[0] != num_seqs or \
+            context_lens.shape[0] != num_seqs:
+        raise ValueError("q/out/block_tables/context_lens disagree on the sequence count")
+    st = load().pa_decode_static_scratch(
+        _ptr(out), _ptr(q), _ptr(key_cache), _ptr(value_cache), cache_desc(key_cache),
+        _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), num_seqs, hq,
+        float(scale), int(max_context_len), int(partition_tokens), _ptr(device_status),
+        _stream(stream))
+    _check(st, "pa_decode_static_scratch")
     return out
 
 

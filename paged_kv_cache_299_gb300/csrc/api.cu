@@ -48,6 +48,14 @@ pa_status check_desc(const pa_cache_desc& cd) {
 
 }  // namespace
 
+namespace pkv {
+// Lets other translation units of the library report a host-side rejection through
+// pa_last_error().
+pa_status record_error(pa_status st, const char* message) {
+  return fail(st, "%s", message);
+}
+}  // namespace pkv
+
 extern "C" {
 
 pa_status pa_compute_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_seq,
