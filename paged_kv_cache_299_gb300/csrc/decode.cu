@@ -103,80 +103,123 @@ __device__ __forceinline__ Piece piece_at(const int32_t* base, int num_seqs, int
   return pc;
 }
 
+// Query head whose score lane `dq` of a 4-lane group holds after score_for_own_head: the
+// reduce-scatter below leaves head (2 * (dq & 1) + (dq >> 1)) in lane dq for GROUP 4, head
+// (dq & 1) for GROUP 2, head 0 for GROUP 1.  The map is its own inverse, so it also gives
+// the lane that owns a head.
+template <int GROUP>
+__device__ __forceinline__ int own_head(int dq) {
+  if (GROUP == 4) return 2 * (dq & 1) + (dq >> 1);
+  if (GROUP == 2) return dq & 1;
+  return 0;
+}
+
+// Finish the 4-lane dot products of one token: a[h] is this lane's partial over its 16 dims.
+// Returns the full score of own_head(dq) (reduce-scatter: 3 shuffles for 4 heads).
+template <int GROUP>
+__device__ __forceinline__ float score_for_own_head(const float (&a)[GROUP], int dq) {
+  if (GROUP == 4) {
+    const bool b0 = dq & 1;
+    const float send0 = b0 ? a[0] : a[2];
+    const float send1 = b0 ? a[1] : a[3];
+    float keep0 = b0 ? a[2] : a[0];
+    float keep1 = b0 ? a[3] : a[1];
+    keep0 += __shfl_xor_sync(0xffffffffu, send0, 1);
+    keep1 += __shfl_xor_sync(0xffffffffu, send1, 1);
+    const bool b1 = dq & 2;
+    const float send = b1 ? keep0 : keep1;
+    const float keep = b1 ? keep1 : keep0;
+    return keep + __shfl_xor_sync(0xffffffffu, send, 2);
+  } else if (GROUP == 2) {
+    const bool b0 = dq & 1;
+    float keep = (b0 ? a[1] : a[0]) + __shfl_xor_sync(0xffffffffu, b0 ? a[0] : a[1], 1);
+    return keep + __shfl_xor_sync(0xffffffffu, keep, 2);
+  } else {
+    float v = a[0] + __shfl_xor_sync(0xffffffffu, a[0], 1);
+    return v + __shfl_xor_sync(0xffffffffu, v, 2);
+  }
+}
+
+// Value of `v` held by the owner lane of head h in this lane's 4-lane group.
+template <int GROUP>
+__device__ __forceinline__ float from_owner(float v, int lane, int h) {
+  if (GROUP == 1) return v;
+  return __shfl_sync(0xffffffffu, v, (lane & ~3) | own_head<GROUP>(h));
+}
+
+__device__ __forceinline__ void unpack8(uint4 a, uint4 b, float2 (&f)[8]) {
+  f[0] = bf16x2_to_float2(a.x); f[1] = bf16x2_to_float2(a.y);
+  f[2] = bf16x2_to_float2(a.z); f[3] = bf16x2_to_float2(a.w);
+  f[4] = bf16x2_to_float2(b.x); f[5] = bf16x2_to_float2(b.y);
+  f[6] = bf16x2_to_float2(b.z); f[7] = bf16x2_to_float2(b.w);
+}
+
 // Process one 16-token tile pair held in shared memory.  Lane (tg, dq) handles tokens tg
 // and tg + 8; its 16 dims are the 16-byte chunks c0 (set 0) and c1 (set 1) of each row.
+// After the score reduction the lane keeps the online-softmax state (m, l) of one query
+// head; its output slice o covers every head of the group.  m is the running reference
+// maximum in log2 units, raised only when a score exceeds it by more than 2^8.
 template <int GROUP, bool TAIL>
 __device__ __forceinline__ void attend_tile(const uint8_t* __restrict__ kt,
-                                            const uint8_t* __restrict__ vt, int tg, int c0,
-                                            int c1, int valid_tokens,
-                                            const float2 (&qf)[GROUP][8], float (&m)[GROUP],
-                                            float (&l)[GROUP], float2 (&o)[GROUP][8]) {
+                                            const uint8_t* __restrict__ vt, int lane, int tg,
+                                            int dq, int c0, int c1, int valid_tokens,
+                                            const float2 (&qf)[GROUP][8], float& m, float& l,
+                                            float2 (&o)[GROUP][8]) {
+  float s[2];
 #pragma unroll
   for (int step = 0; step < 2; ++step) {
-    const int t = tg + 8 * step;
-    const uint8_t* krow = kt + t * kRowBytes;
-    const uint4 ka = lds128(krow + c0 * 16);
-    const uint4 kb = lds128(krow + c1 * 16);
-    const float2 kf[8] = {bf16x2_to_float2(ka.x), bf16x2_to_float2(ka.y),
-                          bf16x2_to_float2(ka.z), bf16x2_to_float2(ka.w),
-                          bf16x2_to_float2(kb.x), bf16x2_to_float2(kb.y),
-                          bf16x2_to_float2(kb.z), bf16x2_to_float2(kb.w)};
-    float sc[GROUP];
+    const uint8_t* krow = kt + (tg + 8 * step) * kRowBytes;
+    float2 kf[8];
+    unpack8(lds128(krow + c0 * 16), lds128(krow + c1 * 16), kf);
+    float a[GROUP];
 #pragma unroll
     for (int h = 0; h < GROUP; ++h) {
-      float2 acc = make_float2(0.f, 0.f);
+      float2 acc = __fmul2_rn(qf[h][0], kf[0]);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc = __ffma2_rn(qf[h][i], kf[i], acc);
-      sc[h] = acc.x + acc.y;
+      for (int i = 1; i < 8; ++i) acc = __ffma2_rn(qf[h][i], kf[i], acc);
+      a[h] = acc.x + acc.y;
     }
-#pragma unroll
-    for (int h = 0; h < GROUP; ++h) sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], 1);
-#pragma unroll
-    for (int h = 0; h < GROUP; ++h) sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], 2);
-    const bool valid = !TAIL || t < valid_tokens;
-    float dlt[GROUP];
-    bool grow = false;
+    s[step] = score_for_own_head<GROUP>(a, dq);
+    if (TAIL && tg + 8 * step >= valid_tokens) s[step] = -INFINITY;
+  }
+  const float mt = fmaxf(s[0], s[1]);
+  const bool grow = mt - m > kRescaleThreshold;  // first tile: m = -inf
+  if (__any_sync(0xffffffffu, grow)) {
+    const float alpha = grow ? fast_exp2(m - mt) : 1.f;
+    if (grow) {
+      l *= alpha;
+      m = mt;
+    }
 #pragma unroll
     for (int h = 0; h < GROUP; ++h) {
-      if (TAIL && !valid) sc[h] = -INFINITY;
-      dlt[h] = sc[h] - m[h];
-      grow |= dlt[h] > kRescaleThreshold;
-    }
-    if (__any_sync(0xffffffffu, grow)) {
+      const float ah = from_owner<GROUP>(alpha, lane, h);
+      const float2 aa = make_float2(ah, ah);
 #pragma unroll
-      for (int h = 0; h < GROUP; ++h) {
-        if (dlt[h] > kRescaleThreshold) {
-          const float a = fast_exp2(m[h] - sc[h]);
-          l[h] *= a;
-          const float2 aa = make_float2(a, a);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) o[h][i] = __fmul2_rn(o[h][i], aa);
-          m[h] = sc[h];
-          dlt[h] = 0.f;
-        }
-      }
+      for (int i = 0; i < 8; ++i) o[h][i] = __fmul2_rn(o[h][i], aa);
     }
-    float pr[GROUP];
+  }
+  float pr[2];
 #pragma unroll
-    for (int h = 0; h < GROUP; ++h) {
-      pr[h] = fast_exp2(dlt[h]);
-      if (TAIL && !valid) pr[h] = 0.f;
-      l[h] += pr[h];
-    }
-    const uint8_t* vrow = vt + t * kRowBytes;
+  for (int step = 0; step < 2; ++step) {
+    pr[step] = fast_exp2(s[step] - m);
+    if (TAIL && tg + 8 * step >= valid_tokens) pr[step] = 0.f;  // also covers m = -inf
+  }
+  l += pr[0] + pr[1];
+#pragma unroll
+  for (int step = 0; step < 2; ++step) {
+    const uint8_t* vrow = vt + (tg + 8 * step) * kRowBytes;
     uint4 va = lds128(vrow + c0 * 16);
     uint4 vb = lds128(vrow + c1 * 16);
-    if (TAIL && !valid) {  // unused slots may hold anything (NaN included): never multiply
+    if (TAIL && tg + 8 * step >= valid_tokens) {  // unused slots may hold NaN: never multiply
       va = make_uint4(0, 0, 0, 0);
       vb = make_uint4(0, 0, 0, 0);
     }
-    const float2 vf[8] = {bf16x2_to_float2(va.x), bf16x2_to_float2(va.y),
-                          bf16x2_to_float2(va.z), bf16x2_to_float2(va.w),
-                          bf16x2_to_float2(vb.x), bf16x2_to_float2(vb.y),
-                          bf16x2_to_float2(vb.z), bf16x2_to_float2(vb.w)};
+    float2 vf[8];
+    unpack8(va, vb, vf);
 #pragma unroll
     for (int h = 0; h < GROUP; ++h) {
-      const float2 pp = make_float2(pr[h], pr[h]);
+      const float ph = from_owner<GROUP>(pr[step], lane, h);
+      const float2 pp = make_float2(ph, ph);
 #pragma unroll
       for (int i = 0; i < 8; ++i) o[h][i] = __ffma2_rn(pp, vf[i], o[h][i]);
     }
@@ -284,7 +327,7 @@ paged_decode_kernel(const KParams p) {
   if (warp == kNumConsumerWarps) {
     // =============================== producer warp ===============================
     const uint64_t policy = l2_evict_first_policy();
-    int64_t rc = 0;  // tiles issued so far by this CTA
+    int rc = 0;  // tiles issued so far by this CTA
     bool ok = true;
     for (int64_t run = blockIdx.x; run < p.grid && ok; run += gridDim.x) {
     const int64_t stop = run_start(run + 1, total, p.grid, p.chunk);
@@ -301,30 +344,31 @@ paged_decode_kernel(const KParams p) {
         const int32_t phys = mine ? __ldg(row + bb + lane) : 0;
         const bool bad = mine && (phys < 0 || phys >= p.num_blocks);
         if (__any_sync(0xffffffffu, bad) && lane == 0) flag_error(p.status, PA_DEVFLAG_BAD_BLOCK);
-        const int64_t my_rc = rc + lane;
-        const int st = static_cast<int>(my_rc % kNumStages);
-        bool freed = true;
-        if (mine) {
-          freed = abort_flag == 0 &&
-                  mbar_wait(&empty_bar[st], static_cast<uint32_t>((my_rc / kNumStages) & 1) ^ 1u);
+        const int my_rc = rc + lane;
+        const int st = my_rc % kNumStages;
+        bool failed = false;
+        if (mine) {  // each lane fills its stage as soon as that stage is released
+          if (abort_flag == 0 &&
+              mbar_wait(&empty_bar[st], static_cast<uint32_t>((my_rc / kNumStages) & 1) ^ 1u)) {
+            if (bad) {
+              mbar_arrive(&full_bar[st]);  // release the stage; its data is stale
+            } else {
+              mbar_arrive_expect_tx(&full_bar[st], 2 * kTileBytes);
+              const size_t off = (static_cast<size_t>(phys) * KV + pc.g) * kTileBytes;
+              uint8_t* dst = ring + st * 2 * kTileBytes;
+              bulk_copy_g2s(dst, p.key_cache + off, kTileBytes, &full_bar[st], policy);
+              bulk_copy_g2s(dst + kTileBytes, p.value_cache + off, kTileBytes, &full_bar[st],
+                            policy);
+            }
+          } else {
+            failed = true;
+          }
         }
-        if (!__all_sync(0xffffffffu, freed)) {
+        if (__any_sync(0xffffffffu, failed)) {
           if (lane == 0 && !abort_flag) flag_error(p.status, PA_DEVFLAG_TIMEOUT);
           abort_flag = 1;
           ok = false;
           break;
-        }
-        if (mine) {
-          if (bad) {
-            mbar_arrive(&full_bar[st]);  // release the stage; its data is stale
-          } else {
-            mbar_arrive_expect_tx(&full_bar[st], 2 * kTileBytes);
-            const size_t off = (static_cast<size_t>(phys) * KV + pc.g) * kTileBytes;
-            uint8_t* dst = ring + st * 2 * kTileBytes;
-            bulk_copy_g2s(dst, p.key_cache + off, kTileBytes, &full_bar[st], policy);
-            bulk_copy_g2s(dst + kTileBytes, p.value_cache + off, kTileBytes, &full_bar[st],
-                          policy);
-          }
         }
         rc += n;
       }
@@ -351,7 +395,8 @@ paged_decode_kernel(const KParams p) {
   const int par = tg & 1;
   const int c0 = dq + 4 * par;        // 16-byte chunk held in register set 0
   const int c1 = dq + 4 * (par ^ 1);  // 16-byte chunk held in register set 1
-  int64_t done = 0;  // tiles consumed so far by this CTA (the producer's running count)
+  const int ho = own_head<GROUP>(dq);
+  int done = 0;  // tiles consumed so far by this CTA (the producer's running count)
   for (int64_t run = blockIdx.x; run < p.grid; run += gridDim.x) {
   const int64_t start = run_start(run, total, p.grid, p.chunk);
   const int64_t stop = run_start(run + 1, total, p.grid, p.chunk);
@@ -360,7 +405,6 @@ paged_decode_kernel(const KParams p) {
     const int32_t L = p.context_lens[pc.s];
     const bool whole = pc.b0 == 0 && pc.b1 == pc.nb;
     const bool first_piece = y == start;
-    const int64_t rc0 = done;
     const int ntiles = pc.b1 - pc.b0;
 
     float2 qf[GROUP][8];
@@ -370,73 +414,67 @@ paged_decode_kernel(const KParams p) {
           p.q + (static_cast<int64_t>(pc.s) * p.num_q_heads + pc.g * GROUP + h) * kHeadDim;
       const uint4 a = ldg_nc128(qrow + c0 * 8);
       const uint4 b = ldg_nc128(qrow + c1 * 8);
-      const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      float2 f[8];
+      unpack8(a, b, f);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float2 f = bf16x2_to_float2(w[i]);
-        qf[h][i] = make_float2(f.x * p.q_scale, f.y * p.q_scale);
-      }
+      for (int i = 0; i < 8; ++i) qf[h][i] = make_float2(f[i].x * p.q_scale, f[i].y * p.q_scale);
     }
-    float m[GROUP], l[GROUP];
+    float m = -INFINITY, l = 0.f;
     float2 o[GROUP][8];
 #pragma unroll
     for (int h = 0; h < GROUP; ++h) {
-      m[h] = -INFINITY;
-      l[h] = 0.f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) o[h][i] = make_float2(0.f, 0.f);
     }
 
-    const int first_k = static_cast<int>(((warp - rc0) % kNumConsumerWarps + kNumConsumerWarps) %
-                                         kNumConsumerWarps);
-    for (int k = first_k; k < ntiles; k += kNumConsumerWarps) {
-      const int64_t rc = rc0 + k;
-      const int st = static_cast<int>(rc % kNumStages);
-      // warp-uniform decision: every lane must take the same path into the shuffles below
-      const bool was_aborted = __any_sync(0xffffffffu, abort_flag != 0);
-      const bool ready = !was_aborted &&
-                         mbar_wait(&full_bar[st], static_cast<uint32_t>((rc / kNumStages) & 1));
-      if (!__all_sync(0xffffffffu, ready)) {
-        if (lane == 0 && !was_aborted) flag_error(p.status, PA_DEVFLAG_TIMEOUT);
+    // This warp takes the piece's tiles with running index = warp (mod W); stage and phase
+    // advance by W per tile (kNumStages is a multiple of W).
+    const int first_k = (warp - done % kNumConsumerWarps + kNumConsumerWarps) % kNumConsumerWarps;
+    int st = (done + first_k) % kNumStages;
+    uint32_t phase = static_cast<uint32_t>(((done + first_k) / kNumStages) & 1);
+    const bool aborted = __any_sync(0xffffffffu, abort_flag != 0);
+    for (int k = first_k; k < ntiles && !aborted; k += kNumConsumerWarps) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&full_bar[st], phase))) {
+        if (lane == 0) flag_error(p.status, PA_DEVFLAG_TIMEOUT);
         abort_flag = 1;
         break;
       }
       const uint8_t* kt = ring + st * 2 * kTileBytes;
       const uint8_t* vt = kt + kTileBytes;
-      const int b = pc.b0 + k;
-      const int valid = L - b * kBlockSize;
+      const int valid = L - (pc.b0 + k) * kBlockSize;
       if (valid >= kBlockSize) {
-        attend_tile<GROUP, false>(kt, vt, tg, c0, c1, kBlockSize, qf, m, l, o);
+        attend_tile<GROUP, false>(kt, vt, lane, tg, dq, c0, c1, kBlockSize, qf, m, l, o);
       } else {
-        attend_tile<GROUP, true>(kt, vt, tg, c0, c1, valid, qf, m, l, o);
+        attend_tile<GROUP, true>(kt, vt, lane, tg, dq, c0, c1, valid, qf, m, l, o);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[st]);
+      st += kNumConsumerWarps;
+      if (st >= kNumStages) {
+        st -= kNumStages;
+        phase ^= 1u;
+      }
     }
 
-    // ---- merge the 32 (warp, token-group) online-softmax states of this piece ----
-    float mx[GROUP];
-#pragma unroll
-    for (int h = 0; h < GROUP; ++h) {
-      mx[h] = m[h];
-      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 4));
-      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 8));
-      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 16));
-    }
-    if (lane == 0) {
-#pragma unroll
-      for (int h = 0; h < GROUP; ++h) red_m[warp * GROUP + h] = mx[h];
-    }
+    // ---- merge the (warp, token-group) online-softmax states of this piece ----
+    // warp maximum of each head: lanes with the same dq own the same head
+    float mw = m;
+    mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 4));
+    mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 8));
+    mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 16));
+    if (tg == 0) red_m[warp * GROUP + ho] = mw;
     named_barrier_sync(1, kConsumerThreads);
-    float M[GROUP];
+    float M_own = red_m[ho];
+#pragma unroll
+    for (int w = 1; w < kNumConsumerWarps; ++w) M_own = fmaxf(M_own, red_m[w * GROUP + ho]);
+    const float f_own = m == -INFINITY ? 0.f : fast_exp2(m - M_own);
+    l *= f_own;
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
 #pragma unroll
     for (int h = 0; h < GROUP; ++h) {
-      M[h] = red_m[h];
-#pragma unroll
-      for (int w = 1; w < kNumConsumerWarps; ++w) M[h] = fmaxf(M[h], red_m[w * GROUP + h]);
-      const float f = m[h] == -INFINITY ? 0.f : fast_exp2(m[h] - M[h]);
-      l[h] *= f;
-      const float2 ff = make_float2(f, f);
+      const float fh = from_owner<GROUP>(f_own, lane, h);
+      const float2 ff = make_float2(fh, fh);
 #pragma unroll
       for (int i = 0; i < 8; ++i) o[h][i] = __fmul2_rn(o[h][i], ff);
       if (par) {  // odd token groups hold chunk dq+4 in set 0: align before summing
@@ -449,7 +487,6 @@ paged_decode_kernel(const KParams p) {
       }
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) {
-        l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           o[h][i].x += __shfl_xor_sync(0xffffffffu, o[h][i].x, off);
@@ -467,18 +504,19 @@ paged_decode_kernel(const KParams p) {
         lo[1] = make_float4(o[h][2].x, o[h][2].y, o[h][3].x, o[h][3].y);
         hi[0] = make_float4(o[h][4].x, o[h][4].y, o[h][5].x, o[h][5].y);
         hi[1] = make_float4(o[h][6].x, o[h][6].y, o[h][7].x, o[h][7].y);
-        if (dq == 0) red_l[warp * GROUP + h] = l[h];
       }
+      red_l[warp * GROUP + ho] = l;
     }
     named_barrier_sync(1, kConsumerThreads);
     for (int e = tid; e < GROUP * kHeadDim; e += kConsumerThreads) {
       const int h = e / kHeadDim;
       const int d = e % kHeadDim;
-      float acc = 0.f, lsum = 0.f;
+      float acc = 0.f, lsum = 0.f, mh = -INFINITY;
 #pragma unroll
       for (int w = 0; w < kNumConsumerWarps; ++w) {
         acc += red_o[(w * GROUP + h) * kHeadDim + d];
         lsum += red_l[w * GROUP + h];
+        mh = fmaxf(mh, red_m[w * GROUP + h]);
       }
       if (whole) {
         const int64_t row = static_cast<int64_t>(pc.s) * p.num_q_heads + pc.g * GROUP + h;
@@ -488,7 +526,7 @@ paged_decode_kernel(const KParams p) {
         float* dst = p.partials + ((run * 2 + slot) * GROUP + h) * kPartialFloats;
         dst[d] = acc;
         if (d == 0) {
-          dst[kHeadDim] = M[h];
+          dst[kHeadDim] = mh;
           dst[kHeadDim + 1] = lsum;
         }
       }
