@@ -121,7 +121,7 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t 
  *   partition_tokens 0 = split evenly over the device; else a multiple of 16 giving
  *                    the run length in tokens
  *   workspace        device buffer of >= pa_decode_workspace_size(...) bytes
- * num_seqs == 0 is a no-op.  At most 8192 sequences per call. */
+ * num_seqs == 0 is a no-op.  At most 4096 sequences per call. */
 pa_status pa_decode(void* out, const void* q, const void* key_cache, const void* value_cache,
                     pa_cache_desc cd, const int32_t* block_tables,
                     int32_t max_blocks_per_seq, const int32_t* context_lens,

@@ -94,6 +94,12 @@ __device__ __forceinline__ void bulk_copy_g2s(void* smem_dst, const void* gmem_s
       : "memory");
 }
 
+// Order this thread's (and, after a warp/block sync, its peers') generic-proxy shared-memory
+// accesses before later async-proxy operations (TMA copies, tensor-core reads).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---- named barrier among a subset of warps ------------------------------------------------
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

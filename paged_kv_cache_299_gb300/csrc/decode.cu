@@ -9,21 +9,24 @@
 //
 // GB300 design (decode is HBM-bound: each (block, kv head) tile of 2 KiB of K + 2 KiB of
 // V is read once and feeds 4 query heads):
-//   * The flattened space of (sequence, kv head, block) tiles is cut into one contiguous
-//     run per CTA, of equal length (or of `chunk` tiles when the caller fixes the
-//     partition), so every SM streams the same number of bytes whatever the length mix.
-//   * One producer warp walks the run, reads the block-table entries 32 at a time and
-//     issues cp.async.bulk (TMA, non-tensor) copies of each K and V tile into an NSTAGES
-//     ring in shared memory, completing on per-stage mbarriers; consumer warps take tiles
-//     round-robin.
-//   * Consumer lane (tg, dq) owns token tg and tg+8 of a tile and a quarter of the 64
-//     dims; q for all GROUP heads stays in registers (pre-scaled by scale*log2 e), the
-//     4-lane dot product is finished with two shuffles, and each lane keeps its own
-//     online-softmax state (max, sum, output slice), rescaled only when the max grows by
-//     more than 2^8, so the per-token cost is FMAs, one exp2 and no cross-lane reduction.
-//   * At the end of a run piece the lanes and warps are merged (log-sum-exp weights) and
-//     either the final bf16 row is written (whole sequence in one CTA) or an unnormalised
-//     (o, max, sum) partial, which merge_partials_kernel combines.
+//   * The flattened space of (sequence, kv head, block) tiles is cut into contiguous runs
+//     of equal length, one per warp of a persistent grid (or runs of `chunk` tiles when
+//     the caller fixes the partition), so every warp streams the same number of bytes
+//     whatever the length mix.
+//   * Each warp streams its own run through a private 4-stage ring in shared memory: lane
+//     0 issues cp.async.bulk (TMA, non-tensor) copies of the K and V tile, completing on
+//     the stage's mbarrier, and refills a stage as soon as the warp has consumed it.  The
+//     block-table entries are fetched 32 at a time, one window ahead.  No producer warp,
+//     no release barriers, no block-wide synchronisation while streaming.
+//   * Lane (tg, dq) owns tokens tg and tg+8 of a tile and a quarter of the 64 dims; q for
+//     all GROUP heads stays in registers (pre-scaled by scale*log2 e).  The 4-lane dot
+//     products are finished by a reduce-scatter that leaves each lane one head's score,
+//     whose online softmax (running max, running sum) it keeps; the reference max is
+//     raised only when a score exceeds it by more than 2^8.
+//   * When a run ends or crosses into the next (sequence, kv head), the warp's eight
+//     token-group states are combined through shared memory (log-sum-exp weights) and
+//     either the final bf16 rows are written (whole sequence in one run) or an
+//     unnormalised (o, max, sum) partial, which merge_partials_kernel combines.
 #include <math.h>
 
 #include "common.cuh"
@@ -33,13 +36,13 @@ namespace pkv {
 
 namespace {
 
-constexpr int kNumConsumerWarps = 7;  // + 1 producer = 8 warps, 2 per SM sub-partition
-constexpr int kNumStages = 28;     // multiple of kNumConsumerWarps; 112 KiB in flight
-constexpr int kProducerBatch = kNumStages < 32 ? kNumStages : 32;  // tiles issued in parallel
+constexpr int kWarps = 8;           // streaming warps per CTA, 2 per SM sub-partition
+constexpr int kStagesPerWarp = 4;   // private ring depth: 16 KiB in flight per warp
+constexpr int kWindow = 32;         // block-table entries fetched per window
 constexpr int kPartialFloats = kHeadDim + 2;  // o[64], max (log2 units), sum
 constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale when max grows > 2^8
-constexpr int kMinTilesPerCta = 4;
-constexpr int kMaxSeqs = 8192;
+constexpr int kMinTilesPerRun = 4;
+constexpr int kMaxSeqs = 4096;
 constexpr int kMergeThreads = 256;
 
 struct KParams {
@@ -55,7 +58,8 @@ struct KParams {
   int32_t num_kv_heads;
   int32_t num_blocks;
   float q_scale;  // scale * log2(e): scores come out in log2 units
-  int32_t grid;      // runs of the decomposition (balanced mode: one per CTA)
+  int32_t grid;      // runs of the decomposition (warp w of the grid serves runs
+                     // w, w + warps, ...)
   int32_t chunk;     // tiles per run, 0 = balanced split into `grid` runs
   int64_t* ws_total;    // total tiles, written by CTA 0
   int32_t* ws_seq_base; // [num_seqs + 1] blocks-per-head prefix, written by CTA 0
@@ -227,45 +231,53 @@ __device__ __forceinline__ void attend_tile(const uint8_t* __restrict__ kt,
 }
 
 template <int GROUP>
-constexpr size_t decode_smem_fixed() {
-  return static_cast<size_t>(kNumStages) * 2 * kTileBytes  // K+V ring
-         + 2 * kNumStages * sizeof(uint64_t)               // full / empty barriers
-         + sizeof(float) * kNumConsumerWarps * GROUP * (2 + kHeadDim);  // merge scratch
+__host__ __device__ constexpr int o_row_floats() {  // one token group's output slice in the merge scratch (+pad)
+  return GROUP * kHeadDim + 4;
 }
 
 template <int GROUP>
-__global__ void __launch_bounds__((kNumConsumerWarps + 1) * 32, 1)
-paged_decode_kernel(const KParams p) {
-  static_assert(kNumStages % kNumConsumerWarps == 0, "stage ring must cycle per warp");
-  static_assert((kNumStages * 2 * kTileBytes + 2 * kNumStages * sizeof(uint64_t)) % 16 == 0,
-                "merge scratch must start on a 16-byte boundary");
-  constexpr int kThreads = (kNumConsumerWarps + 1) * 32;
-  constexpr int kConsumerThreads = kNumConsumerWarps * 32;
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* ring = smem;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kNumStages * 2 * kTileBytes);
-  uint64_t* empty_bar = full_bar + kNumStages;
-  // red_o first: it is written with 16-byte stores (offset = ring + barriers, a multiple of 16)
-  float* red_o = reinterpret_cast<float*>(empty_bar + kNumStages);   // [W][GROUP][64]
-  float* red_m = red_o + kNumConsumerWarps * GROUP * kHeadDim;        // [W][GROUP]
-  float* red_l = red_m + kNumConsumerWarps * GROUP;                   // [W][GROUP]
-  int32_t* seq_base = reinterpret_cast<int32_t*>(red_l + kNumConsumerWarps * GROUP);
-  __shared__ int64_t warp_sums[kThreads / 32];
-  __shared__ volatile int abort_flag;
+constexpr size_t decode_smem_fixed() {
+  return static_cast<size_t>(kWarps) *
+         (kStagesPerWarp * 2 * kTileBytes                           // private K+V rings
+          + 8 * o_row_floats<GROUP>() * sizeof(float)                // o of 8 token groups
+          + 2 * GROUP * 8 * sizeof(float)                            // m, l of 8 token groups
+          + kStagesPerWarp * sizeof(uint64_t));                      // full barriers
+}
 
+// Block-table window: lane j holds the tile (phys_block * Hkv + kv_head) of the j-th of
+// `n` consecutive tiles of one run, or -1 for an invalid block id.
+struct Window {
+  int32_t tile;
+  int n;
+};
+
+template <int GROUP>
+__global__ void __launch_bounds__(kWarps * 32, 1)
+paged_decode_kernel(const KParams p) {
+  constexpr int kThreads = kWarps * 32;
+  constexpr int kORow = o_row_floats<GROUP>();
+  static_assert((kWarps * kStagesPerWarp * 2 * kTileBytes) % 16 == 0, "scratch alignment");
+  static_assert((kORow * sizeof(float)) % 16 == 0, "scratch rows take 16-byte stores");
+  extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int S = p.num_seqs;
   const int KV = p.num_kv_heads;
 
-  if (tid == 0) {
-    for (int i = 0; i < kNumStages; ++i) {
-      mbar_init(&full_bar[i], 1);
-      mbar_init(&empty_bar[i], 1);
-    }
+  uint8_t* ring = smem + warp * (kStagesPerWarp * 2 * kTileBytes);
+  float* scratch = reinterpret_cast<float*>(smem + kWarps * kStagesPerWarp * 2 * kTileBytes);
+  float* o_s = scratch + warp * 8 * kORow;                           // [8 tg][kORow]
+  float* m_s = scratch + kWarps * 8 * kORow + warp * 2 * GROUP * 8;  // [GROUP][8 tg]
+  float* l_s = m_s + GROUP * 8;                                      // [GROUP][8 tg]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(scratch + kWarps * 8 * kORow + kWarps * 2 * GROUP * 8);
+  uint64_t* full_bar = bars + warp * kStagesPerWarp;
+  int32_t* seq_base = reinterpret_cast<int32_t*>(bars + kWarps * kStagesPerWarp);
+  __shared__ int64_t warp_sums[kWarps];
+
+  if (lane == 0) {
+    for (int i = 0; i < kStagesPerWarp; ++i) mbar_init(&full_bar[i], 1);
     fence_barrier_init();
-    abort_flag = 0;
   }
 
   // ---- per-sequence block counts and their exclusive prefix (the tile index space) ----
@@ -296,7 +308,7 @@ paged_decode_kernel(const KParams p) {
     __syncthreads();
     int64_t run = incl - local;
     int64_t grand = 0;
-    for (int w = 0; w < kThreads / 32; ++w) {
+    for (int w = 0; w < kWarps; ++w) {
       if (w < warp) run += warp_sums[w];
       grand += warp_sums[w];
     }
@@ -320,84 +332,84 @@ paged_decode_kernel(const KParams p) {
         flag_error(p.status, PA_DEVFLAG_BAD_CONTEXT);  // contexts beyond max_context_len
     }
   }
-  // This CTA serves runs blockIdx.x, blockIdx.x + gridDim.x, ... (persistent); the
-  // producer and the consumers walk the same sequence of runs and pieces.
-  if (run_start(blockIdx.x, total, p.grid, p.chunk) >= total) return;
+  // From here on every warp works alone: no block-wide synchronisation below.
+  const int64_t total_warps = static_cast<int64_t>(gridDim.x) * kWarps;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+  if (gw >= p.grid) return;
 
-  if (warp == kNumConsumerWarps) {
-    // =============================== producer warp ===============================
-    const uint64_t policy = l2_evict_first_policy();
-    int rc = 0;  // tiles issued so far by this CTA
-    bool ok = true;
-    for (int64_t run = blockIdx.x; run < p.grid && ok; run += gridDim.x) {
-    const int64_t stop = run_start(run + 1, total, p.grid, p.chunk);
-    for (int64_t y = run_start(run, total, p.grid, p.chunk); y < stop && ok;) {
-      const Piece pc = piece_at(seq_base, S, KV, y, stop);
-      const int32_t* row = p.block_tables + static_cast<int64_t>(pc.s) * p.max_blocks_per_seq;
-      // Batches of up to kProducerBatch tiles: lane j owns tile bb + j, waits for its stage to
-      // be released and issues its two copies, so the barrier round trips of a batch overlap.
-      // A batch never holds two tiles of the same stage (kProducerBatch <= kNumStages), and
-      // every earlier tile is already issued, so each lane waits on its stage's current phase.
-      for (int bb = pc.b0; bb < pc.b1 && ok; bb += kProducerBatch) {
-        const int n = min(kProducerBatch, pc.b1 - bb);
-        const bool mine = lane < n;
-        const int32_t phys = mine ? __ldg(row + bb + lane) : 0;
-        const bool bad = mine && (phys < 0 || phys >= p.num_blocks);
-        if (__any_sync(0xffffffffu, bad) && lane == 0) flag_error(p.status, PA_DEVFLAG_BAD_BLOCK);
-        const int my_rc = rc + lane;
-        const int st = my_rc % kNumStages;
-        bool failed = false;
-        if (mine) {  // each lane fills its stage as soon as that stage is released
-          if (abort_flag == 0 &&
-              mbar_wait(&empty_bar[st], static_cast<uint32_t>((my_rc / kNumStages) & 1) ^ 1u)) {
-            if (bad) {
-              mbar_arrive(&full_bar[st]);  // release the stage; its data is stale
-            } else {
-              mbar_arrive_expect_tx(&full_bar[st], 2 * kTileBytes);
-              const size_t off = (static_cast<size_t>(phys) * KV + pc.g) * kTileBytes;
-              uint8_t* dst = ring + st * 2 * kTileBytes;
-              bulk_copy_g2s(dst, p.key_cache + off, kTileBytes, &full_bar[st], policy);
-              bulk_copy_g2s(dst + kTileBytes, p.value_cache + off, kTileBytes, &full_bar[st],
-                            policy);
-            }
-          } else {
-            failed = true;
-          }
-        }
-        if (__any_sync(0xffffffffu, failed)) {
-          if (lane == 0 && !abort_flag) flag_error(p.status, PA_DEVFLAG_TIMEOUT);
-          abort_flag = 1;
-          ok = false;
-          break;
-        }
-        rc += n;
-      }
-      y += pc.b1 - pc.b0;
-    }
-    }
-    // Do not leave copies in flight into shared memory: wait (bounded) for the most
-    // recent fill of every stage that was issued.
-    if (lane == 0) {
-      for (int st = 0; st < kNumStages; ++st) {
-        if (rc <= st) break;
-        const int64_t last = st + ((rc - 1 - st) / kNumStages) * kNumStages;
-        if (!mbar_wait(&full_bar[st], static_cast<uint32_t>((last / kNumStages) & 1))) {
-          flag_error(p.status, PA_DEVFLAG_TIMEOUT);
-        }
-      }
-    }
-    return;
-  }
-
-  // =============================== consumer warps ================================
+  const uint64_t policy = l2_evict_first_policy();
   const int tg = lane >> 2;
   const int dq = lane & 3;
   const int par = tg & 1;
   const int c0 = dq + 4 * par;        // 16-byte chunk held in register set 0
   const int c1 = dq + 4 * (par ^ 1);  // 16-byte chunk held in register set 1
   const int ho = own_head<GROUP>(dq);
-  int done = 0;  // tiles consumed so far by this CTA (the producer's running count)
-  for (int64_t run = blockIdx.x; run < p.grid; run += gridDim.x) {
+
+  // ---- issue side: the warp's runs, walked one block-table window at a time ----
+  int64_t wc_run = gw;
+  int64_t wc_y = run_start(gw, total, p.grid, p.chunk);
+  int64_t wc_stop = run_start(gw + 1, total, p.grid, p.chunk);
+  auto next_window = [&]() -> Window {
+    while (wc_y >= wc_stop && wc_run < p.grid) {
+      wc_run += total_warps;
+      if (wc_run < p.grid) {
+        wc_y = run_start(wc_run, total, p.grid, p.chunk);
+        wc_stop = run_start(wc_run + 1, total, p.grid, p.chunk);
+      }
+    }
+    Window w;
+    w.tile = -1;
+    const int64_t left = wc_stop - wc_y;
+    w.n = wc_run < p.grid ? static_cast<int>(left < kWindow ? left : kWindow) : 0;
+    bool bad = false;
+    if (lane < w.n) {
+      const int64_t y = wc_y + lane;
+      const int s = find_seq(seq_base, S, y, KV);
+      const int nb = seq_base[s + 1] - seq_base[s];
+      const int off = static_cast<int>(y - static_cast<int64_t>(seq_base[s]) * KV);
+      const int g = off / nb;
+      const int b = off - g * nb;
+      const int32_t phys = __ldg(p.block_tables + static_cast<int64_t>(s) * p.max_blocks_per_seq + b);
+      bad = phys < 0 || phys >= p.num_blocks;
+      w.tile = bad ? -1 : phys * KV + g;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) flag_error(p.status, PA_DEVFLAG_BAD_BLOCK);
+    wc_y += w.n;
+    return w;
+  };
+  Window cur = next_window();
+  Window nxt = next_window();
+  int cur_i = 0;
+  int issued = 0;
+  auto issue_one = [&]() {
+    if (cur_i >= cur.n) {
+      cur = nxt;
+      cur_i = 0;
+      if (cur.n == 0) return;  // nothing left to issue
+      nxt = next_window();
+    }
+    const int32_t t = __shfl_sync(0xffffffffu, cur.tile, cur_i);
+    const int st = issued % kStagesPerWarp;
+    if (lane == 0) {
+      if (t >= 0) {
+        mbar_arrive_expect_tx(&full_bar[st], 2 * kTileBytes);
+        const size_t off = static_cast<size_t>(t) * kTileBytes;
+        uint8_t* dst = ring + st * 2 * kTileBytes;
+        bulk_copy_g2s(dst, p.key_cache + off, kTileBytes, &full_bar[st], policy);
+        bulk_copy_g2s(dst + kTileBytes, p.value_cache + off, kTileBytes, &full_bar[st], policy);
+      } else {
+        mbar_arrive(&full_bar[st]);  // invalid block: release the stage with stale data
+      }
+    }
+    ++issued;
+    ++cur_i;
+  };
+  for (int i = 0; i < kStagesPerWarp; ++i) issue_one();
+
+  // ---- consume side: same runs, piece by piece ----
+  int consumed = 0;
+  bool ok = true;
+  for (int64_t run = gw; run < p.grid; run += total_warps) {
   const int64_t start = run_start(run, total, p.grid, p.chunk);
   const int64_t stop = run_start(run + 1, total, p.grid, p.chunk);
   for (int64_t y = start; y < stop;) {
@@ -412,10 +424,8 @@ paged_decode_kernel(const KParams p) {
     for (int h = 0; h < GROUP; ++h) {
       const __nv_bfloat16* qrow =
           p.q + (static_cast<int64_t>(pc.s) * p.num_q_heads + pc.g * GROUP + h) * kHeadDim;
-      const uint4 a = ldg_nc128(qrow + c0 * 8);
-      const uint4 b = ldg_nc128(qrow + c1 * 8);
       float2 f[8];
-      unpack8(a, b, f);
+      unpack8(ldg_nc128(qrow + c0 * 8), ldg_nc128(qrow + c1 * 8), f);
 #pragma unroll
       for (int i = 0; i < 8; ++i) qf[h][i] = make_float2(f[i].x * p.q_scale, f[i].y * p.q_scale);
     }
@@ -427,16 +437,12 @@ paged_decode_kernel(const KParams p) {
       for (int i = 0; i < 8; ++i) o[h][i] = make_float2(0.f, 0.f);
     }
 
-    // This warp takes the piece's tiles with running index = warp (mod W); stage and phase
-    // advance by W per tile (kNumStages is a multiple of W).
-    const int first_k = (warp - done % kNumConsumerWarps + kNumConsumerWarps) % kNumConsumerWarps;
-    int st = (done + first_k) % kNumStages;
-    uint32_t phase = static_cast<uint32_t>(((done + first_k) / kNumStages) & 1);
-    const bool aborted = __any_sync(0xffffffffu, abort_flag != 0);
-    for (int k = first_k; k < ntiles && !aborted; k += kNumConsumerWarps) {
+    for (int k = 0; k < ntiles && ok; ++k) {
+      const int st = consumed % kStagesPerWarp;
+      const uint32_t phase = static_cast<uint32_t>((consumed / kStagesPerWarp) & 1);
       if (!__all_sync(0xffffffffu, mbar_wait(&full_bar[st], phase))) {
         if (lane == 0) flag_error(p.status, PA_DEVFLAG_TIMEOUT);
-        abort_flag = 1;
+        ok = false;
         break;
       }
       const uint8_t* kt = ring + st * 2 * kTileBytes;
@@ -448,93 +454,75 @@ paged_decode_kernel(const KParams p) {
         attend_tile<GROUP, true>(kt, vt, lane, tg, dq, c0, c1, valid, qf, m, l, o);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[st]);
-      st += kNumConsumerWarps;
-      if (st >= kNumStages) {
-        st -= kNumStages;
-        phase ^= 1u;
-      }
+      // every lane's reads of this stage are done: order them before the refill's async write
+      if (lane == 0) fence_proxy_async_smem();
+      ++consumed;
+      issue_one();
     }
 
-    // ---- merge the (warp, token-group) online-softmax states of this piece ----
-    // warp maximum of each head: lanes with the same dq own the same head
-    float mw = m;
-    mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 4));
-    mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 8));
-    mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 16));
-    if (tg == 0) red_m[warp * GROUP + ho] = mw;
-    named_barrier_sync(1, kConsumerThreads);
-    float M_own = red_m[ho];
-#pragma unroll
-    for (int w = 1; w < kNumConsumerWarps; ++w) M_own = fmaxf(M_own, red_m[w * GROUP + ho]);
-    const float f_own = m == -INFINITY ? 0.f : fast_exp2(m - M_own);
-    l *= f_own;
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+    // ---- combine the warp's 8 token-group states through shared memory ----
+    m_s[ho * 8 + tg] = m;  // lanes owning the same head write the same value
+    l_s[ho * 8 + tg] = l;
 #pragma unroll
     for (int h = 0; h < GROUP; ++h) {
-      const float fh = from_owner<GROUP>(f_own, lane, h);
-      const float2 ff = make_float2(fh, fh);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) o[h][i] = __fmul2_rn(o[h][i], ff);
-      if (par) {  // odd token groups hold chunk dq+4 in set 0: align before summing
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 tmp = o[h][i];
-          o[h][i] = o[h][i + 4];
-          o[h][i + 4] = tmp;
-        }
-      }
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          o[h][i].x += __shfl_xor_sync(0xffffffffu, o[h][i].x, off);
-          o[h][i].y += __shfl_xor_sync(0xffffffffu, o[h][i].y, off);
-        }
-      }
+      float* row = o_s + tg * kORow + h * kHeadDim;
+      *reinterpret_cast<float4*>(row + 8 * c0) = make_float4(o[h][0].x, o[h][0].y, o[h][1].x, o[h][1].y);
+      *reinterpret_cast<float4*>(row + 8 * c0 + 4) = make_float4(o[h][2].x, o[h][2].y, o[h][3].x, o[h][3].y);
+      *reinterpret_cast<float4*>(row + 8 * c1) = make_float4(o[h][4].x, o[h][4].y, o[h][5].x, o[h][5].y);
+      *reinterpret_cast<float4*>(row + 8 * c1 + 4) = make_float4(o[h][6].x, o[h][6].y, o[h][7].x, o[h][7].y);
     }
-    if (tg == 0) {
+    __syncwarp();
+    const int e0 = lane * 8;  // this lane combines outputs e0 .. e0+7 of the GROUP x 64
+    if (e0 < GROUP * kHeadDim) {
+      const int h = e0 / kHeadDim;
+      const int d0 = e0 % kHeadDim;
+      float mh = -INFINITY;
 #pragma unroll
-      for (int h = 0; h < GROUP; ++h) {
-        float* dst = red_o + (warp * GROUP + h) * kHeadDim;
-        float4* lo = reinterpret_cast<float4*>(dst + 8 * dq);
-        float4* hi = reinterpret_cast<float4*>(dst + 8 * (dq + 4));
-        lo[0] = make_float4(o[h][0].x, o[h][0].y, o[h][1].x, o[h][1].y);
-        lo[1] = make_float4(o[h][2].x, o[h][2].y, o[h][3].x, o[h][3].y);
-        hi[0] = make_float4(o[h][4].x, o[h][4].y, o[h][5].x, o[h][5].y);
-        hi[1] = make_float4(o[h][6].x, o[h][6].y, o[h][7].x, o[h][7].y);
-      }
-      red_l[warp * GROUP + ho] = l;
-    }
-    named_barrier_sync(1, kConsumerThreads);
-    for (int e = tid; e < GROUP * kHeadDim; e += kConsumerThreads) {
-      const int h = e / kHeadDim;
-      const int d = e % kHeadDim;
-      float acc = 0.f, lsum = 0.f, mh = -INFINITY;
+      for (int t = 0; t < 8; ++t) mh = fmaxf(mh, m_s[h * 8 + t]);
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float lsum = 0.f;
 #pragma unroll
-      for (int w = 0; w < kNumConsumerWarps; ++w) {
-        acc += red_o[(w * GROUP + h) * kHeadDim + d];
-        lsum += red_l[w * GROUP + h];
-        mh = fmaxf(mh, red_m[w * GROUP + h]);
+      for (int t = 0; t < 8; ++t) {
+        const float mt = m_s[h * 8 + t];
+        const float f = mt == -INFINITY ? 0.f : fast_exp2(mt - mh);
+        lsum += f * l_s[h * 8 + t];
+        const float4 a = *reinterpret_cast<const float4*>(o_s + t * kORow + e0);
+        const float4 b = *reinterpret_cast<const float4*>(o_s + t * kORow + e0 + 4);
+        acc[0] += f * a.x; acc[1] += f * a.y; acc[2] += f * a.z; acc[3] += f * a.w;
+        acc[4] += f * b.x; acc[5] += f * b.y; acc[6] += f * b.z; acc[7] += f * b.w;
       }
       if (whole) {
+        const float inv = 1.f / lsum;
         const int64_t row = static_cast<int64_t>(pc.s) * p.num_q_heads + pc.g * GROUP + h;
-        p.out[row * kHeadDim + d] = __float2bfloat16_rn(acc / lsum);
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+          w[i] = *reinterpret_cast<const uint32_t*>(&b2);
+        }
+        *reinterpret_cast<uint4*>(p.out + row * kHeadDim + d0) = make_uint4(w[0], w[1], w[2], w[3]);
       } else {
         const int slot = first_piece ? 0 : 1;
         float* dst = p.partials + ((run * 2 + slot) * GROUP + h) * kPartialFloats;
-        dst[d] = acc;
-        if (d == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<float2*>(dst + d0 + 2 * i) = make_float2(acc[2 * i], acc[2 * i + 1]);
+        if (d0 == 0) {
           dst[kHeadDim] = mh;
           dst[kHeadDim + 1] = lsum;
         }
       }
     }
-    named_barrier_sync(1, kConsumerThreads);  // scratch is reused by the next piece
+    __syncwarp();  // scratch is reused by the next piece
     y += ntiles;
-    done += ntiles;
   }
+  }
+  // After a timeout, leave no copy in flight into this warp's ring (bounded waits).
+  if (!ok && lane == 0) {
+    for (int t = consumed; t < issued; ++t) {
+      if (!mbar_wait(&full_bar[t % kStagesPerWarp],
+                     static_cast<uint32_t>((t / kStagesPerWarp) & 1))) break;
+    }
   }
 }
 
@@ -669,7 +657,7 @@ cudaError_t occupancy(int num_seqs, int* ctas_per_sm) {
   cudaError_t e = prepare_kernel<GROUP>();
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      ctas_per_sm, paged_decode_kernel<GROUP>, (kNumConsumerWarps + 1) * 32,
+      ctas_per_sm, paged_decode_kernel<GROUP>, kWarps * 32,
       smem_bytes<GROUP>(num_seqs));
 }
 
@@ -697,7 +685,7 @@ cudaError_t launch(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t str
   p.ws_seq_base = reinterpret_cast<int32_t*>(ws + 16);
   p.partials = reinterpret_cast<float*>(ws + plan.ws_meta_bytes);
   p.status = a.status;
-  paged_decode_kernel<GROUP><<<plan.grid, (kNumConsumerWarps + 1) * 32, plan.smem_bytes, stream>>>(p);
+  paged_decode_kernel<GROUP><<<plan.grid, kWarps * 32, plan.smem_bytes, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   merge_partials_kernel<GROUP><<<dim3(a.num_kv_heads, a.num_seqs), kMergeThreads, 0, stream>>>(p);
@@ -734,14 +722,15 @@ cudaError_t plan_decode(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_he
     runs = (tiles_upper + plan->chunk - 1) / plan->chunk;
   } else {
     plan->chunk = 0;
-    runs = resident;
-    const int64_t by_size = (tiles_upper + kMinTilesPerCta - 1) / kMinTilesPerCta;
+    runs = resident * kWarps;
+    const int64_t by_size = (tiles_upper + kMinTilesPerRun - 1) / kMinTilesPerRun;
     if (by_size < runs) runs = by_size;
   }
   if (runs < 1) runs = 1;
   if (runs > 0x7fffffff) return cudaErrorInvalidValue;
   plan->runs = static_cast<int>(runs);
-  plan->grid = static_cast<int>(runs < resident ? runs : resident);
+  const int64_t ctas = (runs + kWarps - 1) / kWarps;
+  plan->grid = static_cast<int>(ctas < resident ? ctas : resident);
   plan->ws_meta_bytes = (16 + sizeof(int32_t) * (num_seqs + 1) + 255) / 256 * 256;
   plan->workspace_bytes = plan->ws_meta_bytes +
                           static_cast<size_t>(runs) * 2 * group * kPartialFloats * sizeof(float);
