@@ -36,7 +36,7 @@ namespace pkv {
 
 namespace {
 
-constexpr int kWarps = 8;           // streaming warps per CTA, 2 per SM sub-partition
+constexpr int kWarps = 12;          // streaming warps per CTA, 3 per SM sub-partition
 constexpr int kStagesPerWarp = 4;   // private ring depth: 16 KiB in flight per warp
 constexpr int kWindow = 32;         // block-table entries fetched per window
 constexpr int kPartialFloats = kHeadDim + 2;  // o[64], max (log2 units), sum
@@ -107,21 +107,28 @@ __device__ __forceinline__ Piece piece_at(const int32_t* base, int num_seqs, int
   return pc;
 }
 
-// Query head whose score lane `dq` of a 4-lane group holds after score_for_own_head: the
-// reduce-scatter below leaves head (2 * (dq & 1) + (dq >> 1)) in lane dq for GROUP 4, head
-// (dq & 1) for GROUP 2, head 0 for GROUP 1.  The map is its own inverse, so it also gives
-// the lane that owns a head.
+// Lane layout of a streaming warp: lane = 8 * tg + dq.  Token group tg (0..3) owns tokens
+// tg, tg + 4, tg + 8, tg + 12 of a 16-token tile (one per pass); dim slice dq (0..7) owns
+// dims 8*dq .. 8*dq + 7, one 16-byte chunk of each 128-byte row, so a quarter warp reads
+// one whole row per load and every K/V element is loaded and unpacked exactly once.
+constexpr int kPasses = 4;
+
+// Query head whose score lane `dq` holds after score_for_own_head: the reduce-scatter
+// leaves head (2 * (dq & 1) + ((dq >> 1) & 1)) for GROUP 4, (dq & 1) for GROUP 2, 0 for
+// GROUP 1 (lanes dq and dq ^ 4 hold the same head).  On the low two bits the map is its own
+// inverse, so it also names the lane (within the 8-lane group) that owns a head.
 template <int GROUP>
 __device__ __forceinline__ int own_head(int dq) {
-  if (GROUP == 4) return 2 * (dq & 1) + (dq >> 1);
+  if (GROUP == 4) return 2 * (dq & 1) + ((dq >> 1) & 1);
   if (GROUP == 2) return dq & 1;
   return 0;
 }
 
-// Finish the 4-lane dot products of one token: a[h] is this lane's partial over its 16 dims.
-// Returns the full score of own_head(dq) (reduce-scatter: 3 shuffles for 4 heads).
+// Finish the 8-lane dot products of one token: a[h] is this lane's partial over its 8 dims.
+// Returns the full score of own_head(dq).
 template <int GROUP>
 __device__ __forceinline__ float score_for_own_head(const float (&a)[GROUP], int dq) {
+  float keep;
   if (GROUP == 4) {
     const bool b0 = dq & 1;
     const float send0 = b0 ? a[0] : a[2];
@@ -132,61 +139,59 @@ __device__ __forceinline__ float score_for_own_head(const float (&a)[GROUP], int
     keep1 += __shfl_xor_sync(0xffffffffu, send1, 1);
     const bool b1 = dq & 2;
     const float send = b1 ? keep0 : keep1;
-    const float keep = b1 ? keep1 : keep0;
-    return keep + __shfl_xor_sync(0xffffffffu, send, 2);
+    keep = (b1 ? keep1 : keep0) + __shfl_xor_sync(0xffffffffu, send, 2);
   } else if (GROUP == 2) {
     const bool b0 = dq & 1;
-    float keep = (b0 ? a[1] : a[0]) + __shfl_xor_sync(0xffffffffu, b0 ? a[0] : a[1], 1);
-    return keep + __shfl_xor_sync(0xffffffffu, keep, 2);
+    keep = (b0 ? a[1] : a[0]) + __shfl_xor_sync(0xffffffffu, b0 ? a[0] : a[1], 1);
+    keep += __shfl_xor_sync(0xffffffffu, keep, 2);
   } else {
-    float v = a[0] + __shfl_xor_sync(0xffffffffu, a[0], 1);
-    return v + __shfl_xor_sync(0xffffffffu, v, 2);
+    keep = a[0] + __shfl_xor_sync(0xffffffffu, a[0], 1);
+    keep += __shfl_xor_sync(0xffffffffu, keep, 2);
   }
+  return keep + __shfl_xor_sync(0xffffffffu, keep, 4);
 }
 
-// Value of `v` held by the owner lane of head h in this lane's 4-lane group.
+// Value of `v` held by the owner lane of head h in this lane's 8-lane group.
 template <int GROUP>
 __device__ __forceinline__ float from_owner(float v, int lane, int h) {
   if (GROUP == 1) return v;
-  return __shfl_sync(0xffffffffu, v, (lane & ~3) | own_head<GROUP>(h));
+  return __shfl_sync(0xffffffffu, v, (lane & ~7) | own_head<GROUP>(h));
 }
 
-__device__ __forceinline__ void unpack8(uint4 a, uint4 b, float2 (&f)[8]) {
-  f[0] = bf16x2_to_float2(a.x); f[1] = bf16x2_to_float2(a.y);
-  f[2] = bf16x2_to_float2(a.z); f[3] = bf16x2_to_float2(a.w);
-  f[4] = bf16x2_to_float2(b.x); f[5] = bf16x2_to_float2(b.y);
-  f[6] = bf16x2_to_float2(b.z); f[7] = bf16x2_to_float2(b.w);
+__device__ __forceinline__ void unpack4(uint4 a, float2 (&f)[4]) {
+  f[0] = bf16x2_to_float2(a.x);
+  f[1] = bf16x2_to_float2(a.y);
+  f[2] = bf16x2_to_float2(a.z);
+  f[3] = bf16x2_to_float2(a.w);
 }
 
-// Process one 16-token tile pair held in shared memory.  Lane (tg, dq) handles tokens tg
-// and tg + 8; its 16 dims are the 16-byte chunks c0 (set 0) and c1 (set 1) of each row.
-// After the score reduction the lane keeps the online-softmax state (m, l) of one query
-// head; its output slice o covers every head of the group.  m is the running reference
-// maximum in log2 units, raised only when a score exceeds it by more than 2^8.
+// One 16-token tile pair held in shared memory.  The lane keeps the online-softmax state
+// (m, l) of its own head; m is the running reference maximum in log2 units, raised only
+// when a score exceeds it by more than 2^8.  o covers every head of the group on the
+// lane's 8 dims.
 template <int GROUP, bool TAIL>
 __device__ __forceinline__ void attend_tile(const uint8_t* __restrict__ kt,
                                             const uint8_t* __restrict__ vt, int lane, int tg,
-                                            int dq, int c0, int c1, int valid_tokens,
-                                            const float2 (&qf)[GROUP][8], float& m, float& l,
-                                            float2 (&o)[GROUP][8]) {
-  float s[2];
+                                            int dq, int valid_tokens,
+                                            const float2 (&qf)[GROUP][4], float& m, float& l,
+                                            float2 (&o)[GROUP][4]) {
+  float s[kPasses];
 #pragma unroll
-  for (int step = 0; step < 2; ++step) {
-    const uint8_t* krow = kt + (tg + 8 * step) * kRowBytes;
-    float2 kf[8];
-    unpack8(lds128(krow + c0 * 16), lds128(krow + c1 * 16), kf);
+  for (int j = 0; j < kPasses; ++j) {
+    float2 kf[4];
+    unpack4(lds128(kt + (tg + 4 * j) * kRowBytes + dq * 16), kf);
     float a[GROUP];
 #pragma unroll
     for (int h = 0; h < GROUP; ++h) {
       float2 acc = __fmul2_rn(qf[h][0], kf[0]);
 #pragma unroll
-      for (int i = 1; i < 8; ++i) acc = __ffma2_rn(qf[h][i], kf[i], acc);
+      for (int i = 1; i < 4; ++i) acc = __ffma2_rn(qf[h][i], kf[i], acc);
       a[h] = acc.x + acc.y;
     }
-    s[step] = score_for_own_head<GROUP>(a, dq);
-    if (TAIL && tg + 8 * step >= valid_tokens) s[step] = -INFINITY;
+    s[j] = score_for_own_head<GROUP>(a, dq);
+    if (TAIL && tg + 4 * j >= valid_tokens) s[j] = -INFINITY;
   }
-  const float mt = fmaxf(s[0], s[1]);
+  const float mt = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
   const bool grow = mt - m > kRescaleThreshold;  // first tile: m = -inf
   if (__any_sync(0xffffffffu, grow)) {
     const float alpha = grow ? fast_exp2(m - mt) : 1.f;
@@ -199,49 +204,37 @@ __device__ __forceinline__ void attend_tile(const uint8_t* __restrict__ kt,
       const float ah = from_owner<GROUP>(alpha, lane, h);
       const float2 aa = make_float2(ah, ah);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) o[h][i] = __fmul2_rn(o[h][i], aa);
+      for (int i = 0; i < 4; ++i) o[h][i] = __fmul2_rn(o[h][i], aa);
     }
   }
-  float pr[2];
+  float pr[kPasses];
 #pragma unroll
-  for (int step = 0; step < 2; ++step) {
-    pr[step] = fast_exp2(s[step] - m);
-    if (TAIL && tg + 8 * step >= valid_tokens) pr[step] = 0.f;  // also covers m = -inf
+  for (int j = 0; j < kPasses; ++j) {
+    pr[j] = fast_exp2(s[j] - m);
+    if (TAIL && tg + 4 * j >= valid_tokens) pr[j] = 0.f;  // also covers m = -inf
   }
-  l += pr[0] + pr[1];
+  l += (pr[0] + pr[1]) + (pr[2] + pr[3]);
 #pragma unroll
-  for (int step = 0; step < 2; ++step) {
-    const uint8_t* vrow = vt + (tg + 8 * step) * kRowBytes;
-    uint4 va = lds128(vrow + c0 * 16);
-    uint4 vb = lds128(vrow + c1 * 16);
-    if (TAIL && tg + 8 * step >= valid_tokens) {  // unused slots may hold NaN: never multiply
-      va = make_uint4(0, 0, 0, 0);
-      vb = make_uint4(0, 0, 0, 0);
-    }
-    float2 vf[8];
-    unpack8(va, vb, vf);
+  for (int j = 0; j < kPasses; ++j) {
+    uint4 va = lds128(vt + (tg + 4 * j) * kRowBytes + dq * 16);
+    if (TAIL && tg + 4 * j >= valid_tokens) va = make_uint4(0, 0, 0, 0);  // may hold NaN
+    float2 vf[4];
+    unpack4(va, vf);
 #pragma unroll
     for (int h = 0; h < GROUP; ++h) {
-      const float ph = from_owner<GROUP>(pr[step], lane, h);
+      const float ph = from_owner<GROUP>(pr[j], lane, h);
       const float2 pp = make_float2(ph, ph);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) o[h][i] = __ffma2_rn(pp, vf[i], o[h][i]);
+      for (int i = 0; i < 4; ++i) o[h][i] = __ffma2_rn(pp, vf[i], o[h][i]);
     }
   }
-}
-
-template <int GROUP>
-__host__ __device__ constexpr int o_row_floats() {  // one token group's output slice in the merge scratch (+pad)
-  return GROUP * kHeadDim + 4;
 }
 
 template <int GROUP>
 constexpr size_t decode_smem_fixed() {
   return static_cast<size_t>(kWarps) *
-         (kStagesPerWarp * 2 * kTileBytes                           // private K+V rings
-          + 8 * o_row_floats<GROUP>() * sizeof(float)                // o of 8 token groups
-          + 2 * GROUP * 8 * sizeof(float)                            // m, l of 8 token groups
-          + kStagesPerWarp * sizeof(uint64_t));                      // full barriers
+         (kStagesPerWarp * 2 * kTileBytes          // private K+V rings
+          + kStagesPerWarp * sizeof(uint64_t));    // full barriers
 }
 
 // Block-table window: lane j holds the tile (phys_block * Hkv + kv_head) of the j-th of
@@ -255,9 +248,6 @@ template <int GROUP>
 __global__ void __launch_bounds__(kWarps * 32, 1)
 paged_decode_kernel(const KParams p) {
   constexpr int kThreads = kWarps * 32;
-  constexpr int kORow = o_row_floats<GROUP>();
-  static_assert((kWarps * kStagesPerWarp * 2 * kTileBytes) % 16 == 0, "scratch alignment");
-  static_assert((kORow * sizeof(float)) % 16 == 0, "scratch rows take 16-byte stores");
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -266,11 +256,7 @@ paged_decode_kernel(const KParams p) {
   const int KV = p.num_kv_heads;
 
   uint8_t* ring = smem + warp * (kStagesPerWarp * 2 * kTileBytes);
-  float* scratch = reinterpret_cast<float*>(smem + kWarps * kStagesPerWarp * 2 * kTileBytes);
-  float* o_s = scratch + warp * 8 * kORow;                           // [8 tg][kORow]
-  float* m_s = scratch + kWarps * 8 * kORow + warp * 2 * GROUP * 8;  // [GROUP][8 tg]
-  float* l_s = m_s + GROUP * 8;                                      // [GROUP][8 tg]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(scratch + kWarps * 8 * kORow + kWarps * 2 * GROUP * 8);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kStagesPerWarp * 2 * kTileBytes);
   uint64_t* full_bar = bars + warp * kStagesPerWarp;
   int32_t* seq_base = reinterpret_cast<int32_t*>(bars + kWarps * kStagesPerWarp);
   __shared__ int64_t warp_sums[kWarps];
@@ -338,12 +324,8 @@ paged_decode_kernel(const KParams p) {
   if (gw >= p.grid) return;
 
   const uint64_t policy = l2_evict_first_policy();
-  const int tg = lane >> 2;
-  const int dq = lane & 3;
-  const int par = tg & 1;
-  const int c0 = dq + 4 * par;        // 16-byte chunk held in register set 0
-  const int c1 = dq + 4 * (par ^ 1);  // 16-byte chunk held in register set 1
-  const int ho = own_head<GROUP>(dq);
+  const int tg = lane >> 3;  // token group
+  const int dq = lane & 7;   // dim slice: dims 8*dq .. 8*dq+7
 
   // ---- issue side: the warp's runs, walked one block-table window at a time ----
   int64_t wc_run = gw;
@@ -407,7 +389,7 @@ paged_decode_kernel(const KParams p) {
   for (int i = 0; i < kStagesPerWarp; ++i) issue_one();
 
   // ---- consume side: same runs, piece by piece ----
-  int consumed = 0;
+  int waited = 0;  // tiles whose data this warp has waited for (stage = waited % stages)
   bool ok = true;
   for (int64_t run = gw; run < p.grid; run += total_warps) {
   const int64_t start = run_start(run, total, p.grid, p.chunk);
@@ -419,107 +401,104 @@ paged_decode_kernel(const KParams p) {
     const bool first_piece = y == start;
     const int ntiles = pc.b1 - pc.b0;
 
-    float2 qf[GROUP][8];
+    float2 qf[GROUP][4];
 #pragma unroll
     for (int h = 0; h < GROUP; ++h) {
       const __nv_bfloat16* qrow =
           p.q + (static_cast<int64_t>(pc.s) * p.num_q_heads + pc.g * GROUP + h) * kHeadDim;
-      float2 f[8];
-      unpack8(ldg_nc128(qrow + c0 * 8), ldg_nc128(qrow + c1 * 8), f);
+      float2 f[4];
+      unpack4(ldg_nc128(qrow + dq * 8), f);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) qf[h][i] = make_float2(f[i].x * p.q_scale, f[i].y * p.q_scale);
+      for (int i = 0; i < 4; ++i) qf[h][i] = make_float2(f[i].x * p.q_scale, f[i].y * p.q_scale);
     }
     float m = -INFINITY, l = 0.f;
-    float2 o[GROUP][8];
+    float2 o[GROUP][4];
 #pragma unroll
     for (int h = 0; h < GROUP; ++h) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) o[h][i] = make_float2(0.f, 0.f);
+      for (int i = 0; i < 4; ++i) o[h][i] = make_float2(0.f, 0.f);
     }
 
     for (int k = 0; k < ntiles && ok; ++k) {
-      const int st = consumed % kStagesPerWarp;
-      const uint32_t phase = static_cast<uint32_t>((consumed / kStagesPerWarp) & 1);
+      const int st = waited % kStagesPerWarp;
+      const uint32_t phase = static_cast<uint32_t>((waited / kStagesPerWarp) & 1);
       if (!__all_sync(0xffffffffu, mbar_wait(&full_bar[st], phase))) {
         if (lane == 0) flag_error(p.status, PA_DEVFLAG_TIMEOUT);
         ok = false;
         break;
       }
+      ++waited;
       const uint8_t* kt = ring + st * 2 * kTileBytes;
       const uint8_t* vt = kt + kTileBytes;
       const int valid = L - (pc.b0 + k) * kBlockSize;
       if (valid >= kBlockSize) {
-        attend_tile<GROUP, false>(kt, vt, lane, tg, dq, c0, c1, kBlockSize, qf, m, l, o);
+        attend_tile<GROUP, false>(kt, vt, lane, tg, dq, kBlockSize, qf, m, l, o);
       } else {
-        attend_tile<GROUP, true>(kt, vt, lane, tg, dq, c0, c1, valid, qf, m, l, o);
+        attend_tile<GROUP, true>(kt, vt, lane, tg, dq, valid, qf, m, l, o);
       }
       __syncwarp();
       // every lane's reads of this stage are done: order them before the refill's async write
       if (lane == 0) fence_proxy_async_smem();
-      ++consumed;
       issue_one();
     }
 
-    // ---- combine the warp's 8 token-group states through shared memory ----
-    m_s[ho * 8 + tg] = m;  // lanes owning the same head write the same value
-    l_s[ho * 8 + tg] = l;
+    // ---- combine the warp's 4 token-group states (lanes with the same dq own one head) ----
+    float mh = m;
+    mh = fmaxf(mh, __shfl_xor_sync(0xffffffffu, mh, 8));
+    mh = fmaxf(mh, __shfl_xor_sync(0xffffffffu, mh, 16));
+    const float f_own = m == -INFINITY ? 0.f : fast_exp2(m - mh);
+    float lsum = l * f_own;
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 8);
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);
 #pragma unroll
     for (int h = 0; h < GROUP; ++h) {
-      float* row = o_s + tg * kORow + h * kHeadDim;
-      *reinterpret_cast<float4*>(row + 8 * c0) = make_float4(o[h][0].x, o[h][0].y, o[h][1].x, o[h][1].y);
-      *reinterpret_cast<float4*>(row + 8 * c0 + 4) = make_float4(o[h][2].x, o[h][2].y, o[h][3].x, o[h][3].y);
-      *reinterpret_cast<float4*>(row + 8 * c1) = make_float4(o[h][4].x, o[h][4].y, o[h][5].x, o[h][5].y);
-      *reinterpret_cast<float4*>(row + 8 * c1 + 4) = make_float4(o[h][6].x, o[h][6].y, o[h][7].x, o[h][7].y);
-    }
-    __syncwarp();
-    const int e0 = lane * 8;  // this lane combines outputs e0 .. e0+7 of the GROUP x 64
-    if (e0 < GROUP * kHeadDim) {
-      const int h = e0 / kHeadDim;
-      const int d0 = e0 % kHeadDim;
-      float mh = -INFINITY;
+      const float fh = from_owner<GROUP>(f_own, lane, h);
+      const float2 ff = make_float2(fh, fh);
 #pragma unroll
-      for (int t = 0; t < 8; ++t) mh = fmaxf(mh, m_s[h * 8 + t]);
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      float lsum = 0.f;
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const float mt = m_s[h * 8 + t];
-        const float f = mt == -INFINITY ? 0.f : fast_exp2(mt - mh);
-        lsum += f * l_s[h * 8 + t];
-        const float4 a = *reinterpret_cast<const float4*>(o_s + t * kORow + e0);
-        const float4 b = *reinterpret_cast<const float4*>(o_s + t * kORow + e0 + 4);
-        acc[0] += f * a.x; acc[1] += f * a.y; acc[2] += f * a.z; acc[3] += f * a.w;
-        acc[4] += f * b.x; acc[5] += f * b.y; acc[6] += f * b.z; acc[7] += f * b.w;
+      for (int i = 0; i < 4; ++i) {
+        float2 v = __fmul2_rn(o[h][i], ff);
+        v.x += __shfl_xor_sync(0xffffffffu, v.x, 8);
+        v.y += __shfl_xor_sync(0xffffffffu, v.y, 8);
+        v.x += __shfl_xor_sync(0xffffffffu, v.x, 16);
+        v.y += __shfl_xor_sync(0xffffffffu, v.y, 16);
+        o[h][i] = v;
       }
-      if (whole) {
-        const float inv = 1.f / lsum;
-        const int64_t row = static_cast<int64_t>(pc.s) * p.num_q_heads + pc.g * GROUP + h;
-        uint32_t w[4];
+    }
+    // token group 0 (lanes 0..7) now holds the sums of dims 8*dq .. 8*dq+7 of every head
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-          w[i] = *reinterpret_cast<const uint32_t*>(&b2);
-        }
-        *reinterpret_cast<uint4*>(p.out + row * kHeadDim + d0) = make_uint4(w[0], w[1], w[2], w[3]);
-      } else {
-        const int slot = first_piece ? 0 : 1;
-        float* dst = p.partials + ((run * 2 + slot) * GROUP + h) * kPartialFloats;
+    for (int h = 0; h < GROUP; ++h) {
+      const float hm = from_owner<GROUP>(mh, lane, h);
+      const float hl = from_owner<GROUP>(lsum, lane, h);
+      if (tg == 0) {
+        if (whole) {
+          const float inv = 1.f / hl;
+          const int64_t row = static_cast<int64_t>(pc.s) * p.num_q_heads + pc.g * GROUP + h;
+          uint32_t w[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          *reinterpret_cast<float2*>(dst + d0 + 2 * i) = make_float2(acc[2 * i], acc[2 * i + 1]);
-        if (d0 == 0) {
-          dst[kHeadDim] = mh;
-          dst[kHeadDim + 1] = lsum;
+          for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(o[h][i].x * inv, o[h][i].y * inv);
+            w[i] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          *reinterpret_cast<uint4*>(p.out + row * kHeadDim + dq * 8) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+          const int slot = first_piece ? 0 : 1;
+          float* dst = p.partials + ((run * 2 + slot) * GROUP + h) * kPartialFloats;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) *reinterpret_cast<float2*>(dst + dq * 8 + 2 * i) = o[h][i];
+          if (dq == 0) {
+            dst[kHeadDim] = hm;
+            dst[kHeadDim + 1] = hl;
+          }
         }
       }
     }
-    __syncwarp();  // scratch is reused by the next piece
     y += ntiles;
   }
   }
   // After a timeout, leave no copy in flight into this warp's ring (bounded waits).
   if (!ok && lane == 0) {
-    for (int t = consumed; t < issued; ++t) {
+    for (int t = waited; t < issued; ++t) {
       if (!mbar_wait(&full_bar[t % kStagesPerWarp],
                      static_cast<uint32_t>((t / kStagesPerWarp) & 1))) break;
     }
