@@ -44,9 +44,30 @@ def parse_args():
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--traffic", type=float, default=None,
-                    help="DRAM bytes per decode launch from an ncu capture (for roofline)")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="override the workload's layer count (small cases for profilers)")
     return ap.parse_args()
+
+
+def ncu_traffic(cfg: int):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on
+    this workload with the current decode source (else None)."""
+    import hashlib
+    src = os.path.join(ROOT, "paged_kv_cache_299_gb300", "csrc", "decode.cu")
+    summary = os.path.join(ROOT, "profiles", "paged_decode_kernel.md")
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        fields = {}
+        for line in open(summary):
+            if "=" in line and line.strip().startswith(("source_sha256", "config")):
+                k, v = line.split("=", 1)
+                fields[k.strip()] = v.strip()
+        if fields.get("source_sha256") != digest:
+            return None
+        v = fields.get(f"config{cfg}_dram_bytes_per_launch")
+        return int(v) if v else None
+    except Exception:
+        return None
 
 
 def measured_peaks():
@@ -59,9 +80,13 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def workload(cfg: int):
+def workload(cfg: int, layers=None, seed_offset=0):
     from paged_kv_cache_299_gb300 import workloads as wl
-    return wl.CONFIGS[cfg]()
+    make = wl.CONFIGS[cfg]
+    w = make() if not seed_offset else make(seed=make().seed + seed_offset)
+    if layers is not None:
+        w.layers = int(layers)
+    return w
 
 
 def describe(w) -> dict:
@@ -184,7 +209,7 @@ class DeviceStep:
         if w.num_decode:
             need = pa.pa_decode_workspace_size(w.num_decode, w.num_kv_heads, w.num_q_heads,
                                                self.max_ctx_dec, w.partition_tokens)
-            self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+            self.ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
         assert pa.pa_check_device_status(self.status) == pa.PA_OK
 
     def launches_per_step(self) -> int:
@@ -218,10 +243,8 @@ def run_gpu(args, rank, world):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = workload(args.config)
-    if world > 1:  # weak scaling: every rank serves its own batch (seed offset)
-        from paged_kv_cache_299_gb300 import workloads as wl
-        w = wl.CONFIGS[args.config](seed=w.seed + 100 * rank)
+    # weak scaling: every rank serves its own batch (seed offset per rank)
+    w = workload(args.config, args.layers, 100 * rank if world > 1 else 0)
     st = DeviceStep(w, dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     kv_bytes = w.decode_kv_bytes()
@@ -301,8 +324,9 @@ def run_gpu(args, rank, world):
         achieved = per_launch / (dec_ms * 1e-3) / 1e9
         res["roofline"] = {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": args.traffic,
-            "kernel": "pa_decode (paged_decode_kernel + merge_partials_kernel)",
+            "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.config),
+            "kernel": "pa_decode: paged_decode_kernel (split-KV merge in-kernel up to "
+                      "8192-token contexts, else + merge_partials_kernel)",
             "peak_source": f"{peak_src} hbm_gbs", "pct_of_8tbs": round(100 * achieved / 8000, 2),
             "launch_ms": round(dec_ms, 5), "algorithmic_bytes_per_launch": int(per_launch)}
     if e2e:
@@ -410,7 +434,7 @@ def cpu_baseline(w, cfg: int, target_s: float) -> dict:
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    w = workload(args.config)
+    w = workload(args.config, args.layers)
     sw, step, kv = oracle_sample(w, 4)
     for _ in range(args.warmup):
         step()

@@ -101,8 +101,11 @@ pa_status pa_reshape_and_cache(const void* key, const void* value,
                                int32_t* device_status, pa_stream_t stream);
 
 /* Bytes of device workspace pa_decode needs for these sizes on the current device
- * (0 when the sizes are invalid).  The workspace holds the split-KV partial results and
- * the per-sequence block offsets; it needs no initialisation. */
+ * (0 when the sizes are invalid).  The workspace holds the split-KV partial results, the
+ * per-sequence block offsets and one piece counter per (sequence, kv head).  Zero-fill it
+ * once before its first use; every completed call leaves the counters at zero again, so
+ * the same buffer can be reused call after call (zero it again after a call that reported
+ * a device-side error). */
 size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_heads,
                                 int32_t max_context_len, int32_t partition_tokens);
 
@@ -120,7 +123,8 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t 
  *   max_context_len  host-known upper bound of context_lens (sizes the grid)
  *   partition_tokens 0 = split evenly over the device; else a multiple of 16 giving
  *                    the run length in tokens
- *   workspace        device buffer of >= pa_decode_workspace_size(...) bytes
+ *   workspace        zero-initialised device buffer of >= pa_decode_workspace_size(...)
+ *                    bytes (see pa_decode_workspace_size)
  * num_seqs == 0 is a no-op.  At most 4096 sequences per call. */
 pa_status pa_decode(void* out, const void* q, const void* key_cache, const void* value_cache,
                     pa_cache_desc cd, const int32_t* block_tables,
@@ -162,10 +166,11 @@ pa_status pa_prefill_chunk(void* out, const void* q, const int32_t* query_start_
  *     short fixed partitions over very long contexts may not.
  *   - The first call on a device looks up the array's device address (once per device,
  *     with that device current); make that first call before any stream capture.
- *   - All calls share the array and it keeps the last call's contents.  Nothing in it has
- *     to start at zero (each call writes every entry it later reads), but calls that can
- *     overlap on the GPU (different streams, or different host threads) race on it: order
- *     them on one stream.
+ *   - All calls share the array and it keeps the last call's contents.  The only part
+ *     that must start at zero, the per-segment piece counters, is zero when the library
+ *     loads and every completed call leaves it at zero; everything else is written before
+ *     it is read.  Calls that can overlap on the GPU (different streams, or different host
+ *     threads) race on the array: order them on one stream.
  *   - No allocation of any kind happens inside this call. */
 #define PA_DECODE_STATIC_SCRATCH_BYTES ((size_t)4 << 20)
 pa_status pa_decode_static_scratch(void* out, const void* q, const void* key_cache,

@@ -186,7 +186,7 @@ def pa_decode(out, q, key_cache, value_cache, block_tables, context_lens, scale,
     if workspace is None:
         need = pa_decode_workspace_size(num_seqs, key_cache.shape[1], hq, max_context_len,
                                         partition_tokens)
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=q.device)
     _need(workspace, "workspace", torch.uint8, 1)
     st = load().pa_decode(_ptr(out), _ptr(q), _ptr(key_cache), _ptr(value_cache),
                           cache_desc(key_cache), _ptr(block_tables), block_tables.shape[1],

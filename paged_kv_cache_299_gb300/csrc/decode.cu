@@ -42,6 +42,9 @@ constexpr int kWindow = 32;         // block-table entries fetched per window
 constexpr int kPartialFloats = kHeadDim + 2;  // o[64], max (log2 units), sum
 constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale when max grows > 2^8
 constexpr int kMinTilesPerRun = 4;
+// Longest context whose split segments are merged inside the attention kernel; longer ones
+// (many pieces per segment) go to the parallel merge kernel.
+constexpr int kFusedMergeMaxContext = 8192;
 constexpr int kMaxSeqs = 4096;
 constexpr int kMergeThreads = 256;
 
@@ -64,6 +67,9 @@ struct KParams {
   int64_t* ws_total;    // total tiles, written by CTA 0
   int32_t* ws_seq_base; // [num_seqs + 1] blocks-per-head prefix, written by CTA 0
   float* partials;      // [runs][2][GROUP][kPartialFloats]
+  int32_t* seg_count;   // [num_seqs * Hkv] pieces published per split segment (fused merge);
+                        // zero between calls: the merging warp resets its counter
+  int32_t fused_merge;  // 1: the last warp to finish a split segment merges it in place
   int32_t* status;
 };
 
@@ -244,6 +250,122 @@ struct Window {
   int n;
 };
 
+// Pieces of segment [x0, x1) (one (sequence, kv head)): the non-empty runs it touches.  The
+// first piece sits in slot 0 of its run when the segment starts the run, else in slot 1;
+// every later piece starts its run (slot 0).
+struct SegmentPieces {
+  int64_t c_first, c_last;
+  int first_slot;
+};
+
+__device__ __forceinline__ SegmentPieces segment_pieces(int64_t x0, int64_t x1, int64_t total,
+                                                        int32_t runs, int32_t chunk) {
+  SegmentPieces sp;
+  sp.c_first = run_of(x0, total, runs, chunk);
+  sp.c_last = run_of(x1 - 1, total, runs, chunk);
+  sp.first_slot = x0 == run_start(sp.c_first, total, runs, chunk) ? 0 : 1;
+  return sp;
+}
+
+// Number of pieces of a segment, and the run holding piece k (balanced splits only, which
+// is the only mode that merges inside the attention kernel).  With at least one tile per
+// run (total >= runs) every run is non-empty and piece k lies in run c_first + k; otherwise
+// every non-empty run holds exactly one tile and piece k is the run of tile x0 + k.
+__device__ __forceinline__ int segment_piece_count(const SegmentPieces& sp, int64_t x0, int64_t x1,
+                                                   int64_t total, int32_t runs) {
+  return total >= runs ? static_cast<int>(sp.c_last - sp.c_first + 1) : static_cast<int>(x1 - x0);
+}
+__device__ __forceinline__ int64_t segment_piece_run(const SegmentPieces& sp, int64_t x0, int k,
+                                                     int64_t total, int32_t runs, int32_t chunk) {
+  return total >= runs ? sp.c_first + k : run_of(x0 + k, total, runs, chunk);
+}
+
+// One warp combines all pieces of a split segment (log-sum-exp weights) and writes the bf16
+// rows of its GROUP query heads.  Lane k reads piece k's (max, sum), so the pieces' loads
+// overlap; chunks of 32 pieces are combined with a running maximum.  Partials were written
+// by other warps in this launch, so they are read through L2 (__ldcg), after the caller's
+// acquire fence.
+template <int GROUP>
+__device__ void merge_segment_in_warp(const KParams& p, const SegmentPieces& sp, int64_t x0,
+                                      int64_t x1, int64_t total, int s, int g, int lane) {
+  const int n = segment_piece_count(sp, x0, x1, total, p.grid);
+  float M[GROUP], L[GROUP];
+  float2 acc[GROUP];
+#pragma unroll
+  for (int h = 0; h < GROUP; ++h) {
+    M[h] = -INFINITY;
+    L[h] = 0.f;
+    acc[h] = make_float2(0.f, 0.f);
+  }
+  for (int base = 0; base < n; base += 32) {
+    const int k = base + lane;
+    const bool valid = k < n;
+    const float* rec = p.partials;
+    if (valid) {
+      const int64_t c = segment_piece_run(sp, x0, k, total, p.grid, p.chunk);
+      const int slot = k == 0 ? sp.first_slot : 0;
+      rec = p.partials + (c * 2 + slot) * GROUP * kPartialFloats;
+    }
+    // every head's (max, sum) of piece k, all loads in flight together
+    float mk[GROUP], lk[GROUP], wk[GROUP];
+#pragma unroll
+    for (int h = 0; h < GROUP; ++h) {
+      mk[h] = valid ? __ldcg(rec + h * kPartialFloats + kHeadDim) : -INFINITY;
+      lk[h] = valid ? __ldcg(rec + h * kPartialFloats + kHeadDim + 1) : 0.f;
+    }
+#pragma unroll
+    for (int h = 0; h < GROUP; ++h) {
+      float cm = mk[h];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
+      const float nm = fmaxf(M[h], cm);
+      const float keep = M[h] == -INFINITY ? 0.f : fast_exp2(M[h] - nm);
+      wk[h] = valid ? fast_exp2(mk[h] - nm) : 0.f;
+      float lw = wk[h] * lk[h];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
+      L[h] = L[h] * keep + lw;
+      acc[h].x *= keep;
+      acc[h].y *= keep;
+      M[h] = nm;
+    }
+    // output slices: 4 pieces x GROUP heads of loads in flight per round
+    const int cnt = min(32, n - base);
+    for (int j0 = 0; j0 < cnt; j0 += 4) {
+      float2 v[4][GROUP];
+      float w[4][GROUP];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u < cnt ? j0 + u : j0;  // clamp; weight zeroed below
+        const float* rj = reinterpret_cast<const float*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(rec), j));
+#pragma unroll
+        for (int h = 0; h < GROUP; ++h) {
+          w[u][h] = __shfl_sync(0xffffffffu, wk[h], j);
+          if (j0 + u >= cnt) w[u][h] = 0.f;
+          v[u][h] = __ldcg(reinterpret_cast<const float2*>(rj + h * kPartialFloats) + lane);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+#pragma unroll
+        for (int h = 0; h < GROUP; ++h) {
+          acc[h].x += w[u][h] * v[u][h].x;
+          acc[h].y += w[u][h] * v[u][h].y;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < GROUP; ++h) {
+    const float inv = 1.f / L[h];
+    __nv_bfloat16* out =
+        p.out + (static_cast<int64_t>(s) * p.num_q_heads + g * GROUP + h) * kHeadDim;
+    reinterpret_cast<__nv_bfloat162*>(out)[lane] =
+        __floats2bfloat162_rn(acc[h].x * inv, acc[h].y * inv);
+  }
+}
+
 template <int GROUP>
 __global__ void __launch_bounds__(kWarps * 32, 1)
 paged_decode_kernel(const KParams p) {
@@ -316,6 +438,14 @@ paged_decode_kernel(const KParams p) {
       *p.ws_total = total;
       if (p.chunk > 0 && static_cast<int64_t>(p.grid) * p.chunk < total)
         flag_error(p.status, PA_DEVFLAG_BAD_CONTEXT);  // contexts beyond max_context_len
+    }
+  }
+  if (p.fused_merge && blockIdx.x == 0) {  // empty contexts: zero rows (no tile writes them)
+    const int row_elems = p.num_q_heads * kHeadDim;
+    for (int s0 = 0; s0 < S; ++s0) {
+      if (seq_base[s0 + 1] != seq_base[s0]) continue;
+      __nv_bfloat16* out = p.out + static_cast<int64_t>(s0) * row_elems;
+      for (int e = tid; e < row_elems; e += kThreads) out[e] = __float2bfloat16_rn(0.f);
     }
   }
   // From here on every warp works alone: no block-wide synchronisation below.
@@ -493,6 +623,23 @@ paged_decode_kernel(const KParams p) {
         }
       }
     }
+    if (!whole && p.fused_merge) {
+      // Publish this piece; the warp that publishes the segment's last piece merges it.
+      __threadfence();
+      __syncwarp();
+      const int64_t x0 = static_cast<int64_t>(seq_base[pc.s]) * KV + static_cast<int64_t>(pc.g) * pc.nb;
+      const SegmentPieces sp = segment_pieces(x0, x0 + pc.nb, total, p.grid, p.chunk);
+      int last = 0;
+      if (lane == 0) {
+        const int n = segment_piece_count(sp, x0, x0 + pc.nb, total, p.grid);
+        last = atomicAdd(&p.seg_count[pc.s * KV + pc.g], 1) == n - 1;
+      }
+      if (__shfl_sync(0xffffffffu, last, 0)) {
+        __threadfence();  // acquire the other pieces' partials
+        merge_segment_in_warp<GROUP>(p, sp, x0, x0 + pc.nb, total, pc.s, pc.g, lane);
+        if (lane == 0) p.seg_count[pc.s * KV + pc.g] = 0;  // ready for the next call
+      }
+    }
     y += ntiles;
   }
   }
@@ -662,11 +809,13 @@ cudaError_t launch(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t str
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   p.ws_total = reinterpret_cast<int64_t*>(ws);
   p.ws_seq_base = reinterpret_cast<int32_t*>(ws + 16);
+  p.seg_count = reinterpret_cast<int32_t*>(ws + plan.ws_count_offset);
   p.partials = reinterpret_cast<float*>(ws + plan.ws_meta_bytes);
+  p.fused_merge = plan.fused_merge ? 1 : 0;
   p.status = a.status;
   paged_decode_kernel<GROUP><<<plan.grid, kWarps * 32, plan.smem_bytes, stream>>>(p);
   e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || plan.fused_merge) return e;
   merge_partials_kernel<GROUP><<<dim3(a.num_kv_heads, a.num_seqs), kMergeThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
@@ -710,7 +859,10 @@ cudaError_t plan_decode(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_he
   plan->runs = static_cast<int>(runs);
   const int64_t ctas = (runs + kWarps - 1) / kWarps;
   plan->grid = static_cast<int>(ctas < resident ? ctas : resident);
-  plan->ws_meta_bytes = (16 + sizeof(int32_t) * (num_seqs + 1) + 255) / 256 * 256;
+  plan->fused_merge = partition_tokens == 0 && max_context_len <= kFusedMergeMaxContext;
+  plan->ws_count_offset = (16 + sizeof(int32_t) * (num_seqs + 1) + 255) / 256 * 256;
+  plan->ws_meta_bytes = plan->ws_count_offset +
+                        (sizeof(int32_t) * num_seqs * num_kv_heads + 255) / 256 * 256;
   plan->workspace_bytes = plan->ws_meta_bytes +
                           static_cast<size_t>(runs) * 2 * group * kPartialFloats * sizeof(float);
   return cudaSuccess;

@@ -27,6 +27,8 @@ struct DecodePlan {
   int runs;           // units of the tile decomposition; CTA c serves runs c, c + grid, ...
   int chunk;          // tiles per run (fixed mode), 0 = balanced split of the real total
   size_t smem_bytes;  // dynamic shared memory of the attention kernel
+  bool fused_merge;          // split segments merged inside the attention kernel
+  size_t ws_count_offset;    // offset of the per-segment piece counters (must start zeroed)
   size_t ws_meta_bytes;      // offset of the partials inside the workspace
   size_t workspace_bytes;    // total workspace
 };

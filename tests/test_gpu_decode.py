@@ -218,3 +218,23 @@ def test_group_sizes_one_and_two():
             v.double().cpu().transpose(0, 1)[None], scale=0.125, enable_gqa=True)[0, :, 0, :]
         mx, mean = errors(out.float().cpu().numpy()[0], ref.numpy())
         assert mx <= ATOL_MAX and mean <= ATOL_MEAN
+
+
+def test_split_segments_merged_in_kernel_and_workspace_reuse():
+    """Contexts up to 8192 tokens are split over many warps and merged inside the attention
+    kernel through per-segment counters; a reused workspace must give the same result."""
+    w = wl.make_workload("long4", [7999, 7999, 6000, 4095], [1, 1, 1, 1], seed=12,
+                         pool_slack=0.1)
+    step = GpuStep(w)
+    need = pa.pa_decode_workspace_size(4, 8, 32, int(w.context_lens.max()), 0)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(3):
+        out = torch.empty_like(step.vals["q_decode"])
+        pa.pa_decode(out, step.vals["q_decode"], step.kc, step.vc, step.bt, step.ctx, w.scale,
+                     int(w.context_lens.max()), workspace=ws, device_status=step.status)
+        outs.append(out)
+    assert step.check_status() == pa.PA_OK
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    ref = oracle_step(w, host_vals(step.vals))
+    assert_close(outs[0], ref["decode"], "long contexts, in-kernel merge")
