@@ -65,6 +65,8 @@ def _bind(lib):
     lib.pko_prefill_chunk.restype = ctypes.c_int
     lib.pko_decode.argtypes = [P, P, i32, P, P, i32, i32, i32, i32, P, i32, P, i32, f64]
     lib.pko_decode.restype = ctypes.c_int
+    lib.pko_copy_blocks.argtypes = [P, P, i32, i32, i32, i32, P, i32]
+    lib.pko_copy_blocks.restype = ctypes.c_int
     return lib
 
 
@@ -172,3 +174,13 @@ def prefill_chunk(q, query_start_loc, key_cache, value_cache, block_tables, cont
                                     _ptr(vc), nb, hkv, d, bs, _ptr(bt), bt.shape[1],
                                     _ptr(cl), hq, float(scale))
     return out, int(err)
+
+
+def copy_blocks(key_cache, value_cache, block_mapping):
+    """In-place block copies (pairs [n, 2] of src, dst); returns the error code."""
+    bm = _arr(np.asarray(block_mapping, dtype=np.int64).reshape(-1, 2), np.int64)
+    if not (key_cache.flags.c_contiguous and value_cache.flags.c_contiguous):
+        raise ValueError("caches must be contiguous")
+    nb, hkv, bs, d = key_cache.shape
+    return int(_load().pko_copy_blocks(_ptr(key_cache), _ptr(value_cache), nb, hkv, d, bs,
+                                       _ptr(bm), bm.shape[0]))

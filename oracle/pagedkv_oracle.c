@@ -135,6 +135,33 @@ int pko_reshape_and_cache(const uint16_t* key, const uint16_t* value,
   return err;
 }
 
+/* Block copy used by copy-on-write ("vLLM", PagedAttention: sequences that share a prompt
+ * share its physical blocks and a block is copied only when one of them writes to it).
+ * For each pair (src, dst) of block_mapping, every byte of block src (all kv heads, all
+ * offsets, all dims) in both pools is copied to block dst, pairs in order. */
+int pko_copy_blocks(uint16_t* key_cache, uint16_t* value_cache, int32_t num_blocks,
+                    int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                    const int64_t* block_mapping, int32_t num_pairs) {
+  int err = PKO_OK;
+  for (int32_t i = 0; i < num_pairs; ++i) {
+    int64_t src = block_mapping[2 * i];
+    int64_t dst = block_mapping[2 * i + 1];
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+      err = PKO_BAD_BLOCK;
+      continue;
+    }
+    for (int32_t h = 0; h < num_kv_heads; ++h)
+      for (int32_t off = 0; off < block_size; ++off)
+        for (int32_t d = 0; d < head_dim; ++d) {
+          int64_t from = pool_index(src, h, off, d, num_kv_heads, block_size, head_dim);
+          int64_t to = pool_index(dst, h, off, d, num_kv_heads, block_size, head_dim);
+          key_cache[to] = key_cache[from];
+          value_cache[to] = value_cache[from];
+        }
+  }
+  return err;
+}
+
 /* Gather the first `len` tokens of one sequence's kv head into contiguous double arrays
  * K[len][D], V[len][D] by walking its block table. */
 static int gather_sequence(const uint16_t* key_cache, const uint16_t* value_cache,

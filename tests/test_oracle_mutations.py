@@ -40,6 +40,8 @@ MUTATIONS = {
                            [pins.test_block_arithmetic_golden]),
     "value_store_from_key": ("value_cache[dst] = value[src];", "value_cache[dst] = key[src];",
                              [pins.test_scatter_layout_matches_numpy_indexing]),
+    "copy_blocks_keys_only": ("          value_cache[to] = value_cache[from];", "",
+                              [pins.test_copy_blocks_copies_whole_blocks_in_order]),
     "score_sign_flipped": ("scores[j] = scale * dot;", "scores[j] = -scale * dot;",
                            [pins.test_two_keys_logistic_closed_form]),
 }

@@ -287,3 +287,22 @@ def test_zero_context_gives_zeros_and_bad_block_is_reported():
     out, err = oracle.decode(np.zeros((1, 32, 64), np.uint16), kc, kc,
                              np.array([[5]], np.int32), np.array([3], np.int32), 0.125)
     assert err == oracle.BAD_BLOCK
+
+
+# ---- copy-on-write block copy -----------------------------------------------------------
+
+def test_copy_blocks_copies_whole_blocks_in_order():
+    """Block dst becomes a byte copy of block src in both pools (numpy indexing), pairs
+    applied in order; nothing else changes."""
+    rng = np.random.default_rng(5)
+    kc = rng.integers(0, 2**16, size=(6, 8, 16, 64), dtype=np.uint16)
+    vc = rng.integers(0, 2**16, size=(6, 8, 16, 64), dtype=np.uint16)
+    k0, v0 = kc.copy(), vc.copy()
+    pairs = [(1, 4), (4, 5), (0, 2)]  # 4 <- 1, then 5 <- (new) 4, then 2 <- 0
+    assert oracle.copy_blocks(kc, vc, pairs) == 0
+    for pool, orig in ((kc, k0), (vc, v0)):
+        assert np.array_equal(pool[4], orig[1]) and np.array_equal(pool[5], orig[1])
+        assert np.array_equal(pool[2], orig[0])
+        for b in (0, 1, 3):
+            assert np.array_equal(pool[b], orig[b])
+    assert oracle.copy_blocks(kc, vc, [(0, 9)]) == oracle.BAD_BLOCK
