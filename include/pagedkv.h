@@ -55,7 +55,8 @@ typedef enum pa_status {
   PA_ERR_CUDA = -3,          /* a CUDA runtime call failed (launch, query, copy) */
   PA_ERR_WORKSPACE = -4,     /* workspace missing or smaller than required */
   PA_ERR_DEVICE_INDEX = -5,  /* device_status reports a bad block id / slot / length */
-  PA_ERR_DEVICE_TIMEOUT = -6 /* device_status reports a pipeline wait that timed out */
+  PA_ERR_DEVICE_TIMEOUT = -6, /* device_status reports a pipeline wait that timed out */
+  PA_ERR_OUT_OF_BLOCKS = -7   /* the block manager has too few free blocks (no change made) */
 } pa_status;
 
 /* Bits a kernel ORs into *device_status. */
@@ -180,6 +181,49 @@ pa_status pa_decode_static_scratch(void* out, const void* q, const void* key_cac
                                    int32_t num_q_heads, float scale, int32_t max_context_len,
                                    int32_t partition_tokens, int32_t* device_status,
                                    pa_stream_t stream);
+
+/* Copy-on-write block copy ("vLLM", PagedAttention: sequences sharing a prompt share its
+ * physical blocks; a block is copied only when one of them writes into it).  For every pair
+ * i, block block_mapping[2i] of both pools is copied, all heads and offsets, bit-exactly, to
+ * block block_mapping[2i+1].
+ *   block_mapping  int64 [num_pairs][2] (src, dst), device memory
+ * Pairs must be independent: no block is both a source and a destination, no destination
+ * appears twice (the order of the copies is not defined).  A pair with an id outside
+ * [0, num_blocks) sets PA_DEVFLAG_BAD_BLOCK and is skipped.  num_pairs == 0 is a no-op. */
+pa_status pa_copy_blocks(void* key_cache, void* value_cache, pa_cache_desc cd,
+                         const int64_t* block_mapping, int32_t num_pairs,
+                         int32_t* device_status, pa_stream_t stream);
+
+/* Host-side block manager ("vLLM", PagedAttention and Continuous Batching): a pool of
+ * num_blocks physical blocks of block_size tokens; each sequence owns a table of blocks,
+ * grown one block at a time as tokens arrive; pa_bm_fork shares a sequence's blocks with a
+ * new sequence (reference counts); appending to a sequence whose partly filled last block is
+ * shared replaces that block with a fresh copy (copy-on-write) and reports the (src, dst)
+ * pair for pa_copy_blocks; freeing a sequence returns the blocks no one else holds.  Not
+ * thread-safe; pure host code (no CUDA calls). */
+typedef struct pa_block_manager pa_block_manager;
+pa_status pa_bm_create(int32_t num_blocks, int32_t block_size, pa_block_manager** out);
+void pa_bm_destroy(pa_block_manager* bm);
+int32_t pa_bm_num_free_blocks(const pa_block_manager* bm);
+/* Current number of sequences holding `block` (-1 for a bad id). */
+int32_t pa_bm_ref_count(const pa_block_manager* bm, int32_t block);
+/* New empty sequence; seq_id >= 0 and unused. */
+pa_status pa_bm_add_sequence(pa_block_manager* bm, int64_t seq_id);
+/* child (unused id) starts as a copy of parent: same tokens, same physical blocks. */
+pa_status pa_bm_fork(pa_block_manager* bm, int64_t parent, int64_t child);
+/* Make room for num_tokens more tokens of seq_id.  On copy-on-write, one pair is written
+ * to cow_pairs (int64 [cow_capacity][2] host array, capacity >= 1) and *num_cow = 1; copy it
+ * with pa_copy_blocks before storing the new tokens.  PA_ERR_OUT_OF_BLOCKS leaves every
+ * table unchanged. */
+pa_status pa_bm_append_tokens(pa_block_manager* bm, int64_t seq_id, int32_t num_tokens,
+                              int64_t* cow_pairs, int32_t cow_capacity, int32_t* num_cow);
+pa_status pa_bm_free_sequence(pa_block_manager* bm, int64_t seq_id);
+/* Tokens held by seq_id (-1 if unknown). */
+int64_t pa_bm_num_tokens(const pa_block_manager* bm, int64_t seq_id);
+/* Writes seq_id's physical block ids to out[0..n) and -1 to out[n..max_blocks); returns n,
+ * or a negative pa_status when the sequence is unknown or has more than max_blocks blocks. */
+int32_t pa_bm_block_table(const pa_block_manager* bm, int64_t seq_id, int32_t* out,
+                          int32_t max_blocks);
 
 /* Synchronise `stream`, read *device_status and translate it: PA_OK when zero,
  * PA_ERR_DEVICE_TIMEOUT when the timeout bit is set, else PA_ERR_DEVICE_INDEX. */

@@ -36,12 +36,16 @@ PA_ERR_CUDA = -3
 PA_ERR_WORKSPACE = -4
 PA_ERR_DEVICE_INDEX = -5
 PA_ERR_DEVICE_TIMEOUT = -6
+PA_ERR_OUT_OF_BLOCKS = -7
 DEVFLAG_BAD_BLOCK, DEVFLAG_BAD_SLOT, DEVFLAG_BAD_CONTEXT, DEVFLAG_TIMEOUT = 1, 2, 4, 8
 
 # Every symbol include/pagedkv.h declares.
 EXPORTED = ("pa_compute_slot_mapping", "pa_reshape_and_cache", "pa_decode_workspace_size",
             "pa_decode", "pa_prefill_chunk", "pa_check_device_status", "pa_status_string",
-            "pa_last_error", "pa_decode_static_scratch")
+            "pa_last_error", "pa_decode_static_scratch", "pa_copy_blocks", "pa_bm_create",
+            "pa_bm_destroy", "pa_bm_num_free_blocks", "pa_bm_ref_count", "pa_bm_add_sequence",
+            "pa_bm_fork", "pa_bm_append_tokens", "pa_bm_free_sequence", "pa_bm_num_tokens",
+            "pa_bm_block_table")
 
 
 def library_path() -> str:
@@ -75,6 +79,29 @@ def load(path: str | None = None):
     lib.pa_decode_static_scratch.argtypes = [P, P, P, P, CacheDesc, P, i32, P, i32, i32, f32,
                                              i32, i32, P, P]
     lib.pa_decode_static_scratch.restype = st
+    lib.pa_copy_blocks.argtypes = [P, P, CacheDesc, P, i32, P, P]
+    lib.pa_copy_blocks.restype = st
+    i64 = ctypes.c_int64
+    lib.pa_bm_create.argtypes = [i32, i32, ctypes.POINTER(P)]
+    lib.pa_bm_create.restype = st
+    lib.pa_bm_destroy.argtypes = [P]
+    lib.pa_bm_destroy.restype = None
+    lib.pa_bm_num_free_blocks.argtypes = [P]
+    lib.pa_bm_num_free_blocks.restype = i32
+    lib.pa_bm_ref_count.argtypes = [P, i32]
+    lib.pa_bm_ref_count.restype = i32
+    lib.pa_bm_add_sequence.argtypes = [P, i64]
+    lib.pa_bm_add_sequence.restype = st
+    lib.pa_bm_fork.argtypes = [P, i64, i64]
+    lib.pa_bm_fork.restype = st
+    lib.pa_bm_append_tokens.argtypes = [P, i64, i32, P, i32, ctypes.POINTER(i32)]
+    lib.pa_bm_append_tokens.restype = st
+    lib.pa_bm_free_sequence.argtypes = [P, i64]
+    lib.pa_bm_free_sequence.restype = st
+    lib.pa_bm_num_tokens.argtypes = [P, i64]
+    lib.pa_bm_num_tokens.restype = i64
+    lib.pa_bm_block_table.argtypes = [P, i64, P, i32]
+    lib.pa_bm_block_table.restype = i32
     lib.pa_check_device_status.argtypes = [P, P]
     lib.pa_check_device_status.restype = st
     lib.pa_status_string.argtypes = [st]
@@ -250,3 +277,72 @@ def pa_check_device_status(device_status, stream=None) -> int:
     """Synchronise and translate the device status word; returns the pa_status code."""
     _need(device_status, "device_status", torch.int32, 1)
     return int(load().pa_check_device_status(_ptr(device_status), _stream(stream)))
+
+
+def pa_copy_blocks(key_cache, value_cache, block_mapping, device_status=None, stream=None):
+    """Copy whole physical blocks of both pools: block_mapping int64 [n, 2] (src, dst)."""
+    _need(key_cache, "key_cache", torch.bfloat16, 4)
+    _need(value_cache, "value_cache", torch.bfloat16, 4)
+    _need(block_mapping, "block_mapping", torch.int64, 2)
+    if key_cache.shape != value_cache.shape or block_mapping.shape[1] != 2:
+        raise ValueError("cache shapes differ or block_mapping is not [n, 2]")
+    st = load().pa_copy_blocks(_ptr(key_cache), _ptr(value_cache), cache_desc(key_cache),
+                               _ptr(block_mapping), block_mapping.shape[0], _ptr(device_status),
+                               _stream(stream))
+    _check(st, "pa_copy_blocks")
+
+
+class BlockManager:
+    """Host-side block manager of include/pagedkv.h (pa_bm_*): block tables grown on
+    demand, forks that share blocks, copy-on-write pairs for pa_copy_blocks."""
+
+    def __init__(self, num_blocks: int, block_size: int = 16):
+        self._lib = load()
+        h = ctypes.c_void_p()
+        _check(self._lib.pa_bm_create(num_blocks, block_size, ctypes.byref(h)), "pa_bm_create")
+        self._h = h
+
+    def close(self):
+        if self._h:
+            self._lib.pa_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def num_free_blocks(self) -> int:
+        return int(self._lib.pa_bm_num_free_blocks(self._h))
+
+    def ref_count(self, block: int) -> int:
+        return int(self._lib.pa_bm_ref_count(self._h, block))
+
+    def add_sequence(self, seq_id: int):
+        _check(self._lib.pa_bm_add_sequence(self._h, seq_id), "pa_bm_add_sequence")
+
+    def fork(self, parent: int, child: int):
+        _check(self._lib.pa_bm_fork(self._h, parent, child), "pa_bm_fork")
+
+    def append_tokens(self, seq_id: int, num_tokens: int):
+        """Returns the list of (src, dst) copy-on-write pairs (at most one)."""
+        pairs = (ctypes.c_int64 * 2)()
+        n = ctypes.c_int32(0)
+        _check(self._lib.pa_bm_append_tokens(self._h, seq_id, num_tokens, pairs, 1,
+                                             ctypes.byref(n)), "pa_bm_append_tokens")
+        return [(int(pairs[0]), int(pairs[1]))] if n.value else []
+
+    def free_sequence(self, seq_id: int):
+        _check(self._lib.pa_bm_free_sequence(self._h, seq_id), "pa_bm_free_sequence")
+
+    def num_tokens(self, seq_id: int) -> int:
+        return int(self._lib.pa_bm_num_tokens(self._h, seq_id))
+
+    def block_table(self, seq_id: int, max_blocks: int):
+        out = (ctypes.c_int32 * max(max_blocks, 1))()
+        n = int(self._lib.pa_bm_block_table(self._h, seq_id, out, max_blocks))
+        if n < 0:
+            _check(n, "pa_bm_block_table")
+        return [int(out[i]) for i in range(max_blocks)], n

@@ -226,6 +226,22 @@ pa_status pa_prefill_chunk(void* out, const void* q, const int32_t* query_start_
                    "prefill launch");
 }
 
+pa_status pa_copy_blocks(void* key_cache, void* value_cache, pa_cache_desc cd,
+                         const int64_t* block_mapping, int32_t num_pairs,
+                         int32_t* device_status, pa_stream_t stream) {
+  pa_status st = check_desc(cd);
+  if (st != PA_OK) return st;
+  if (num_pairs < 0) return fail(PA_ERR_INVALID_ARG, "num_pairs %d", num_pairs);
+  if (num_pairs == 0) return ok();
+  if (!key_cache || !value_cache || !block_mapping) return fail(PA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(key_cache) || !aligned16(value_cache))
+    return fail(PA_ERR_INVALID_ARG, "cache pointers must be 16-byte aligned");
+  return from_cuda(pkv::launch_copy_blocks(key_cache, value_cache, block_mapping, num_pairs,
+                                           cd.num_blocks, cd.num_kv_heads, device_status,
+                                           reinterpret_cast<cudaStream_t>(stream)),
+                   "copy_blocks launch");
+}
+
 pa_status pa_check_device_status(const int32_t* device_status, pa_stream_t stream) {
   if (!device_status) return fail(PA_ERR_INVALID_ARG, "null status pointer");
   int32_t word = 0;
@@ -251,6 +267,7 @@ const char* pa_status_string(pa_status status) {
     case PA_ERR_WORKSPACE: return "workspace missing or too small";
     case PA_ERR_DEVICE_INDEX: return "device reported a bad index";
     case PA_ERR_DEVICE_TIMEOUT: return "device reported a wait timeout";
+    case PA_ERR_OUT_OF_BLOCKS: return "not enough free blocks";
   }
   return "unknown status";
 }

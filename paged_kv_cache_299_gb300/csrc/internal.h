@@ -20,6 +20,10 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value,
                                      int32_t num_kv_heads, int32_t* status,
                                      cudaStream_t stream);
 
+cudaError_t launch_copy_blocks(void* key_cache, void* value_cache, const int64_t* block_mapping,
+                               int32_t num_pairs, int32_t num_blocks, int32_t num_kv_heads,
+                               int32_t* status, cudaStream_t stream);
+
 // Work decomposition of one pa_decode call (identical in the size query and the call).
 struct DecodePlan {
   int group;          // q heads per kv head

@@ -30,7 +30,7 @@ def test_library_builds_and_exports_every_declared_symbol():
 
 def test_status_strings():
     lib = pa.load()
-    for code in range(-6, 1):
+    for code in range(-7, 1):
         assert lib.pa_status_string(code)
     assert lib.pa_status_string(-99) == b"unknown status"
 
