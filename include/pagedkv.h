@@ -65,6 +65,8 @@ typedef enum pa_status {
 #define PA_DEVFLAG_BAD_CONTEXT 0x4 /* context length < 0, beyond its table row, or beyond
                                       the host bound max_context_len */
 #define PA_DEVFLAG_TIMEOUT 0x8     /* an mbarrier wait exceeded its time limit */
+#define PA_DEVFLAG_LAYOUT 0x10     /* shared memory not aligned as the kernel requires
+                                      (work skipped; reported as PA_ERR_DEVICE_INDEX) */
 
 /* Geometry of one layer's pair of cache pools; validated on every call. */
 typedef struct pa_cache_desc {

@@ -44,7 +44,9 @@ constexpr int kQBytes = kTileM * kRowBytes;       // 16 KiB
 constexpr int kKVBytes = kTileN * kRowBytes;      // 16 KiB per K (or V) tile
 constexpr int kPRegionBytes = kTileM * 128;       // 64 keys x 128 rows of bf16
 constexpr int kPBytes = 2 * kPRegionBytes;        // 32 KiB
-constexpr int kSmemBytes = 1024 + kQBytes + 2 * kStages * kKVBytes + kPBytes + 8 * 16 + 16;
+constexpr int kSmemBytes = kQBytes + 2 * kStages * kKVBytes + kPBytes + 8 * 16 + 16 + 16;
+// Two CTAs fit on one SM (2 x (kSmemBytes + 1 KiB reserved) <= 228 KiB, 2 x 256 TMEM
+// columns = 512, <= 168 registers per thread), so one CTA's softmax overlaps the other's MMAs.
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kSCol = 0;
 constexpr uint32_t kOCol = 128;
@@ -73,7 +75,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
   return false;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
                      const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const PParams p) {
@@ -98,9 +100,11 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
   const int n_kv = (keys + kTileN - 1) / kTileN;
   const int blocks_needed = (keys + kBlockSize - 1) / kBlockSize;
 
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];  // 128-byte swizzle atoms need 1 KiB
+  if ((smem_addr(smem) & 1023u) != 0) {  // never issue swizzled copies to a misaligned tile
+    if (tid == 0) flag_error(p.status, PA_DEVFLAG_LAYOUT);
+    return;
+  }
   uint8_t* sq = smem;
   uint8_t* sk = sq + kQBytes;
   uint8_t* sv = sk + kStages * kKVBytes;
@@ -114,7 +118,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
   uint64_t* o_done = p_ready + 1;
   uint64_t* drain = o_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
-  __shared__ volatile int abort_flag;
+  volatile int& abort_flag = *reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   if (tid == 0) {
     mbar_init(q_full, 1);
@@ -338,24 +342,23 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
     if (ok) {
       tc_fence_after_sync();
       __syncwarp();
-      uint32_t o[2][32];
-      tmem_ld32(lane_addr + kOCol, o[0]);
-      tmem_ld32(lane_addr + kOCol + 32, o[1]);
-      tmem_wait_ld();
-      if (row_ok) {
-        const float inv = 1.f / l;
-        __nv_bfloat16* dst = p.out + (static_cast<int64_t>(q0 + token) * p.num_q_heads +
-                                      g * kGroup + hh) * kHeadDim;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
+      const float inv = 1.f / l;
+      __nv_bfloat16* dst = p.out + (static_cast<int64_t>(q0 + token) * p.num_q_heads +
+                                    g * kGroup + hh) * kHeadDim;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {  // 32 columns at a time keeps the register budget
+        uint32_t o[32];
+        tmem_ld32(lane_addr + kOCol + 32 * c, o);
+        tmem_wait_ld();
+        if (row_ok) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int i = q4 * 8 + 2 * e;
-              const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(o[c][i]) * inv,
-                                                              __uint_as_float(o[c][i + 1]) * inv);
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(o[i]) * inv,
+                                                              __uint_as_float(o[i + 1]) * inv);
               w[e] = *reinterpret_cast<const uint32_t*>(&b2);
             }
             *reinterpret_cast<uint4*>(dst + 32 * c + 8 * q4) = make_uint4(w[0], w[1], w[2], w[3]);
