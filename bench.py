@@ -42,6 +42,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--append", choices=["fused", "separate"], default="fused",
+                    help="decode-only steps: store the new tokens inside the decode launch "
+                         "(pa_decode_append) or with pa_reshape_and_cache first")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=None,
@@ -68,6 +71,14 @@ def ncu_traffic(cfg: int):
         return int(v) if v else None
     except Exception:
         return None
+
+
+def measured_bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 1700.0, "fallback"
 
 
 def measured_peaks():
@@ -161,7 +172,7 @@ class DeviceStep:
     """Resident state of one workload: per-layer pools (history already stored through the
     library), this step's inputs, outputs and workspaces."""
 
-    def __init__(self, w, dev):
+    def __init__(self, w, dev, fused_append=False):
         import torch
         from paged_kv_cache_299_gb300 import binding as pa
         self.pa = pa
@@ -173,6 +184,8 @@ class DeviceStep:
         self.ctx = i32(w.context_lens)
         self.new_qsl = i32(w.new_start_loc)
         self.one_token_each = bool((w.new_lens == 1).all())
+        # one new token per decode sequence and no prefill: the store can ride in the decode
+        self.fused_append = bool(fused_append and self.one_token_each and w.num_prefill == 0)
         self.n_new = int(w.new_lens.sum())
         self.bt_dec = self.bt[w.num_prefill:].contiguous()
         self.ctx_dec = self.ctx[w.num_prefill:].contiguous()
@@ -206,6 +219,9 @@ class DeviceStep:
             })
             del vals
             torch.cuda.synchronize(dev)
+        # the library merges split-KV pieces inside the decode kernel up to 8192-token
+        # contexts with automatic partitions; otherwise a second (merge) kernel runs
+        self.ws_merge_kernel = bool(w.partition_tokens > 0 or self.max_ctx_dec > 8192)
         if w.num_decode:
             need = pa.pa_decode_workspace_size(w.num_decode, w.num_kv_heads, w.num_q_heads,
                                                self.max_ctx_dec, w.partition_tokens)
@@ -214,18 +230,44 @@ class DeviceStep:
 
     def launches_per_step(self) -> int:
         w = self.w
-        per_layer = 1 + (2 if w.num_decode else 0) + (1 if w.num_prefill else 0)
+        if self.fused_append:
+            return w.layers * (2 if self.ws_merge_kernel else 1)
+        per_layer = 1 + ((2 if self.ws_merge_kernel else 1) if w.num_decode else 0) + \
+            (1 if w.num_prefill else 0)
         return 1 + per_layer * w.layers
 
-    def step(self, dec_events=None):
+    def prefill_flops(self) -> float:
+        """Causal-useful flops of this step's prefill chunks: row i of a chunk over h prior
+        tokens attends h + i + 1 keys; 4 * head_dim flops per (row, head, key)."""
+        w = self.w
+        h = w.hist_lens[: w.num_prefill].astype(np.float64)
+        n = w.new_lens[: w.num_prefill].astype(np.float64)
+        keys = (n * h + n * (n + 1) / 2).sum()
+        return float(keys * w.num_q_heads * 4 * w.head_dim * w.layers)
+
+    def step(self, dec_events=None, pre_events=None):
         pa, w = self.pa, self.w
+        if self.fused_append:
+            for li, L in enumerate(self.layers):
+                if dec_events is not None:
+                    dec_events[li][0].record()
+                pa.pa_decode_append(L["out_dec"], L["q_dec"], L["new_k"], L["new_v"], L["kc"],
+                                    L["vc"], self.bt_dec, self.ctx_dec, w.scale,
+                                    self.max_ctx_dec, w.partition_tokens, workspace=self.ws)
+                if dec_events is not None:
+                    dec_events[li][1].record()
+            return
         pa.pa_compute_slot_mapping(self.bt, self.ctx, None if self.one_token_each else self.new_qsl,
                                    self.n_new, self.layers[0]["kc"], slot_mapping=self.slots)
         for li, L in enumerate(self.layers):
             pa.pa_reshape_and_cache(L["new_k"], L["new_v"], self.slots, L["kc"], L["vc"])
             if w.num_prefill:
+                if pre_events is not None:
+                    pre_events[li][0].record()
                 pa.pa_prefill_chunk(L["out_pre"], L["q_pre"], self.pre_qsl, self.max_q_pre,
                                     L["kc"], L["vc"], self.bt_pre, self.ctx_pre, w.scale)
+                if pre_events is not None:
+                    pre_events[li][1].record()
             if w.num_decode:
                 if dec_events is not None:
                     dec_events[li][0].record()
@@ -245,7 +287,7 @@ def run_gpu(args, rank, world):
     torch.cuda.set_device(dev)
     # weak scaling: every rank serves its own batch (seed offset per rank)
     w = workload(args.config, args.layers, 100 * rank if world > 1 else 0)
-    st = DeviceStep(w, dev)
+    st = DeviceStep(w, dev, fused_append=args.append == "fused")
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     kv_bytes = w.decode_kv_bytes()
     flush = kv_bytes < 4 * l2
@@ -265,6 +307,8 @@ def run_gpu(args, rank, world):
                for _ in range(w.layers)] for _ in range(K)]
     step_ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
                for _ in range(K)]
+    pre_ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+               for _ in range(w.layers)] for _ in range(K)] if w.num_prefill else None
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
@@ -275,7 +319,7 @@ def run_gpu(args, rank, world):
         if flush:
             flush_buf.fill_(k)  # rewrite a buffer of twice the L2 size between steps
         step_ev[k][0].record()
-        st.step(dec_ev[k] if w.num_decode else None)
+        st.step(dec_ev[k] if w.num_decode else None, pre_ev[k] if pre_ev else None)
         step_ev[k][1].record()
     torch.cuda.synchronize(dev)
     barrier()
@@ -285,6 +329,9 @@ def run_gpu(args, rank, world):
     dec_ms = None
     if w.num_decode:
         dec_ms = sum(a.elapsed_time(b) for row in dec_ev for a, b in row) / (K * w.layers)
+    pre_ms = None
+    if pre_ev:
+        pre_ms = sum(a.elapsed_time(b) for row in pre_ev for a, b in row) / (K * w.layers)
     if world > 1:
         t = torch.tensor([step_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -312,7 +359,9 @@ def run_gpu(args, rank, world):
                        accumulate="f32",
                        l2=("flushed between steps (2x L2 rewrite)" if flush
                            else "inputs larger than L2 (%.1f GB KV per step)" % (kv_bytes / 1e9)),
-                       launch="eager (one C-ABI call per kernel group)"),
+                       launch="eager (one C-ABI call per kernel group)",
+                       store=("fused into decode (pa_decode_append)" if st.fused_append
+                              else "pa_compute_slot_mapping + pa_reshape_and_cache")),
         "tokens_per_s": round(w.num_decode * world / (step_ms * 1e-3), 1),
         "pct_of_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "gpu_launches": st.launches_per_step() * K,
@@ -329,6 +378,14 @@ def run_gpu(args, rank, world):
                       "8192-token contexts, else + merge_partials_kernel)",
             "peak_source": f"{peak_src} hbm_gbs", "pct_of_8tbs": round(100 * achieved / 8000, 2),
             "launch_ms": round(dec_ms, 5), "algorithmic_bytes_per_launch": int(per_launch)}
+    if pre_ms:
+        tfl = st.prefill_flops() / w.layers / (pre_ms * 1e-3) / 1e12
+        bf16_peak, bf16_src = measured_bf16_peak()
+        res["prefill_roofline"] = {
+            "bound": "tensor", "achieved": round(tfl, 1), "peak": bf16_peak, "unit": "TFLOP/s",
+            "frac": round(tfl / bf16_peak, 4), "kernel": "paged_prefill_kernel (tcgen05)",
+            "peak_source": f"{bf16_src} bf16_tflops_sustained", "launch_ms": round(pre_ms, 5),
+            "algorithmic_flops_per_launch": round(st.prefill_flops() / w.layers)}
     if e2e:
         res["e2e"] = {"value": round(kv_bytes * world / (e2e["step_ms"] * 1e-3) / 1e9, 1),
                       "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],

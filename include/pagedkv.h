@@ -136,6 +136,22 @@ pa_status pa_decode(void* out, const void* q, const void* key_cache, const void*
                     int32_t max_context_len, int32_t partition_tokens, void* workspace,
                     size_t workspace_bytes, int32_t* device_status, pa_stream_t stream);
 
+/* Decode with the store of the new tokens fused in: for every sequence s, the token at
+ * position context_lens[s] - 1 (key[s][h][:], value[s][h][:], bf16 [num_seqs][Hkv][D]) is
+ * written to its slot block_tables[s][(L-1) / 16] * 16 + (L-1) % 16 of both pools, and the
+ * attention of pa_decode runs over all L tokens, in one launch.  Results (pools and out) are
+ * bit-identical to pa_reshape_and_cache of those tokens followed by pa_decode.  This removes
+ * the per-step store launches ("vLLM", CUDA Graph: per-token launch overhead; section
+ * Optimized CUDA Kernels: fused kernels skip HBM round trips).  Every other argument,
+ * requirement and error is that of pa_decode; a context of 0 stores nothing. */
+pa_status pa_decode_append(void* out, const void* q, const void* key, const void* value,
+                           void* key_cache, void* value_cache, pa_cache_desc cd,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                           float scale, int32_t max_context_len, int32_t partition_tokens,
+                           void* workspace, size_t workspace_bytes, int32_t* device_status,
+                           pa_stream_t stream);
+
 /* Causal chunked-prefill attention over a paged prefix.  Sequence s has q_len =
  * query_start_loc[s+1] - query_start_loc[s] query rows, the last q_len of its
  * context_lens[s] tokens (already stored); row i sits at position L - q_len + i and

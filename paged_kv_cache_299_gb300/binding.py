@@ -45,7 +45,7 @@ EXPORTED = ("pa_compute_slot_mapping", "pa_reshape_and_cache", "pa_decode_worksp
             "pa_last_error", "pa_decode_static_scratch", "pa_copy_blocks", "pa_bm_create",
             "pa_bm_destroy", "pa_bm_num_free_blocks", "pa_bm_ref_count", "pa_bm_add_sequence",
             "pa_bm_fork", "pa_bm_append_tokens", "pa_bm_free_sequence", "pa_bm_num_tokens",
-            "pa_bm_block_table")
+            "pa_bm_block_table", "pa_decode_append")
 
 
 def library_path() -> str:
@@ -79,6 +79,9 @@ def load(path: str | None = None):
     lib.pa_decode_static_scratch.argtypes = [P, P, P, P, CacheDesc, P, i32, P, i32, i32, f32,
                                              i32, i32, P, P]
     lib.pa_decode_static_scratch.restype = st
+    lib.pa_decode_append.argtypes = [P, P, P, P, P, P, CacheDesc, P, i32, P, i32, i32, f32, i32,
+                                     i32, P, sz, P, P]
+    lib.pa_decode_append.restype = st
     lib.pa_copy_blocks.argtypes = [P, P, CacheDesc, P, i32, P, P]
     lib.pa_copy_blocks.restype = st
     i64 = ctypes.c_int64
@@ -221,6 +224,39 @@ def pa_decode(out, q, key_cache, value_cache, block_tables, context_lens, scale,
                           int(partition_tokens), _ptr(workspace), workspace.numel(),
                           _ptr(device_status), _stream(stream))
     _check(st, "pa_decode")
+    return out
+
+
+def pa_decode_append(out, q, key, value, key_cache, value_cache, block_tables, context_lens,
+                     scale, max_context_len, partition_tokens=0, workspace=None,
+                     device_status=None, stream=None):
+    """Store each sequence's newest token (key/value [S, Hkv, D]) and run paged decode
+    attention, in one launch; bit-identical to pa_reshape_and_cache + pa_decode."""
+    _need(out, "out", torch.bfloat16, 3)
+    _need(q, "q", torch.bfloat16, 3)
+    _need(key, "key", torch.bfloat16, 3)
+    _need(value, "value", torch.bfloat16, 3)
+    _need(key_cache, "key_cache", torch.bfloat16, 4)
+    _need(value_cache, "value_cache", torch.bfloat16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    num_seqs, hq, _ = q.shape
+    if out.shape != q.shape or key.shape != value.shape or key.shape[0] != num_seqs or \
+            key.shape[1:] != (key_cache.shape[1], key_cache.shape[3]) or \
+            block_tables.shape[0] != num_seqs or context_lens.shape[0] != num_seqs:
+        raise ValueError("pa_decode_append argument shapes disagree")
+    if workspace is None:
+        need = pa_decode_workspace_size(num_seqs, key_cache.shape[1], hq, max_context_len,
+                                        partition_tokens)
+        workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=q.device)
+    _need(workspace, "workspace", torch.uint8, 1)
+    st = load().pa_decode_append(_ptr(out), _ptr(q), _ptr(key), _ptr(value), _ptr(key_cache),
+                                 _ptr(value_cache), cache_desc(key_cache), _ptr(block_tables),
+                                 block_tables.shape[1], _ptr(context_lens), num_seqs, hq,
+                                 float(scale), int(max_context_len), int(partition_tokens),
+                                 _ptr(workspace), workspace.numel(), _ptr(device_status),
+                                 _stream(stream))
+    _check(st, "pa_decode_append")
     return out
 
 

@@ -133,7 +133,8 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t 
   return plan.workspace_bytes;
 }
 
-pa_status pa_decode(void* out, const void* q, const void* key_cache, const void* value_cache,
+static pa_status decode_impl(void* out, const void* q, const void* k_new, const void* v_new,
+                             const void* key_cache, const void* value_cache,
                     pa_cache_desc cd, const int32_t* block_tables,
                     int32_t max_blocks_per_seq, const int32_t* context_lens,
                     int32_t num_seqs, int32_t num_q_heads, float scale,
@@ -152,6 +153,8 @@ pa_status pa_decode(void* out, const void* q, const void* key_cache, const void*
   if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
     return fail(PA_ERR_INVALID_ARG, "out/q/cache pointers must be 16-byte aligned");
   if (!(scale > 0.f) || !isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale %g", scale);
+  if ((k_new == nullptr) != (v_new == nullptr) || (k_new && (!aligned16(k_new) || !aligned16(v_new))))
+    return fail(PA_ERR_INVALID_ARG, "k_new / v_new: both or neither, 16-byte aligned");
   pkv::DecodePlan plan;
   cudaError_t e = pkv::plan_decode(num_seqs, cd.num_kv_heads, num_q_heads, max_context_len,
                                    partition_tokens, &plan);
@@ -174,8 +177,36 @@ pa_status pa_decode(void* out, const void* q, const void* key_cache, const void*
   a.scale = scale;
   a.workspace = workspace;
   a.status = device_status;
+  a.k_new = k_new;
+  a.v_new = v_new;
   return from_cuda(pkv::launch_decode(a, plan, reinterpret_cast<cudaStream_t>(stream)),
                    "decode launch");
+}
+
+pa_status pa_decode(void* out, const void* q, const void* key_cache, const void* value_cache,
+                    pa_cache_desc cd, const int32_t* block_tables,
+                    int32_t max_blocks_per_seq, const int32_t* context_lens,
+                    int32_t num_seqs, int32_t num_q_heads, float scale,
+                    int32_t max_context_len, int32_t partition_tokens, void* workspace,
+                    size_t workspace_bytes, int32_t* device_status, pa_stream_t stream) {
+  return decode_impl(out, q, nullptr, nullptr, key_cache, value_cache, cd, block_tables,
+                     max_blocks_per_seq, context_lens, num_seqs, num_q_heads, scale,
+                     max_context_len, partition_tokens, workspace, workspace_bytes,
+                     device_status, stream);
+}
+
+pa_status pa_decode_append(void* out, const void* q, const void* key, const void* value,
+                           void* key_cache, void* value_cache, pa_cache_desc cd,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                           float scale, int32_t max_context_len, int32_t partition_tokens,
+                           void* workspace, size_t workspace_bytes, int32_t* device_status,
+                           pa_stream_t stream) {
+  if (num_seqs > 0 && (!key || !value)) return fail(PA_ERR_INVALID_ARG, "null key/value");
+  return decode_impl(out, q, key, value, key_cache, value_cache, cd, block_tables,
+                     max_blocks_per_seq, context_lens, num_seqs, num_q_heads, scale,
+                     max_context_len, partition_tokens, workspace, workspace_bytes,
+                     device_status, stream);
 }
 
 pa_status pa_prefill_chunk(void* out, const void* q, const int32_t* query_start_loc,

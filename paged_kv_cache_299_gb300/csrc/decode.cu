@@ -70,6 +70,10 @@ struct KParams {
   int32_t* seg_count;   // [num_seqs * Hkv] pieces published per split segment (fused merge);
                         // zero between calls: the merging warp resets its counter
   int32_t fused_merge;  // 1: the last warp to finish a split segment merges it in place
+  const uint8_t* k_new;  // optional [num_seqs][Hkv][64] bf16: token at position L-1 to store
+  const uint8_t* v_new;  //   (fused append: stored to its slot and used in attention)
+  uint8_t* key_cache_w;    // writable views of the pools (fused append)
+  uint8_t* value_cache_w;
   int32_t* status;
 };
 
@@ -240,7 +244,8 @@ template <int GROUP>
 constexpr size_t decode_smem_fixed() {
   return static_cast<size_t>(kWarps) *
          (kStagesPerWarp * 2 * kTileBytes          // private K+V rings
-          + kStagesPerWarp * sizeof(uint64_t));    // full barriers
+          + kStagesPerWarp * sizeof(uint64_t)      // full barriers
+          + kStagesPerWarp * sizeof(int32_t));     // tile id held by each stage
 }
 
 // Block-table window: lane j holds the tile (phys_block * Hkv + kv_head) of the j-th of
@@ -380,7 +385,10 @@ paged_decode_kernel(const KParams p) {
   uint8_t* ring = smem + warp * (kStagesPerWarp * 2 * kTileBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kStagesPerWarp * 2 * kTileBytes);
   uint64_t* full_bar = bars + warp * kStagesPerWarp;
-  int32_t* seq_base = reinterpret_cast<int32_t*>(bars + kWarps * kStagesPerWarp);
+  int32_t* stage_tile = reinterpret_cast<int32_t*>(bars + kWarps * kStagesPerWarp) +
+                        warp * kStagesPerWarp;
+  int32_t* seq_base = reinterpret_cast<int32_t*>(bars + kWarps * kStagesPerWarp) +
+                      kWarps * kStagesPerWarp;
   __shared__ int64_t warp_sums[kWarps];
 
   if (lane == 0) {
@@ -503,6 +511,7 @@ paged_decode_kernel(const KParams p) {
     const int32_t t = __shfl_sync(0xffffffffu, cur.tile, cur_i);
     const int st = issued % kStagesPerWarp;
     if (lane == 0) {
+      stage_tile[st] = t;  // read back by the fused append
       if (t >= 0) {
         mbar_arrive_expect_tx(&full_bar[st], 2 * kTileBytes);
         const size_t off = static_cast<size_t>(t) * kTileBytes;
@@ -541,6 +550,15 @@ paged_decode_kernel(const KParams p) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) qf[h][i] = make_float2(f[i].x * p.q_scale, f[i].y * p.q_scale);
     }
+    // Fused append: this piece holds the (sequence, kv head)'s last tile, whose row
+    // (L - 1) % 16 is the new token.  Lanes 0-7 carry its K chunks, 8-15 its V chunks.
+    const bool append_here = p.k_new != nullptr && pc.b1 == pc.nb && lane < 16;
+    uint4 new_row = make_uint4(0, 0, 0, 0);
+    if (append_here) {
+      const uint8_t* src = (lane < 8 ? p.k_new : p.v_new) +
+                           (static_cast<int64_t>(pc.s) * KV + pc.g) * kRowBytes + (lane & 7) * 16;
+      new_row = ldg_nc128(src);
+    }
     float m = -INFINITY, l = 0.f;
     float2 o[GROUP][4];
 #pragma unroll
@@ -561,6 +579,20 @@ paged_decode_kernel(const KParams p) {
       const uint8_t* kt = ring + st * 2 * kTileBytes;
       const uint8_t* vt = kt + kTileBytes;
       const int valid = L - (pc.b0 + k) * kBlockSize;
+      if (p.k_new != nullptr && pc.b0 + k == pc.nb - 1) {
+        // the new token: into the tile before it is read, and into its slot in the pools
+        if (append_here) {
+          const int off = ((L - 1) % kBlockSize) * kRowBytes + (lane & 7) * 16;
+          uint8_t* tile = const_cast<uint8_t*>(lane < 8 ? kt : vt);
+          *reinterpret_cast<uint4*>(tile + off) = new_row;
+          const int32_t t = stage_tile[st];
+          if (t >= 0) {
+            uint8_t* pool = lane < 8 ? p.key_cache_w : p.value_cache_w;
+            *reinterpret_cast<uint4*>(pool + static_cast<size_t>(t) * kTileBytes + off) = new_row;
+          }
+        }
+        __syncwarp();
+      }
       if (valid >= kBlockSize) {
         attend_tile<GROUP, false>(kt, vt, lane, tg, dq, kBlockSize, qf, m, l, o);
       } else {
@@ -812,6 +844,10 @@ cudaError_t launch(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t str
   p.seg_count = reinterpret_cast<int32_t*>(ws + plan.ws_count_offset);
   p.partials = reinterpret_cast<float*>(ws + plan.ws_meta_bytes);
   p.fused_merge = plan.fused_merge ? 1 : 0;
+  p.k_new = static_cast<const uint8_t*>(a.k_new);
+  p.v_new = static_cast<const uint8_t*>(a.v_new);
+  p.key_cache_w = static_cast<uint8_t*>(const_cast<void*>(a.key_cache));
+  p.value_cache_w = static_cast<uint8_t*>(const_cast<void*>(a.value_cache));
   p.status = a.status;
   paged_decode_kernel<GROUP><<<plan.grid, kWarps * 32, plan.smem_bytes, stream>>>(p);
   e = cudaGetLastError();

@@ -56,6 +56,8 @@ struct DecodeArgs {
   float scale;
   void* workspace;
   int32_t* status;
+  const void* k_new = nullptr;  // fused append (pa_decode_append), else null
+  const void* v_new = nullptr;
 };
 
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream);
