@@ -45,6 +45,8 @@ def parse_args():
     ap.add_argument("--append", choices=["fused", "separate"], default="fused",
                     help="decode-only steps: store the new tokens inside the decode launch "
                          "(pa_decode_append) or with pa_reshape_and_cache first")
+    ap.add_argument("--launch", choices=["eager", "graph"], default="graph",
+                    help="time the step as eager C-ABI calls or as one CUDA-graph replay")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=None,
@@ -314,24 +316,40 @@ def run_gpu(args, rank, world):
     time.sleep(0.3)
     torch.cuda.synchronize(dev)
     barrier()
+    graph = None
+    if args.launch == "graph":
+        from paged_kv_cache_299_gb300 import graphs
+        graph = graphs.StepGraph(st.step)
     t_wall = time.perf_counter()
     for k in range(K):
         if flush:
             flush_buf.fill_(k)  # rewrite a buffer of twice the L2 size between steps
         step_ev[k][0].record()
-        st.step(dec_ev[k] if w.num_decode else None, pre_ev[k] if pre_ev else None)
+        if graph is not None:
+            graph.replay()
+        else:
+            st.step(dec_ev[k] if w.num_decode else None, pre_ev[k] if pre_ev else None)
         step_ev[k][1].record()
     torch.cuda.synchronize(dev)
+    if graph is not None:  # per-kernel timing: an eager pass right after, same workload
+        for k in range(min(K, 20)):
+            if flush:
+                flush_buf.fill_(k)
+            st.step(dec_ev[k] if w.num_decode else None, pre_ev[k] if pre_ev else None)
+        torch.cuda.synchronize(dev)
     barrier()
     wall = time.perf_counter() - t_wall
     clocks = sampler.stop()
     step_ms = sum(a.elapsed_time(b) for a, b in step_ev) / K
+    n_kernel_steps = min(K, 20) if graph is not None else K
     dec_ms = None
     if w.num_decode:
-        dec_ms = sum(a.elapsed_time(b) for row in dec_ev for a, b in row) / (K * w.layers)
+        dec_ms = sum(a.elapsed_time(b) for row in dec_ev[:n_kernel_steps] for a, b in row) / (
+            n_kernel_steps * w.layers)
     pre_ms = None
     if pre_ev:
-        pre_ms = sum(a.elapsed_time(b) for row in pre_ev for a, b in row) / (K * w.layers)
+        pre_ms = sum(a.elapsed_time(b) for row in pre_ev[:n_kernel_steps] for a, b in row) / (
+            n_kernel_steps * w.layers)
     if world > 1:
         t = torch.tensor([step_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -340,7 +358,7 @@ def run_gpu(args, rank, world):
     # ---- end to end through the public API with host buffers ----
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(st, max(3, min(K, 50)), dev)
+        e2e = run_e2e(st, max(3, min(K, 50)), dev, graph)
         if world > 1:
             t = torch.tensor([e2e["step_ms"]], device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -359,7 +377,9 @@ def run_gpu(args, rank, world):
                        accumulate="f32",
                        l2=("flushed between steps (2x L2 rewrite)" if flush
                            else "inputs larger than L2 (%.1f GB KV per step)" % (kv_bytes / 1e9)),
-                       launch="eager (one C-ABI call per kernel group)",
+                       launch=("CUDA graph: one replay per step (kernel times from an "
+                               "eager pass right after)" if graph is not None
+                               else "eager (one C-ABI call per kernel group)"),
                        store=("fused into decode (pa_decode_append)" if st.fused_append
                               else "pa_compute_slot_mapping + pa_reshape_and_cache")),
         "tokens_per_s": round(w.num_decode * world / (step_ms * 1e-3), 1),
@@ -395,7 +415,7 @@ def run_gpu(args, rank, world):
     print(json.dumps(res), flush=True)
 
 
-def run_e2e(st: DeviceStep, steps: int, dev) -> dict:
+def run_e2e(st: DeviceStep, steps: int, dev, graph=None) -> dict:
     """Each step: pinned host -> device copy of the step's inputs (queries, new K/V, block
     tables, context lengths), the step through the C ABI, device -> host copy of the
     attention outputs.  Timed on the device with events around the whole loop."""
@@ -419,7 +439,10 @@ def run_e2e(st: DeviceStep, steps: int, dev) -> dict:
     def one():
         for h, d in host_in:
             d.copy_(h, non_blocking=True)
-        st.step()
+        if graph is not None:
+            graph.replay()
+        else:
+            st.step()
         for h, d in host_out:
             h.copy_(d, non_blocking=True)
 
