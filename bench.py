@@ -75,6 +75,23 @@ def ncu_traffic(cfg: int):
         return None
 
 
+def max_over_ranks(value: float, device) -> float:
+    """Slowest rank's time (every rank gets it); identity for a single process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank: int, world: int, step_ms: float) -> float:
+    """Weak scaling: every rank moves bytes_per_rank per step; the job's throughput is
+    all ranks' bytes over the slowest rank's step time."""
+    return bytes_per_rank * world / (step_ms * 1e-3) / 1e9
+
+
 def measured_bf16_peak():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -350,24 +367,18 @@ def run_gpu(args, rank, world):
     if pre_ev:
         pre_ms = sum(a.elapsed_time(b) for row in pre_ev[:n_kernel_steps] for a, b in row) / (
             n_kernel_steps * w.layers)
-    if world > 1:
-        t = torch.tensor([step_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(step_ms, dev)
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(st, max(3, min(K, 50)), dev, graph)
-        if world > 1:
-            t = torch.tensor([e2e["step_ms"]], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e["step_ms"] = float(t.item())
+        e2e["step_ms"] = max_over_ranks(e2e["step_ms"], dev)
 
     if rank != 0:
         return
     peak, peak_src = measured_peaks()
-    value = kv_bytes * world / (step_ms * 1e-3) / 1e9
+    value = whole_job_gbs(kv_bytes, world, step_ms)
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
@@ -407,7 +418,7 @@ def run_gpu(args, rank, world):
             "peak_source": f"{bf16_src} bf16_tflops_sustained", "launch_ms": round(pre_ms, 5),
             "algorithmic_flops_per_launch": round(st.prefill_flops() / w.layers)}
     if e2e:
-        res["e2e"] = {"value": round(kv_bytes * world / (e2e["step_ms"] * 1e-3) / 1e9, 1),
+        res["e2e"] = {"value": round(whole_job_gbs(kv_bytes, world, e2e["step_ms"]), 1),
                       "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
                       "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e["step_ms"], 4)}
     if not args.no_cpu_baseline and world == 1:

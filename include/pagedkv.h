@@ -243,6 +243,14 @@ int64_t pa_bm_num_tokens(const pa_block_manager* bm, int64_t seq_id);
 int32_t pa_bm_block_table(const pa_block_manager* bm, int64_t seq_id, int32_t* out,
                           int32_t max_blocks);
 
+/* Diagnostic for the failure path: launches one warp that waits on an mbarrier nothing
+ * arrives on, using the bounded wait of the pipelines with a limit of limit_ms (1..1000);
+ * when it expires the kernel sets PA_DEVFLAG_TIMEOUT in *device_status and returns.  Lets a
+ * test confirm that a stalled pipeline reports instead of hanging and leaves the context
+ * usable.  No counterpart on the pages (engineering support only). */
+pa_status pa_selftest_wait_timeout(int32_t* device_status, int32_t limit_ms,
+                                   pa_stream_t stream);
+
 /* Synchronise `stream`, read *device_status and translate it: PA_OK when zero,
  * PA_ERR_DEVICE_TIMEOUT when the timeout bit is set, else PA_ERR_DEVICE_INDEX. */
 pa_status pa_check_device_status(const int32_t* device_status, pa_stream_t stream);

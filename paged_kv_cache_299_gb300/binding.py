@@ -45,7 +45,7 @@ EXPORTED = ("pa_compute_slot_mapping", "pa_reshape_and_cache", "pa_decode_worksp
             "pa_last_error", "pa_decode_static_scratch", "pa_copy_blocks", "pa_bm_create",
             "pa_bm_destroy", "pa_bm_num_free_blocks", "pa_bm_ref_count", "pa_bm_add_sequence",
             "pa_bm_fork", "pa_bm_append_tokens", "pa_bm_free_sequence", "pa_bm_num_tokens",
-            "pa_bm_block_table", "pa_decode_append")
+            "pa_bm_block_table", "pa_decode_append", "pa_selftest_wait_timeout")
 
 
 def library_path() -> str:
@@ -105,6 +105,8 @@ def load(path: str | None = None):
     lib.pa_bm_num_tokens.restype = i64
     lib.pa_bm_block_table.argtypes = [P, i64, P, i32]
     lib.pa_bm_block_table.restype = i32
+    lib.pa_selftest_wait_timeout.argtypes = [P, i32, P]
+    lib.pa_selftest_wait_timeout.restype = st
     lib.pa_check_device_status.argtypes = [P, P]
     lib.pa_check_device_status.restype = st
     lib.pa_status_string.argtypes = [st]
@@ -382,3 +384,10 @@ class BlockManager:
         if n < 0:
             _check(n, "pa_bm_block_table")
         return [int(out[i]) for i in range(max_blocks)], n
+
+
+def pa_selftest_wait_timeout(device_status, limit_ms=50, stream=None):
+    """Launch the bounded-wait diagnostic (see include/pagedkv.h)."""
+    _need(device_status, "device_status", torch.int32, 1)
+    _check(load().pa_selftest_wait_timeout(_ptr(device_status), int(limit_ms), _stream(stream)),
+           "pa_selftest_wait_timeout")

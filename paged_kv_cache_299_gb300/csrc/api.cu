@@ -273,6 +273,15 @@ pa_status pa_copy_blocks(void* key_cache, void* value_cache, pa_cache_desc cd,
                    "copy_blocks launch");
 }
 
+pa_status pa_selftest_wait_timeout(int32_t* device_status, int32_t limit_ms,
+                                   pa_stream_t stream) {
+  if (!device_status) return fail(PA_ERR_INVALID_ARG, "null status pointer");
+  if (limit_ms < 1 || limit_ms > 1000) return fail(PA_ERR_INVALID_ARG, "limit_ms %d", limit_ms);
+  return from_cuda(pkv::launch_wait_timeout_selftest(device_status, limit_ms,
+                                                     reinterpret_cast<cudaStream_t>(stream)),
+                   "timeout self-test launch");
+}
+
 pa_status pa_check_device_status(const int32_t* device_status, pa_stream_t stream) {
   if (!device_status) return fail(PA_ERR_INVALID_ARG, "null status pointer");
   int32_t word = 0;

@@ -89,6 +89,32 @@ __global__ void reshape_and_cache_kernel(const uint4* __restrict__ key,
   value_cache[dst] = vv;
 }
 
+// Diagnostic: one warp waits on an mbarrier that nothing ever arrives on, with the same
+// bounded-wait loop the pipelines use but a caller-chosen limit; when the limit passes it
+// records PA_DEVFLAG_TIMEOUT and returns, leaving the context usable.
+__global__ void wait_timeout_selftest_kernel(int32_t* status, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(&bar, 0)) {
+    if (global_timer_ns() - t0 > limit_ns) {
+      flag_error(status, PA_DEVFLAG_TIMEOUT);
+      return;
+    }
+  }
+}
+
+cudaError_t launch_wait_timeout_selftest(int32_t* status, int32_t limit_ms, cudaStream_t stream) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(
+      status, static_cast<unsigned long long>(limit_ms) * 1000000ull);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_seq,
                                 const int32_t* context_lens, const int32_t* query_start_loc,
                                 int32_t num_seqs, int32_t num_tokens, int32_t num_blocks,

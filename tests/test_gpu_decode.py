@@ -238,3 +238,13 @@ def test_split_segments_merged_in_kernel_and_workspace_reuse():
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
     ref = oracle_step(w, host_vals(step.vals))
     assert_close(outs[0], ref["decode"], "long contexts, in-kernel merge")
+
+
+def test_a_wait_that_runs_out_reports_timeout_and_leaves_the_context_usable():
+    status = pa.new_device_status()
+    pa.pa_selftest_wait_timeout(status, limit_ms=50)
+    assert pa.pa_check_device_status(status) == pa.PA_ERR_DEVICE_TIMEOUT
+    assert int(status.item()) & pa.DEVFLAG_TIMEOUT
+    w = wl.random_small(77, num_seqs=2, max_ctx=50)
+    step = GpuStep(w)
+    assert torch.isfinite(step.decode().float()).all()
