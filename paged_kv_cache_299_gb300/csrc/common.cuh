@@ -113,6 +113,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Maximum of three floats in one instruction.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Two packed bf16 (low half = lower index) -> float2, exact.
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));

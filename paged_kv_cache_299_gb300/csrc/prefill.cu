@@ -12,12 +12,13 @@
 //   * One CTA per (32-token query tile, K/V head, sequence).  Its 128 MMA rows are the
 //     32 tokens x 4 query heads that share the K/V head (row = 4 * token + head), so each
 //     K/V tile feeds four heads.
-//   * Warp 5 loads the Q tile with one 3-D TMA box and gathers every 128-key K/V tile as
-//     eight 16-row TMA boxes at the physical blocks named by the block table (128-byte
-//     swizzle), into a 2-stage ring.
-//   * Warp 4 (one thread) issues S = Q K^T (M128 N128 K64, fp32 in TMEM columns 0..127)
-//     and O += P V (M128 N64 K128, TMEM columns 128..191, V read N-major) and commits
-//     them to mbarriers.
+//   * Warp 5 loads the Q tile with one 3-D TMA box and gathers every 64-key K/V tile as
+//     four 16-row TMA boxes at the physical blocks named by the block table (128-byte
+//     swizzle), into a 4-stage ring.
+//   * Warp 4 (one thread) issues S = Q K^T (M128 N64 K64, fp32, two TMEM buffers so the
+//     next tile's scores are computed during this tile's softmax) and O += P V (M128 N64
+//     K64, TMEM columns 128..191, V read N-major) and commits them to mbarriers.
+//   * Two CTAs share an SM; query tiles with the longest causal span start first.
 //   * Warps 0-3 own one TMEM lane = one query row each: they read S, mask by absolute
 //     position, keep the running max / sum in registers (O in TMEM is rescaled only when
 //     the max grows by more than 2^8), write P as bf16 into a swizzled K-major smem tile,
@@ -37,19 +38,20 @@ namespace {
 constexpr int kGroup = 4;                         // query heads per K/V head
 constexpr int kTokensPerTile = 32;
 constexpr int kTileM = kTokensPerTile * kGroup;   // 128 MMA rows
-constexpr int kTileN = 128;                       // keys per K/V tile
+constexpr int kTileN = 64;                        // keys per K/V tile
 constexpr int kBlocksPerTile = kTileN / kBlockSize;
-constexpr int kStages = 2;
+constexpr int kStages = 4;                        // K/V ring depth
 constexpr int kQBytes = kTileM * kRowBytes;       // 16 KiB
-constexpr int kKVBytes = kTileN * kRowBytes;      // 16 KiB per K (or V) tile
-constexpr int kPRegionBytes = kTileM * 128;       // 64 keys x 128 rows of bf16
-constexpr int kPBytes = 2 * kPRegionBytes;        // 32 KiB
+constexpr int kKVBytes = kTileN * kRowBytes;      // 8 KiB per K (or V) tile
+constexpr int kPBytes = kTileM * kTileN * 2;      // 16 KiB: one 128-byte-swizzled region
+constexpr int kNumBars = 1 + 2 * kStages + 2 + 3; // q, kv full/empty, s x2, p, o, drain
 constexpr int kSmemBytes = kQBytes + 2 * kStages * kKVBytes + kPBytes + 8 * 16 + 16 + 16;
+static_assert(kNumBars <= 16, "barrier area");
 // Two CTAs fit on one SM (2 x (kSmemBytes + 1 KiB reserved) <= 228 KiB, 2 x 256 TMEM
 // columns = 512, <= 168 registers per thread), so one CTA's softmax overlaps the other's MMAs.
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kSCol = 0;
-constexpr uint32_t kOCol = 128;
+constexpr uint32_t kSCol = 0;     // two S buffers: columns 0..63 and 64..127
+constexpr uint32_t kOCol = 128;   // O: columns 128..191
 constexpr int kThreads = 192;
 constexpr float kRescaleThreshold = 8.0f;
 
@@ -79,9 +81,11 @@ __global__ void __launch_bounds__(kThreads, 2)
 paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
                      const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const PParams p) {
-  const int tile = blockIdx.x;
+  // The query-tile index is the slowest grid dimension, reversed: the tiles with the
+  // longest causal spans of every sequence and head are dispatched first.
+  const int tile = gridDim.z - 1 - blockIdx.z;
   const int g = blockIdx.y;
-  const int s = blockIdx.z;
+  const int s = blockIdx.x;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -113,8 +117,8 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = kv_full + kStages;
-  uint64_t* s_ready = kv_empty + kStages;
-  uint64_t* p_ready = s_ready + 1;
+  uint64_t* s_ready = kv_empty + kStages;  // [2]
+  uint64_t* p_ready = s_ready + 2;
   uint64_t* o_done = p_ready + 1;
   uint64_t* drain = o_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
@@ -126,7 +130,8 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
-    mbar_init(s_ready, 1);
+    mbar_init(&s_ready[0], 1);
+    mbar_init(&s_ready[1], 1);
     mbar_init(p_ready, kTileM);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
@@ -191,54 +196,48 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
     }
   } else if (warp == 4) {
     // ================================ MMA issuer ==================================
+    // Order: S(0), S(1), PV(0), S(2), PV(1), ...: the scores of the next tile are on the
+    // tensor core while the row warps run the softmax of the current one.
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(kTileM, kTileN, false);
       constexpr uint32_t kIdescO = idesc_bf16_f32(kTileM, kHeadDim, true);
-      const uint32_t s_tmem = tmem + kSCol;
       const uint32_t o_tmem = tmem + kOCol;
       const uint32_t q_base = smem_addr(sq);
       const uint32_t p_base = smem_addr(sp);
-      auto issue_pv = [&](int t) {
-        const uint32_t v_base = smem_addr(sv + (t % kStages) * kKVBytes);
-#pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk) {
-          const uint64_t a = sw128_desc(p_base + (kk / 4) * kPRegionBytes + (kk % 4) * 32, 16, 1024);
-          const uint64_t b = sw128_desc(v_base + kk * 16 * kRowBytes, 16, 1024);
-          umma_bf16(o_tmem, a, b, kIdescO, (t > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(o_done);
-        umma_commit(&kv_empty[t % kStages]);
-      };
-      bool ok = wait_or_abort(q_full, 0, &abort_flag, p.status);
-      int j = 0;
-      for (; ok && j < n_kv; ++j) {
+      auto issue_s = [&](int j) -> bool {
         const int st = j % kStages;
         if (!wait_or_abort(&kv_full[st], static_cast<uint32_t>((j / kStages) & 1), &abort_flag,
-                           p.status)) {
-          ok = false;
-          break;
-        }
+                           p.status))
+          return false;
         tc_fence_after_sync();
-        if (j > 0) {
-          if (!wait_or_abort(p_ready, static_cast<uint32_t>((j - 1) & 1), &abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          issue_pv(j - 1);
-        }
         const uint32_t k_base = smem_addr(sk + st * kKVBytes);
+        const uint32_t s_tmem = tmem + kSCol + (j & 1) * kTileN;
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 16; ++kk) {
           umma_bf16(s_tmem, sw128_desc(q_base + kk * 32, 16, 1024),
                     sw128_desc(k_base + kk * 32, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
         }
-        umma_commit(s_ready);
-      }
-      if (ok && wait_or_abort(p_ready, static_cast<uint32_t>((n_kv - 1) & 1), &abort_flag,
-                              p.status)) {
+        umma_commit(&s_ready[j & 1]);
+        return true;
+      };
+      auto issue_pv = [&](int j) {
+        const uint32_t v_base = smem_addr(sv + (j % kStages) * kKVBytes);
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk) {
+          const uint64_t a = sw128_desc(p_base + kk * 32, 16, 1024);
+          const uint64_t b = sw128_desc(v_base + kk * 16 * kRowBytes, 16, 1024);
+          umma_bf16(o_tmem, a, b, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(o_done);
+        umma_commit(&kv_empty[j % kStages]);
+      };
+      bool ok = wait_or_abort(q_full, 0, &abort_flag, p.status);
+      if (ok) ok = issue_s(0);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        if (j + 1 < n_kv && !issue_s(j + 1)) break;  // S buffer (j+1)&1 was freed by P(j-1)
+        if (!wait_or_abort(p_ready, static_cast<uint32_t>(j & 1), &abort_flag, p.status)) break;
         tc_fence_after_sync();
-        issue_pv(n_kv - 1);
+        issue_pv(j);
       }
       // wait (bounded) until every MMA issued above has completed
       umma_commit(drain);
@@ -252,28 +251,41 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
     const int token = tok0 + tt;
     const bool row_ok = token < q_len;
     const int pos = L - q_len + min(token, q_len - 1);
+    const int pos_lo = L - q_len + tok0;  // smallest position among this CTA's rows
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     float m = -INFINITY;
     float l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      ok = wait_or_abort(s_ready, static_cast<uint32_t>(j & 1), &abort_flag, p.status);
+      ok = wait_or_abort(&s_ready[j & 1], static_cast<uint32_t>((j >> 1) & 1), &abort_flag,
+                         p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after_sync();
       const int kb = j * kTileN;
-      uint32_t v[32];
-      float mt = -INFINITY;
+      const uint32_t s_addr = lane_addr + kSCol + (j & 1) * kTileN;
+      uint32_t v[2][32];  // raw scores; then, in place in v[0], packed bf16 probabilities
+      tmem_ld32(s_addr, v[0]);
+      tmem_ld32(s_addr + 32, v[1]);
+      tmem_wait_ld();
+      if (kb + kTileN - 1 > pos_lo) {
+        // a tile on the causal diagonal (uniform over the CTA): hide keys past each row's
+        // position before the maximum; exp2(-inf) = 0 then drops them from P and the sum
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld32(lane_addr + kSCol + 32 * c, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float x = kb + 32 * c + i <= pos ? __uint_as_float(v[i]) * p.qk_scale : -INFINITY;
-          mt = fmaxf(mt, x);
-        }
+        for (int i = 0; i < kTileN; ++i)
+          if (kb + i > pos) v[i >> 5][i & 31] = __float_as_uint(-INFINITY);
       }
+      // tile maximum of the raw scores (the scale is positive, so it commutes with max)
+      float mx[4];
+#pragma unroll
+      for (int a4 = 0; a4 < 4; ++a4) {
+        mx[a4] = __uint_as_float(v[a4 >> 1][16 * (a4 & 1)]);
+#pragma unroll
+        for (int i = 1; i < 16; i += 2)
+          mx[a4] = max3f(mx[a4], __uint_as_float(v[a4 >> 1][16 * (a4 & 1) + i]),
+                         __uint_as_float(v[a4 >> 1][16 * (a4 & 1) + i + 1]));
+      }
+      const float mt = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])) * p.qk_scale;
       const float m_new = fmaxf(m, mt);
       const bool grow = m_new - m > kRescaleThreshold;  // true on the first tile (m = -inf)
       float alpha = 1.f;
@@ -281,54 +293,59 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
         alpha = fast_exp2(m - m_new);
         m = m_new;
       }
-      if (j > 0) {
-        // the previous P.V must be done: P is overwritten below and O may be rescaled
-        ok = wait_or_abort(o_done, static_cast<uint32_t>((j - 1) & 1), &abort_flag, p.status);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after_sync();
-        if (__any_sync(0xffffffffu, grow)) {
+      // p = 2^(s * scale - m) two at a time, packed to bf16 into v[0]
+      const float2 qs2 = make_float2(p.qk_scale, p.qk_scale);
+      const float2 nm2 = make_float2(-m, -m);
+      float2 sum2 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            tmem_ld32(lane_addr + kOCol + 32 * c, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-            tmem_st32(lane_addr + kOCol + 32 * c, v);
-          }
-          tmem_wait_st();
-        }
+      for (int i = 0; i < kTileN / 2; ++i) {
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(v[i >> 4][(2 * i) & 31]),
+                                                __uint_as_float(v[i >> 4][(2 * i + 1) & 31])),
+                                    qs2, nm2);
+        const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+        sum2 = __fadd2_rn(sum2, e);
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(e.x, e.y);
+        v[0][i] = *reinterpret_cast<const uint32_t*>(&b2);
       }
-      if (j == n_kv - 1 && kb + r >= keys) {
+      const float psum = sum2.x + sum2.y;
+      if (j == n_kv - 1 && r < kTileN && kb + r >= keys) {
         // V rows past the last needed key are never weighted, but may hold NaN (unused
         // slots) or stale data: zero them so 0 * V stays 0 in the tensor core.
         uint4* vrow = reinterpret_cast<uint4*>(sv + (j % kStages) * kKVBytes + r * kRowBytes);
 #pragma unroll
         for (int i = 0; i < kRowBytes / 16; ++i) vrow[i] = make_uint4(0, 0, 0, 0);
       }
-      float psum = 0.f;
-      __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the row-local branch
+      if (j > 0) {
+        // P(j-1) must be consumed before P(j) overwrites it, and O may need rescaling
+        ok = wait_or_abort(o_done, static_cast<uint32_t>((j - 1) & 1), &abort_flag, p.status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after_sync();
+        if (__any_sync(0xffffffffu, grow)) {
+          uint32_t(&o)[32] = v[1];  // the raw scores there are spent
+          const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld32(lane_addr + kSCol + 32 * c, v);
-        tmem_wait_ld();
-        uint32_t packed[16];
+          for (int c = 0; c < 2; ++c) {
+            tmem_ld32(lane_addr + kOCol + 32 * c, o);
+            tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int k0 = kb + 32 * c + 2 * i;
-          const float p0 = k0 <= pos ? fast_exp2(__uint_as_float(v[2 * i]) * p.qk_scale - m) : 0.f;
-          const float p1 = k0 + 1 <= pos ? fast_exp2(__uint_as_float(v[2 * i + 1]) * p.qk_scale - m) : 0.f;
-          psum += p0 + p1;
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-          packed[i] = *reinterpret_cast<const uint32_t*>(&b2);
+            for (int i = 0; i < 16; ++i) {
+              const float2 x = __fmul2_rn(
+                  make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), a2);
+              o[2 * i] = __float_as_uint(x.x);
+              o[2 * i + 1] = __float_as_uint(x.y);
+            }
+            tmem_st32(lane_addr + kOCol + 32 * c, o);
+          }
+          tmem_wait_st();
         }
-        uint8_t* region = sp + (c >> 1) * kPRegionBytes + r * 128;
+      }
+      uint8_t* prow = sp + r * 128;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int chunk = ((c & 1) * 4 + q4) ^ (r & 7);
-          *reinterpret_cast<uint4*>(region + chunk * 16) =
-              make_uint4(packed[4 * q4], packed[4 * q4 + 1], packed[4 * q4 + 2], packed[4 * q4 + 3]);
-        }
+      for (int q4 = 0; q4 < kTileN / 8; ++q4) {
+        const int chunk = q4 ^ (r & 7);
+        *reinterpret_cast<uint4*>(prow + chunk * 16) =
+            make_uint4(v[0][4 * q4], v[0][4 * q4 + 1], v[0][4 * q4 + 2], v[0][4 * q4 + 3]);
       }
       l = l * alpha + psum;
       fence_proxy_async_smem();
@@ -447,7 +464,9 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.num_q_heads = a.num_q_heads;
   p.qk_scale = a.scale * 1.4426950408889634f;
   p.status = a.status;
-  dim3 grid((a.max_query_len + kTokensPerTile - 1) / kTokensPerTile, a.num_kv_heads, a.num_seqs);
+  const int tiles = (a.max_query_len + kTokensPerTile - 1) / kTokensPerTile;
+  if (tiles > 65535 || a.num_kv_heads > 65535) return cudaErrorInvalidValue;
+  dim3 grid(a.num_seqs, a.num_kv_heads, tiles);
   paged_prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
