@@ -14,7 +14,7 @@
 //     K/V tile feeds four heads.
 //   * Warp 5 loads the Q tile with one 3-D TMA box and gathers every 64-key K/V tile as
 //     four 16-row TMA boxes at the physical blocks named by the block table (128-byte
-//     swizzle), into a 4-stage ring.
+//     swizzle), into a 3-stage ring.
 //   * Warp 4 (one thread) issues S = Q K^T (M128 N64 K64, fp32, two TMEM buffers so the
 //     next tile's scores are computed during this tile's softmax) and O += P V (M128 N64
 //     K64, TMEM columns 128..191, V read N-major) and commits them to mbarriers.
@@ -22,7 +22,8 @@
 //   * Warps 0-3 own one TMEM lane = one query row each: they read S, mask by absolute
 //     position, keep the running max / sum in registers (O in TMEM is rescaled only when
 //     the max grows by more than 2^8), write P as bf16 into a swizzled K-major smem tile,
-//     and finally normalise O and store bf16 rows.
+//     and finally normalise O and store bf16 rows.  P is double-buffered: the softmax of
+//     tile j+1 waits for the P V of tile j only when O must be rescaled.
 // Every mbarrier wait is bounded; on timeout the CTA records PA_DEVFLAG_TIMEOUT, drains
 // its own copies and MMAs, frees its tensor memory and returns.
 #include <cudaTypedefs.h>
@@ -43,15 +44,16 @@ constexpr int kBlocksPerTile = kTileN / kBlockSize;
 constexpr int kStages = 4;                        // K/V ring depth
 constexpr int kQBytes = kTileM * kRowBytes;       // 16 KiB
 constexpr int kKVBytes = kTileN * kRowBytes;      // 8 KiB per K (or V) tile
-constexpr int kPBytes = kTileM * kTileN * 2;      // 16 KiB: one 128-byte-swizzled region
-constexpr int kNumBars = 1 + 2 * kStages + 2 + 3; // q, kv full/empty, s x2, p, o, drain
-constexpr int kSmemBytes = kQBytes + 2 * kStages * kKVBytes + kPBytes + 8 * 16 + 16 + 16;
+constexpr int kNumBars = 1 + 2 * kStages + 2 + 4; // q, kv full/empty, s x2, p, o, drain, q_tmem
+constexpr int kSmemBytes = kQBytes + 2 * kStages * kKVBytes + 8 * 16 + 16 + 16;
 static_assert(kNumBars <= 16, "barrier area");
 // Two CTAs fit on one SM (2 x (kSmemBytes + 1 KiB reserved) <= 228 KiB, 2 x 256 TMEM
 // columns = 512, <= 168 registers per thread), so one CTA's softmax overlaps the other's MMAs.
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kSCol = 0;     // two S buffers: columns 0..63 and 64..127
-constexpr uint32_t kOCol = 128;   // O: columns 128..191
+constexpr uint32_t kSCol = 0;     // two S buffers (fp32): columns 0..63 and 64..127
+constexpr uint32_t kOCol = 128;   // O (fp32): columns 128..191
+constexpr uint32_t kQCol = 192;   // Q (bf16 pairs): columns 192..223, the A operand of S = Q K^T
+constexpr uint32_t kPCol = 224;   // P (bf16 pairs): columns 224..255, the A operand of O += P V
 constexpr int kThreads = 192;
 constexpr float kRescaleThreshold = 8.0f;
 
@@ -112,8 +114,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
   uint8_t* sq = smem;
   uint8_t* sk = sq + kQBytes;
   uint8_t* sv = sk + kStages * kKVBytes;
-  uint8_t* sp = sv + kStages * kKVBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sp + kPBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sv + kStages * kKVBytes);
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = kv_full + kStages;
@@ -121,6 +122,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
   uint64_t* p_ready = s_ready + 2;
   uint64_t* o_done = p_ready + 1;
   uint64_t* drain = o_done + 1;
+  uint64_t* q_tmem = drain + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int& abort_flag = *reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -135,6 +137,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
     mbar_init(p_ready, kTileM);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
+    mbar_init(q_tmem, kTileM);
     fence_barrier_init();
     abort_flag = 0;
   }
@@ -196,14 +199,13 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
     }
   } else if (warp == 4) {
     // ================================ MMA issuer ==================================
-    // Order: S(0), S(1), PV(0), S(2), PV(1), ...: the scores of the next tile are on the
-    // tensor core while the row warps run the softmax of the current one.
+    // Both A operands live in tensor memory (Q copied there once, P written there by the
+    // row warps), so each MMA streams only its B tile (K or V, 2 KiB per K16 step) from
+    // shared memory.  Order: S(0), S(1), PV(0), S(2), PV(1), ...: the scores of the next
+    // tile are on the tensor core while the row warps run the softmax of the current one.
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(kTileM, kTileN, false);
       constexpr uint32_t kIdescO = idesc_bf16_f32(kTileM, kHeadDim, true);
-      const uint32_t o_tmem = tmem + kOCol;
-      const uint32_t q_base = smem_addr(sq);
-      const uint32_t p_base = smem_addr(sp);
       auto issue_s = [&](int j) -> bool {
         const int st = j % kStages;
         if (!wait_or_abort(&kv_full[st], static_cast<uint32_t>((j / kStages) & 1), &abort_flag,
@@ -214,8 +216,8 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
         const uint32_t s_tmem = tmem + kSCol + (j & 1) * kTileN;
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-          umma_bf16(s_tmem, sw128_desc(q_base + kk * 32, 16, 1024),
-                    sw128_desc(k_base + kk * 32, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+          umma_bf16_ts(s_tmem, tmem + kQCol + kk * 8, sw128_desc(k_base + kk * 32, 16, 1024),
+                       kIdescS, kk > 0 ? 1u : 0u);
         }
         umma_commit(&s_ready[j & 1]);
         return true;
@@ -224,15 +226,17 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
         const uint32_t v_base = smem_addr(sv + (j % kStages) * kKVBytes);
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk) {
-          const uint64_t a = sw128_desc(p_base + kk * 32, 16, 1024);
           const uint64_t b = sw128_desc(v_base + kk * 16 * kRowBytes, 16, 1024);
-          umma_bf16(o_tmem, a, b, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + kOCol, tmem + kPCol + kk * 8, b, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(o_done);
         umma_commit(&kv_empty[j % kStages]);
       };
-      bool ok = wait_or_abort(q_full, 0, &abort_flag, p.status);
-      if (ok) ok = issue_s(0);
+      bool ok = wait_or_abort(q_tmem, 0, &abort_flag, p.status);
+      if (ok) {
+        tc_fence_after_sync();
+        ok = issue_s(0);
+      }
       for (int j = 0; ok && j < n_kv; ++j) {
         if (j + 1 < n_kv && !issue_s(j + 1)) break;  // S buffer (j+1)&1 was freed by P(j-1)
         if (!wait_or_abort(p_ready, static_cast<uint32_t>(j & 1), &abort_flag, p.status)) break;
@@ -255,8 +259,26 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     float m = -INFINITY;
     float l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
+    bool ok = wait_or_abort(q_full, 0, &abort_flag, p.status);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      // copy this row of the (128-byte swizzled) Q tile into tensor memory
+      uint32_t qv[32];
+      const uint8_t* qrow = sq + r * kRowBytes;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 x = lds128(qrow + ((c ^ (r & 7)) * 16));
+        qv[4 * c] = x.x;
+        qv[4 * c + 1] = x.y;
+        qv[4 * c + 2] = x.z;
+        qv[4 * c + 3] = x.w;
+      }
+      tmem_st32(lane_addr + kQCol, qv);
+      tmem_wait_st();
+      tc_fence_before_sync();
+      mbar_arrive(q_tmem);
+    }
+    for (int j = 0; ok && j < n_kv; ++j) {
       ok = wait_or_abort(&s_ready[j & 1], static_cast<uint32_t>((j >> 1) & 1), &abort_flag,
                          p.status);
       ok = __all_sync(0xffffffffu, ok);
@@ -307,13 +329,13 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
         const __nv_bfloat162 b2 = __floats2bfloat162_rn(e.x, e.y);
         v[0][i] = *reinterpret_cast<const uint32_t*>(&b2);
       }
-      const float psum = sum2.x + sum2.y;
       if (j == n_kv - 1 && r < kTileN && kb + r >= keys) {
         // V rows past the last needed key are never weighted, but may hold NaN (unused
         // slots) or stale data: zero them so 0 * V stays 0 in the tensor core.
         uint4* vrow = reinterpret_cast<uint4*>(sv + (j % kStages) * kKVBytes + r * kRowBytes);
 #pragma unroll
         for (int i = 0; i < kRowBytes / 16; ++i) vrow[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
       }
       if (j > 0) {
         // P(j-1) must be consumed before P(j) overwrites it, and O may need rescaling
@@ -337,18 +359,11 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
             }
             tmem_st32(lane_addr + kOCol + 32 * c, o);
           }
-          tmem_wait_st();
         }
       }
-      uint8_t* prow = sp + r * 128;
-#pragma unroll
-      for (int q4 = 0; q4 < kTileN / 8; ++q4) {
-        const int chunk = q4 ^ (r & 7);
-        *reinterpret_cast<uint4*>(prow + chunk * 16) =
-            make_uint4(v[0][4 * q4], v[0][4 * q4 + 1], v[0][4 * q4 + 2], v[0][4 * q4 + 3]);
-      }
-      l = l * alpha + psum;
-      fence_proxy_async_smem();
+      tmem_st32(lane_addr + kPCol, v[0]);
+      l = l * alpha + (sum2.x + sum2.y);
+      tmem_wait_st();
       tc_fence_before_sync();
       mbar_arrive(p_ready);
     }
