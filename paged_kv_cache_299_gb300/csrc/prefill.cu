@@ -47,6 +47,7 @@ constexpr int kKVBytes = kTileN * kRowBytes;      // 8 KiB per K (or V) tile
 constexpr int kNumBars = 1 + 2 * kStages + 2 + 4; // q, kv full/empty, s x2, p, o, drain, q_tmem
 constexpr int kSmemBytes = kQBytes + 2 * kStages * kKVBytes + 8 * 16 + 16 + 16;
 static_assert(kNumBars <= 16, "barrier area");
+static_assert(32 % kBlocksPerTile == 0, "block-table windows hold whole K/V tiles");
 // Two CTAs fit on one SM (2 x (kSmemBytes + 1 KiB reserved) <= 228 KiB, 2 x 256 TMEM
 // columns = 512, <= 168 registers per thread), so one CTA's softmax overlaps the other's MMAs.
 constexpr uint32_t kTmemCols = 256;
@@ -162,12 +163,28 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
       mbar_arrive_expect_tx(q_full, kQBytes);
       tma_load_3d(sq, &tmap_q, 0, g * kGroup, q0 + tok0, q_full);
     }
+    // The block table is read 32 entries (eight K/V tiles) at a time, one entry per lane,
+    // with the next window already in flight, so no tile waits on a block-table load.
+    auto fetch = [&](int base) -> int32_t {
+      return base + lane < blocks_needed ? __ldg(row + base + lane) : 0;
+    };
+    int win_base = 0;
+    int32_t win = fetch(0);
+    int32_t win_next = fetch(32);
     int issued = 0;
     for (int j = 0; j < n_kv; ++j) {
       const int st = j % kStages;
-      const int lb = j * kBlocksPerTile + lane;
+      const int lb0 = j * kBlocksPerTile;
+      if (lb0 >= win_base + 32) {
+        win_base += 32;
+        win = win_next;
+        win_next = fetch(win_base + 32);
+      }
+      const int lb = lb0 + lane;
       const bool need = lane < kBlocksPerTile && lb < blocks_needed;
-      const int32_t phys = need ? __ldg(row + lb) : 0;
+      const int32_t entry =
+          __shfl_sync(0xffffffffu, win, (lb0 - win_base) + (lane & (kBlocksPerTile - 1)));
+      const int32_t phys = need ? entry : 0;
       const bool bad = need && (phys < 0 || phys >= p.num_blocks);
       const bool load = need && !bad;
       const unsigned mask = __ballot_sync(0xffffffffu, load);
