@@ -8,22 +8,25 @@
 // over key tiles so no score matrix reaches HBM.
 //
 // GB300 design.  QK^T and PV are dense contractions, so they run on the 5th-generation
-// tensor cores with accumulators in tensor memory:
-//   * One CTA per (32-token query tile, K/V head, sequence).  Its 128 MMA rows are the
-//     32 tokens x 4 query heads that share the K/V head (row = 4 * token + head), so each
-//     K/V tile feeds four heads.
+// tensor cores with accumulators in tensor memory (TMEM):
+//   * One CTA per (32-token query tile, K/V head, sequence), two CTAs per SM.  Its 128 MMA
+//     rows are the 32 tokens x 4 query heads that share the K/V head (row = 4 * token +
+//     head), so each K/V tile feeds four heads.  The query-tile index is the slowest grid
+//     dimension, reversed, so the tiles with the longest causal spans start first.
 //   * Warp 5 loads the Q tile with one 3-D TMA box and gathers every 64-key K/V tile as
 //     four 16-row TMA boxes at the physical blocks named by the block table (128-byte
-//     swizzle), into a 3-stage ring.
-//   * Warp 4 (one thread) issues S = Q K^T (M128 N64 K64, fp32, two TMEM buffers so the
-//     next tile's scores are computed during this tile's softmax) and O += P V (M128 N64
-//     K64, TMEM columns 128..191, V read N-major) and commits them to mbarriers.
-//   * Two CTAs share an SM; query tiles with the longest causal span start first.
+//     swizzle), into a 4-stage ring; the block table is read in prefetched 32-entry windows.
+//   * Warp 4 (one thread) issues S = Q K^T (M128 N64 K64 into one of two fp32 S buffers,
+//     so the next tile's scores are computed during this tile's softmax) and O += P V
+//     (M128 N64 K64, V read N-major).  Both A operands come from TMEM: Q is copied there
+//     once by the row warps and P is written there per tile, so each MMA streams only its
+//     K or V tile from shared memory.
 //   * Warps 0-3 own one TMEM lane = one query row each: they read S, mask by absolute
-//     position, keep the running max / sum in registers (O in TMEM is rescaled only when
-//     the max grows by more than 2^8), write P as bf16 into a swizzled K-major smem tile,
-//     and finally normalise O and store bf16 rows.  P is double-buffered: the softmax of
-//     tile j+1 waits for the P V of tile j only when O must be rescaled.
+//     position (diagonal tiles only), keep the running max / sum in registers (O in TMEM is
+//     rescaled only when the max grows by more than 2^8), write P as packed bf16 into TMEM,
+//     and finally normalise O and store bf16 rows.
+// TMEM per CTA (256 columns): S buffers 0..63 and 64..127, O 128..191, Q 192..223,
+// P 224..255.
 // Every mbarrier wait is bounded; on timeout the CTA records PA_DEVFLAG_TIMEOUT, drains
 // its own copies and MMAs, frees its tensor memory and returns.
 #include <cudaTypedefs.h>
