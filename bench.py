@@ -42,6 +42,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--mixed", choices=["split", "unified"], default="split",
+                    help="steps with prefill chunks and decode rows: pa_prefill_chunk + "
+                         "pa_decode, or one pa_attention_varlen over all sequences")
     ap.add_argument("--append", choices=["fused", "separate"], default="fused",
                     help="decode-only steps: store the new tokens inside the decode launch "
                          "(pa_decode_append) or with pa_reshape_and_cache first")
@@ -191,7 +194,7 @@ class DeviceStep:
     """Resident state of one workload: per-layer pools (history already stored through the
     library), this step's inputs, outputs and workspaces."""
 
-    def __init__(self, w, dev, fused_append=False):
+    def __init__(self, w, dev, fused_append=False, mixed="split"):
         import torch
         from paged_kv_cache_299_gb300 import binding as pa
         self.pa = pa
@@ -213,6 +216,14 @@ class DeviceStep:
         self.pre_qsl = i32(w.prefill_query_start_loc)
         self.max_ctx_dec = int(w.decode_context_lens.max()) if w.num_decode else 0
         self.max_q_pre = int(w.new_lens[: w.num_prefill].max()) if w.num_prefill else 0
+        # unified: one varlen call serves the chunks (first) and the decode rows of a step
+        self.unified = bool(mixed == "unified" and w.num_prefill and w.num_decode
+                            and self.one_token_each is False)
+        n_pre_rows = int(w.prefill_query_start_loc[-1]) if w.num_prefill else 0
+        self.all_qsl = i32(np.concatenate([w.prefill_query_start_loc[: w.num_prefill + 1]
+                                           if w.num_prefill else [0],
+                                           n_pre_rows + np.arange(1, w.num_decode + 1)]))
+        self.n_rows = n_pre_rows + w.num_decode
         self.status = pa.new_device_status(dev)
         self.slots = torch.empty(self.n_new, dtype=torch.int64, device=dev)
         shape = (w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim)
@@ -230,17 +241,24 @@ class DeviceStep:
                 pa.pa_reshape_and_cache(vals["hist_k"], vals["hist_v"], hs, kc, vc,
                                         device_status=self.status)
                 del hs
+            # queries and outputs of all rows in one buffer (chunks first, then decode rows);
+            # the per-kind tensors are views into it
+            q_all = torch.cat([vals["q_prefill"], vals["q_decode"]]).contiguous()
+            out_all = torch.empty_like(q_all)
             self.layers.append({
                 "kc": kc, "vc": vc, "new_k": vals["new_k"], "new_v": vals["new_v"],
-                "q_dec": vals["q_decode"], "q_pre": vals["q_prefill"],
-                "out_dec": torch.empty_like(vals["q_decode"]),
-                "out_pre": torch.empty_like(vals["q_prefill"]),
+                "q_all": q_all, "out_all": out_all,
+                "q_pre": q_all[:n_pre_rows], "q_dec": q_all[n_pre_rows:],
+                "out_pre": out_all[:n_pre_rows], "out_dec": out_all[n_pre_rows:],
             })
             del vals
             torch.cuda.synchronize(dev)
         # the library merges split-KV pieces inside the decode kernel up to 8192-token
         # contexts with automatic partitions; otherwise a second (merge) kernel runs
         self.ws_merge_kernel = bool(w.partition_tokens > 0 or self.max_ctx_dec > 8192)
+        if self.unified:
+            self.ws_var = torch.empty(pa.pa_varlen_workspace_size(w.num_seqs, self.n_rows),
+                                      dtype=torch.uint8, device=dev)
         if w.num_decode:
             need = pa.pa_decode_workspace_size(w.num_decode, w.num_kv_heads, w.num_q_heads,
                                                self.max_ctx_dec, w.partition_tokens)
@@ -251,6 +269,8 @@ class DeviceStep:
         w = self.w
         if self.fused_append:
             return w.layers * (2 if self.ws_merge_kernel else 1)
+        if self.unified:  # store, plan, attention
+            return 1 + 3 * w.layers
         per_layer = 1 + ((2 if self.ws_merge_kernel else 1) if w.num_decode else 0) + \
             (1 if w.num_prefill else 0)
         return 1 + per_layer * w.layers
@@ -280,6 +300,15 @@ class DeviceStep:
                                    self.n_new, self.layers[0]["kc"], slot_mapping=self.slots)
         for li, L in enumerate(self.layers):
             pa.pa_reshape_and_cache(L["new_k"], L["new_v"], self.slots, L["kc"], L["vc"])
+            if self.unified:
+                if dec_events is not None:
+                    dec_events[li][0].record()
+                pa.pa_attention_varlen(L["out_all"], L["q_all"], self.all_qsl,
+                                       max(self.max_q_pre, 1), L["kc"], L["vc"], self.bt,
+                                       self.ctx, w.scale, workspace=self.ws_var)
+                if dec_events is not None:
+                    dec_events[li][1].record()
+                continue
             if w.num_prefill:
                 if pre_events is not None:
                     pre_events[li][0].record()
@@ -306,7 +335,7 @@ def run_gpu(args, rank, world):
     torch.cuda.set_device(dev)
     # weak scaling: every rank serves its own batch (seed offset per rank)
     w = workload(args.config, args.layers, 100 * rank if world > 1 else 0)
-    st = DeviceStep(w, dev, fused_append=args.append == "fused")
+    st = DeviceStep(w, dev, fused_append=args.append == "fused", mixed=args.mixed)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     kv_bytes = w.decode_kv_bytes()
     flush = kv_bytes < 4 * l2
@@ -327,7 +356,8 @@ def run_gpu(args, rank, world):
     step_ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
                for _ in range(K)]
     pre_ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-               for _ in range(w.layers)] for _ in range(K)] if w.num_prefill else None
+               for _ in range(w.layers)] for _ in range(K)] if w.num_prefill and not st.unified \
+        else None
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
@@ -392,14 +422,28 @@ def run_gpu(args, rank, world):
                                "eager pass right after)" if graph is not None
                                else "eager (one C-ABI call per kernel group)"),
                        store=("fused into decode (pa_decode_append)" if st.fused_append
-                              else "pa_compute_slot_mapping + pa_reshape_and_cache")),
+                              else "pa_compute_slot_mapping + pa_reshape_and_cache"),
+                       **({"attention": "pa_attention_varlen: one launch for chunks and "
+                                        "decode rows (plus its one-CTA plan kernel)"}
+                          if st.unified else {})),
         "tokens_per_s": round(w.num_decode * world / (step_ms * 1e-3), 1),
         "pct_of_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "gpu_launches": st.launches_per_step() * K,
         "wall_s_timed": round(wall, 3),
         "clocks": clocks,
     }
-    if dec_ms:
+    if dec_ms and st.unified:
+        # the varlen launch reads the K/V of every sequence of the step at least once
+        per_launch = float(np.sum(w.context_lens)) * w.num_kv_heads * w.head_dim * 2 * 2
+        achieved = per_launch / (dec_ms * 1e-3) / 1e9
+        res["roofline"] = {
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": None,
+            "kernel": "pa_attention_varlen: varlen_plan_kernel + paged_prefill_kernel "
+                      "(tcgen05) over the chunks and decode rows",
+            "peak_source": f"{peak_src} hbm_gbs", "launch_ms": round(dec_ms, 5),
+            "algorithmic_bytes_per_launch": int(per_launch)}
+    elif dec_ms:
         per_launch = kv_bytes / w.layers
         achieved = per_launch / (dec_ms * 1e-3) / 1e9
         res["roofline"] = {

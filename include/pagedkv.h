@@ -118,7 +118,9 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t 
  * where K_s[j] / V_s[j] is the token at logical position j found through block_tables.
  * The (sequence, K/V head, block) tiles are split evenly over the SMs (or into runs of
  * partition_tokens tokens); runs that end inside a sequence leave (running max, running
- * sum, unnormalised output) partials that a second kernel merges.
+ * sum, unnormalised output) partials.  With partition_tokens == 0 and max_context_len <=
+ * 8192 the warp that finishes the last piece of a sequence merges them inside the same
+ * kernel; otherwise a second kernel merges them.
  *   out              bf16 [num_seqs][num_q_heads][D] output
  *   q                bf16 [num_seqs][num_q_heads][D]
  *   block_tables     int32 [num_seqs][max_blocks_per_seq]
@@ -169,6 +171,35 @@ pa_status pa_prefill_chunk(void* out, const void* q, const int32_t* query_start_
                            const int32_t* context_lens, int32_t num_seqs,
                            int32_t num_q_heads, float scale, int32_t* device_status,
                            pa_stream_t stream);
+
+/* Bytes of device workspace pa_attention_varlen needs for a batch of num_seqs sequences
+ * carrying num_query_tokens query rows in total: 16 + 8 x (num_query_tokens / 32 +
+ * num_seqs + 1).  Returns 0 for negative arguments. */
+size_t pa_varlen_workspace_size(int32_t num_seqs, int32_t num_query_tokens);
+
+/* One continuous-batching step's attention in one attention launch ("vLLM", Continuous
+ * Batching: sequences in the prefill and in the decode phase share a step).  Arguments,
+ * semantics and results are exactly those of pa_prefill_chunk: a sequence with q_len = 1
+ * is a decode row, q_len > 1 a causal chunk, q_len = 0 contributes nothing, and the
+ * sequences may come in any order.  Instead of one CTA per (sequence, 32-row query tile,
+ * KV head) over a padded grid, a one-CTA plan kernel lists the (sequence, tile) items that
+ * exist, sorted by their number of 64-key tiles (heaviest first), and the tensor-core
+ * kernel runs over that list, so a batch of mostly short decode rows launches no empty
+ * CTAs and the longest spans start first.  Outputs are bit-identical to pa_prefill_chunk.
+ *   workspace        device buffer of at least pa_varlen_workspace_size(num_seqs,
+ *                    num_query_tokens) bytes, 16-byte aligned, caller-owned; no
+ *                    initialisation needed; the call overwrites it.
+ * Errors: those of pa_prefill_chunk; PA_ERR_WORKSPACE for a missing, misaligned or short
+ * workspace.  A query_start_loc whose rows run past num_query_tokens is flagged on the
+ * device (PA_DEVFLAG_BAD_CONTEXT) and those sequences are skipped. */
+pa_status pa_attention_varlen(void* out, const void* q, const int32_t* query_start_loc,
+                              int32_t num_query_tokens, int32_t max_query_len,
+                              const void* key_cache, const void* value_cache, pa_cache_desc cd,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* context_lens, int32_t num_seqs,
+                              int32_t num_q_heads, float scale, void* workspace,
+                              size_t workspace_bytes, int32_t* device_status,
+                              pa_stream_t stream);
 
 /* Paged decode attention that needs no workspace from the caller.  The paper has no
  * counterpart for this call.  It exists for callers that cannot allocate device memory

@@ -45,7 +45,8 @@ EXPORTED = ("pa_compute_slot_mapping", "pa_reshape_and_cache", "pa_decode_worksp
             "pa_last_error", "pa_decode_static_scratch", "pa_copy_blocks", "pa_bm_create",
             "pa_bm_destroy", "pa_bm_num_free_blocks", "pa_bm_ref_count", "pa_bm_add_sequence",
             "pa_bm_fork", "pa_bm_append_tokens", "pa_bm_free_sequence", "pa_bm_num_tokens",
-            "pa_bm_block_table", "pa_decode_append", "pa_selftest_wait_timeout")
+            "pa_bm_block_table", "pa_decode_append", "pa_selftest_wait_timeout",
+            "pa_varlen_workspace_size", "pa_attention_varlen")
 
 
 def library_path() -> str:
@@ -76,6 +77,11 @@ def load(path: str | None = None):
     lib.pa_prefill_chunk.argtypes = [P, P, P, i32, i32, P, P, CacheDesc, P, i32, P, i32, i32,
                                      f32, P, P]
     lib.pa_prefill_chunk.restype = st
+    lib.pa_varlen_workspace_size.argtypes = [i32, i32]
+    lib.pa_varlen_workspace_size.restype = sz
+    lib.pa_attention_varlen.argtypes = [P, P, P, i32, i32, P, P, CacheDesc, P, i32, P, i32,
+                                        i32, f32, P, sz, P, P]
+    lib.pa_attention_varlen.restype = st
     lib.pa_decode_static_scratch.argtypes = [P, P, P, P, CacheDesc, P, i32, P, i32, i32, f32,
                                              i32, i32, P, P]
     lib.pa_decode_static_scratch.restype = st
@@ -308,6 +314,40 @@ def pa_prefill_chunk(out, q, query_start_loc, max_query_len, key_cache, value_ca
                                  num_seqs, q.shape[1], float(scale), _ptr(device_status),
                                  _stream(stream))
     _check(st, "pa_prefill_chunk")
+    return out
+
+
+def pa_varlen_workspace_size(num_seqs, num_query_tokens) -> int:
+    return int(load().pa_varlen_workspace_size(num_seqs, num_query_tokens))
+
+
+def pa_attention_varlen(out, q, query_start_loc, max_query_len, key_cache, value_cache,
+                        block_tables, context_lens, scale, workspace=None, device_status=None,
+                        stream=None):
+    """One continuous-batching step's attention (decode rows and causal chunks mixed) in one
+    attention launch over a work-sorted item list; same results as pa_prefill_chunk."""
+    _need(out, "out", torch.bfloat16, 3)
+    _need(q, "q", torch.bfloat16, 3)
+    _need(query_start_loc, "query_start_loc", torch.int32, 1)
+    _need(key_cache, "key_cache", torch.bfloat16, 4)
+    _need(value_cache, "value_cache", torch.bfloat16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    num_seqs = context_lens.shape[0]
+    if out.shape != q.shape or query_start_loc.shape[0] != num_seqs + 1 or \
+            block_tables.shape[0] != num_seqs:
+        raise ValueError("varlen argument shapes disagree")
+    if workspace is None:
+        workspace = torch.empty(max(16, pa_varlen_workspace_size(num_seqs, q.shape[0])),
+                                dtype=torch.uint8, device=q.device)
+    st = load().pa_attention_varlen(_ptr(out), _ptr(q), _ptr(query_start_loc), q.shape[0],
+                                    int(max_query_len), _ptr(key_cache), _ptr(value_cache),
+                                    cache_desc(key_cache), _ptr(block_tables),
+                                    block_tables.shape[1], _ptr(context_lens), num_seqs,
+                                    q.shape[1], float(scale), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(),
+                                    _ptr(device_status), _stream(stream))
+    _check(st, "pa_attention_varlen")
     return out
 
 

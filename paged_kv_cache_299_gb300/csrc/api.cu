@@ -209,21 +209,27 @@ pa_status pa_decode_append(void* out, const void* q, const void* key, const void
                      device_status, stream);
 }
 
-pa_status pa_prefill_chunk(void* out, const void* q, const int32_t* query_start_loc,
-                           int32_t num_query_tokens, int32_t max_query_len,
-                           const void* key_cache,
-                           const void* value_cache, pa_cache_desc cd,
-                           const int32_t* block_tables, int32_t max_blocks_per_seq,
-                           const int32_t* context_lens, int32_t num_seqs,
-                           int32_t num_q_heads, float scale, int32_t* device_status,
-                           pa_stream_t stream) {
+namespace {
+
+// Validation and argument packing shared by pa_prefill_chunk and pa_attention_varlen;
+// returns PA_OK with *skip set when there is nothing to do.
+pa_status chunk_args(void* out, const void* q, const int32_t* query_start_loc,
+                     int32_t num_query_tokens, int32_t max_query_len, const void* key_cache,
+                     const void* value_cache, pa_cache_desc cd, const int32_t* block_tables,
+                     int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                     int32_t num_q_heads, float scale, int32_t* device_status,
+                     pkv::PrefillArgs* a, bool* skip) {
+  *skip = false;
   pa_status st = check_desc(cd);
   if (st != PA_OK) return st;
   if (num_seqs < 0 || max_query_len < 0 || num_query_tokens < 0 || max_blocks_per_seq <= 0)
     return fail(PA_ERR_INVALID_ARG,
                 "num_seqs %d, num_query_tokens %d, max_query_len %d, max_blocks_per_seq %d",
                 num_seqs, num_query_tokens, max_query_len, max_blocks_per_seq);
-  if (num_seqs == 0 || max_query_len == 0 || num_query_tokens == 0) return ok();
+  if (num_seqs == 0 || max_query_len == 0 || num_query_tokens == 0) {
+    *skip = true;
+    return PA_OK;
+  }
   if (max_query_len > num_query_tokens)
     return fail(PA_ERR_INVALID_ARG, "max_query_len %d > num_query_tokens %d", max_query_len,
                 num_query_tokens);
@@ -236,25 +242,70 @@ pa_status pa_prefill_chunk(void* out, const void* q, const int32_t* query_start_
   if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
     return fail(PA_ERR_INVALID_ARG, "out/q/cache pointers must be 16-byte aligned");
   if (!(scale > 0.f) || !isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale %g", scale);
+  a->out = out;
+  a->q = q;
+  a->query_start_loc = query_start_loc;
+  a->num_query_tokens = num_query_tokens;
+  a->max_query_len = max_query_len;
+  a->key_cache = key_cache;
+  a->value_cache = value_cache;
+  a->num_blocks = cd.num_blocks;
+  a->num_kv_heads = cd.num_kv_heads;
+  a->block_tables = block_tables;
+  a->max_blocks_per_seq = max_blocks_per_seq;
+  a->context_lens = context_lens;
+  a->num_seqs = num_seqs;
+  a->num_q_heads = num_q_heads;
+  a->scale = scale;
+  a->status = device_status;
+  return PA_OK;
+}
+
+}  // namespace
+
+pa_status pa_prefill_chunk(void* out, const void* q, const int32_t* query_start_loc,
+                           int32_t num_query_tokens, int32_t max_query_len,
+                           const void* key_cache,
+                           const void* value_cache, pa_cache_desc cd,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* context_lens, int32_t num_seqs,
+                           int32_t num_q_heads, float scale, int32_t* device_status,
+                           pa_stream_t stream) {
   pkv::PrefillArgs a;
-  a.out = out;
-  a.q = q;
-  a.query_start_loc = query_start_loc;
-  a.num_query_tokens = num_query_tokens;
-  a.max_query_len = max_query_len;
-  a.key_cache = key_cache;
-  a.value_cache = value_cache;
-  a.num_blocks = cd.num_blocks;
-  a.num_kv_heads = cd.num_kv_heads;
-  a.block_tables = block_tables;
-  a.max_blocks_per_seq = max_blocks_per_seq;
-  a.context_lens = context_lens;
-  a.num_seqs = num_seqs;
-  a.num_q_heads = num_q_heads;
-  a.scale = scale;
-  a.status = device_status;
+  bool skip;
+  pa_status st = chunk_args(out, q, query_start_loc, num_query_tokens, max_query_len, key_cache,
+                            value_cache, cd, block_tables, max_blocks_per_seq, context_lens,
+                            num_seqs, num_q_heads, scale, device_status, &a, &skip);
+  if (st != PA_OK || skip) return st == PA_OK ? ok() : st;
   return from_cuda(pkv::launch_prefill(a, reinterpret_cast<cudaStream_t>(stream)),
                    "prefill launch");
+}
+
+size_t pa_varlen_workspace_size(int32_t num_seqs, int32_t num_query_tokens) {
+  if (num_seqs < 0 || num_query_tokens < 0) return 0;
+  return pkv::varlen_workspace_size(num_seqs, num_query_tokens);
+}
+
+pa_status pa_attention_varlen(void* out, const void* q, const int32_t* query_start_loc,
+                              int32_t num_query_tokens, int32_t max_query_len,
+                              const void* key_cache, const void* value_cache, pa_cache_desc cd,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* context_lens, int32_t num_seqs,
+                              int32_t num_q_heads, float scale, void* workspace,
+                              size_t workspace_bytes, int32_t* device_status,
+                              pa_stream_t stream) {
+  pkv::PrefillArgs a;
+  bool skip;
+  pa_status st = chunk_args(out, q, query_start_loc, num_query_tokens, max_query_len, key_cache,
+                            value_cache, cd, block_tables, max_blocks_per_seq, context_lens,
+                            num_seqs, num_q_heads, scale, device_status, &a, &skip);
+  if (st != PA_OK || skip) return st == PA_OK ? ok() : st;
+  const size_t need = pkv::varlen_workspace_size(num_seqs, num_query_tokens);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < need)
+    return fail(PA_ERR_WORKSPACE, "varlen workspace %zu bytes at %p, need %zu (16-byte aligned)",
+                workspace_bytes, workspace, need);
+  return from_cuda(pkv::launch_varlen(a, workspace, reinterpret_cast<cudaStream_t>(stream)),
+                   "varlen launch");
 }
 
 pa_status pa_copy_blocks(void* key_cache, void* value_cache, pa_cache_desc cd,

@@ -85,4 +85,9 @@ struct PrefillArgs {
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 
+// Unified varlen launch: a work-list plan kernel (items sorted by work) and the chunk
+// kernel over that list.  The workspace holds the item count and the items.
+size_t varlen_workspace_size(int32_t num_seqs, int32_t num_query_tokens);
+cudaError_t launch_varlen(const PrefillArgs& a, void* workspace, cudaStream_t stream);
+
 }  // namespace pkv

@@ -72,6 +72,11 @@ struct PParams {
   int32_t num_q_heads;
   float qk_scale;  // scale * log2(e)
   int32_t* status;
+  int32_t num_query_tokens;
+  // Work-list mode (unified varlen launch): CTA b serves item b / num_kv_heads, KV head
+  // b % num_kv_heads; items are (sequence, query tile) pairs, heaviest first.
+  const int32_t* items;
+  const int32_t* item_count;
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
@@ -87,11 +92,20 @@ __global__ void __launch_bounds__(kThreads, 2)
 paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
                      const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const PParams p) {
-  // The query-tile index is the slowest grid dimension, reversed: the tiles with the
-  // longest causal spans of every sequence and head are dispatched first.
-  const int tile = gridDim.z - 1 - blockIdx.z;
-  const int g = blockIdx.y;
-  const int s = blockIdx.x;
+  int tile, g, s;
+  if (p.items != nullptr) {
+    const int item = static_cast<int>(blockIdx.x) / p.num_kv_heads;
+    if (item >= *p.item_count) return;
+    s = p.items[2 * item];
+    tile = p.items[2 * item + 1];
+    g = static_cast<int>(blockIdx.x) % p.num_kv_heads;
+  } else {
+    // The query-tile index is the slowest grid dimension, reversed: the tiles with the
+    // longest causal spans of every sequence and head are dispatched first.
+    tile = gridDim.z - 1 - blockIdx.z;
+    g = blockIdx.y;
+    s = blockIdx.x;
+  }
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -100,6 +114,10 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
   const int q_len = p.query_start_loc[s + 1] - q0;
   const int tok0 = tile * kTokensPerTile;
   if (tok0 >= q_len) return;
+  if (q0 < 0 || q0 + q_len > p.num_query_tokens) {  // rows outside q / out
+    if (tid == 0) flag_error(p.status, PA_DEVFLAG_BAD_CONTEXT);
+    return;
+  }
   const int L = p.context_lens[s];
   if (L < q_len || static_cast<int64_t>(L) > static_cast<int64_t>(p.max_blocks_per_seq) * kBlockSize) {
     if (tid == 0) flag_error(p.status, PA_DEVFLAG_BAD_CONTEXT);
@@ -470,7 +488,11 @@ bool encode_q(CUtensorMap* map, const void* base, uint64_t tokens, uint64_t head
 
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
+namespace {
+
+// Shared set-up of both launch forms: kernel attributes, tensor maps, parameters.
+cudaError_t prepare(const PrefillArgs& a, CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv,
+                    PParams* p) {
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(paged_prefill_kernel,
@@ -483,26 +505,164 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   }
   const uint64_t pool_rows = static_cast<uint64_t>(a.num_blocks) * a.num_kv_heads * kBlockSize;
   if (pool_rows >= (1ull << 31)) return cudaErrorInvalidValue;
-  CUtensorMap tq, tk, tv;
-  if (!encode_q(&tq, a.q, static_cast<uint64_t>(a.num_query_tokens), a.num_q_heads) ||
-      !encode_rows(&tk, a.key_cache, pool_rows, kBlockSize) ||
-      !encode_rows(&tv, a.value_cache, pool_rows, kBlockSize))
+  if (!encode_q(tq, a.q, static_cast<uint64_t>(a.num_query_tokens), a.num_q_heads) ||
+      !encode_rows(tk, a.key_cache, pool_rows, kBlockSize) ||
+      !encode_rows(tv, a.value_cache, pool_rows, kBlockSize))
     return cudaErrorInvalidValue;
+  p->out = static_cast<__nv_bfloat16*>(a.out);
+  p->query_start_loc = a.query_start_loc;
+  p->block_tables = a.block_tables;
+  p->max_blocks_per_seq = a.max_blocks_per_seq;
+  p->context_lens = a.context_lens;
+  p->num_blocks = a.num_blocks;
+  p->num_kv_heads = a.num_kv_heads;
+  p->num_q_heads = a.num_q_heads;
+  p->qk_scale = a.scale * 1.4426950408889634f;
+  p->status = a.status;
+  p->num_query_tokens = a.num_query_tokens;
+  p->items = nullptr;
+  p->item_count = nullptr;
+  return cudaSuccess;
+}
+
+// ---- work list of the unified varlen launch ---------------------------------------------
+// Items are (sequence, 32-token query tile) pairs; an item's work is its number of 64-key
+// tiles.  One CTA counting-sorts them by work, heaviest first, so the long causal spans
+// and long decode contexts start before the short ones and the launch ends without a long
+// tail.  Items of one work value keep no particular order (outputs do not depend on it).
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanBuckets = 4096;  // work values >= 4095 tiles share the last bucket
+
+__device__ __forceinline__ int plan_bucket(int L, int q_len, int t) {
+  const int ntok = min(kTokensPerTile, q_len - t * kTokensPerTile);
+  const int keys = max(1, L - q_len + t * kTokensPerTile + ntok);
+  return min((keys + kTileN - 1) / kTileN, kPlanBuckets - 1);
+}
+
+__global__ void __launch_bounds__(kPlanThreads)
+varlen_plan_kernel(const int32_t* query_start_loc, const int32_t* context_lens, int num_seqs,
+                   int num_query_tokens, int max_items, int32_t* items, int32_t* item_count,
+                   int32_t* status) {
+  __shared__ int hist[kPlanBuckets];  // counts, then (after the scan) next free position
+  __shared__ int warp_total[kPlanThreads / 32];
+  __shared__ int grand_total;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  constexpr int kWarps = kPlanThreads / 32;
+  for (int b = tid; b < kPlanBuckets; b += kPlanThreads) hist[b] = 0;
+  __syncthreads();
+  // histogram of item work; a sequence's tiles are spread over the lanes of one warp
+  for (int s = warp; s < num_seqs; s += kWarps) {
+    const int q0 = query_start_loc[s];
+    const int q_len = query_start_loc[s + 1] - q0;
+    if (q_len == 0) continue;
+    if (q_len < 0 || q0 < 0 || q0 + q_len > num_query_tokens) {  // rows outside q / out
+      if (lane == 0) flag_error(status, PA_DEVFLAG_BAD_CONTEXT);
+      continue;
+    }
+    const int L = context_lens[s];
+    const int tiles = (q_len + kTokensPerTile - 1) / kTokensPerTile;
+    for (int t = lane; t < tiles; t += 32) atomicAdd(&hist[plan_bucket(L, q_len, t)], 1);
+  }
+  __syncthreads();
+  // exclusive scan from the heaviest bucket down: thread i owns buckets 4095-4i .. 4092-4i
+  constexpr int kPer = kPlanBuckets / kPlanThreads;
+  int local[kPer];
+  int sum = 0;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    local[k] = hist[kPlanBuckets - 1 - (kPer * tid + k)];
+    sum += local[k];
+  }
+  int incl = sum;  // inclusive scan within the warp
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) warp_total[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_total[lane];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, w, d);
+      if (lane >= d) w += v;
+    }
+    warp_total[lane] = w;  // inclusive over warps
+    if (lane == 31) grand_total = w;
+  }
+  __syncthreads();
+  int start = (warp > 0 ? warp_total[warp - 1] : 0) + incl - sum;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    hist[kPlanBuckets - 1 - (kPer * tid + k)] = start;
+    start += local[k];
+  }
+  __syncthreads();
+  for (int s = warp; s < num_seqs; s += kWarps) {
+    const int q0 = query_start_loc[s];
+    const int q_len = query_start_loc[s + 1] - q0;
+    if (q_len <= 0 || q0 < 0 || q0 + q_len > num_query_tokens) continue;
+    const int L = context_lens[s];
+    const int tiles = (q_len + kTokensPerTile - 1) / kTokensPerTile;
+    for (int t = lane; t < tiles; t += 32) {
+      const int pos = atomicAdd(&hist[plan_bucket(L, q_len, t)], 1);
+      if (pos < max_items) {
+        items[2 * pos] = s;
+        items[2 * pos + 1] = t;
+      }
+    }
+  }
+  if (tid == 0) {
+    *item_count = min(grand_total, max_items);
+    if (grand_total > max_items) flag_error(status, PA_DEVFLAG_BAD_CONTEXT);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
+  CUtensorMap tq, tk, tv;
   PParams p;
-  p.out = static_cast<__nv_bfloat16*>(a.out);
-  p.query_start_loc = a.query_start_loc;
-  p.block_tables = a.block_tables;
-  p.max_blocks_per_seq = a.max_blocks_per_seq;
-  p.context_lens = a.context_lens;
-  p.num_blocks = a.num_blocks;
-  p.num_kv_heads = a.num_kv_heads;
-  p.num_q_heads = a.num_q_heads;
-  p.qk_scale = a.scale * 1.4426950408889634f;
-  p.status = a.status;
+  cudaError_t e = prepare(a, &tq, &tk, &tv, &p);
+  if (e != cudaSuccess) return e;
   const int tiles = (a.max_query_len + kTokensPerTile - 1) / kTokensPerTile;
   if (tiles > 65535 || a.num_kv_heads > 65535) return cudaErrorInvalidValue;
   dim3 grid(a.num_seqs, a.num_kv_heads, tiles);
   paged_prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+int64_t varlen_max_items(int32_t num_seqs, int32_t num_query_tokens) {
+  return static_cast<int64_t>(num_query_tokens) / kTokensPerTile + num_seqs + 1;
+}
+
+size_t varlen_workspace_size(int32_t num_seqs, int32_t num_query_tokens) {
+  return 16 + 8 * static_cast<size_t>(varlen_max_items(num_seqs, num_query_tokens));
+}
+
+cudaError_t launch_varlen(const PrefillArgs& a, void* workspace, cudaStream_t stream) {
+  CUtensorMap tq, tk, tv;
+  PParams p;
+  cudaError_t e = prepare(a, &tq, &tk, &tv, &p);
+  if (e != cudaSuccess) return e;
+  const int64_t max_items = varlen_max_items(a.num_seqs, a.num_query_tokens);
+  const int64_t blocks = max_items * a.num_kv_heads;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  int32_t* count = static_cast<int32_t*>(workspace);
+  int32_t* items = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + 16);
+  varlen_plan_kernel<<<1, kPlanThreads, 0, stream>>>(a.query_start_loc, a.context_lens,
+                                                     a.num_seqs, a.num_query_tokens,
+                                                     static_cast<int>(max_items), items, count,
+                                                     a.status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  p.items = items;
+  p.item_count = count;
+  paged_prefill_kernel<<<static_cast<unsigned>(blocks), kThreads, kSmemBytes, stream>>>(tq, tk,
+                                                                                        tv, p);
   return cudaGetLastError();
 }
 
