@@ -124,6 +124,10 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
     return;
   }
   const int ntok = min(kTokensPerTile, q_len - tok0);
+  // Row warp w holds tokens tok0 + 8w .. +7; a warp with none of them inside the chunk
+  // (every warp but the first for a decode row) skips the softmax entirely: the rows it
+  // would produce are discarded, and MMA rows are independent.
+  const int live_warps = min(4, (ntok + kTokensPerTile / 4 - 1) / (kTokensPerTile / 4));
   const int keys = L - q_len + tok0 + ntok;  // this tile needs keys 0 .. keys-1
   const int n_kv = (keys + kTileN - 1) / kTileN;
   const int blocks_needed = (keys + kBlockSize - 1) / kBlockSize;
@@ -156,10 +160,10 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
     }
     mbar_init(&s_ready[0], 1);
     mbar_init(&s_ready[1], 1);
-    mbar_init(p_ready, kTileM);
+    mbar_init(p_ready, 32 * live_warps);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
-    mbar_init(q_tmem, kTileM);
+    mbar_init(q_tmem, 32 * live_warps);
     fence_barrier_init();
     abort_flag = 0;
   }
@@ -285,7 +289,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
       umma_commit(drain);
       if (!mbar_wait(drain, 0)) flag_error(p.status, PA_DEVFLAG_TIMEOUT);
     }
-  } else {
+  } else if (warp < live_warps) {
     // ============================ softmax / epilogue (warps 0-3) ============================
     const int r = tid;  // MMA row == TMEM lane
     const int tt = r >> 2;
@@ -367,12 +371,16 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
         const __nv_bfloat162 b2 = __floats2bfloat162_rn(e.x, e.y);
         v[0][i] = *reinterpret_cast<const uint32_t*>(&b2);
       }
-      if (j == n_kv - 1 && r < kTileN && kb + r >= keys) {
+      if (j == n_kv - 1 && kb + kTileN > keys) {
         // V rows past the last needed key are never weighted, but may hold NaN (unused
-        // slots) or stale data: zero them so 0 * V stays 0 in the tensor core.
-        uint4* vrow = reinterpret_cast<uint4*>(sv + (j % kStages) * kKVBytes + r * kRowBytes);
+        // slots) or stale data: zero them so 0 * V stays 0 in the tensor core.  The live
+        // row warps share the 64 rows.
+        for (int zr = r; zr < kTileN; zr += 32 * live_warps) {
+          if (kb + zr < keys) continue;
+          uint4* vrow = reinterpret_cast<uint4*>(sv + (j % kStages) * kKVBytes + zr * kRowBytes);
 #pragma unroll
-        for (int i = 0; i < kRowBytes / 16; ++i) vrow[i] = make_uint4(0, 0, 0, 0);
+          for (int i = 0; i < kRowBytes / 16; ++i) vrow[i] = make_uint4(0, 0, 0, 0);
+        }
         fence_proxy_async_smem();
       }
       if (j > 0) {
