@@ -598,9 +598,10 @@ paged_decode_kernel(const KParams p) {
       } else {
         attend_tile<GROUP, true>(kt, vt, lane, tg, dq, valid, qf, m, l, o);
       }
+      // Every lane's reads of this stage have completed (their values fed the arithmetic
+      // above); the warp barrier orders them before lane 0 issues the refill into the same
+      // buffer, as a consumer's release orders its reads before a producer's next copy.
       __syncwarp();
-      // every lane's reads of this stage are done: order them before the refill's async write
-      if (lane == 0) fence_proxy_async_smem();
       issue_one();
     }
 
