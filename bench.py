@@ -190,9 +190,23 @@ class ClockSampler:
 # ----------------------------------------------------------------------------------------
 # the GB300 arm
 # ----------------------------------------------------------------------------------------
+def carve(torch, dev, specs):
+    """Tensors (name, shape, dtype) carved out of one device buffer at 256-byte offsets, so
+    that a step's inputs, or its outputs, cross the host link in a single copy."""
+    views, offs, total = {}, [], 0
+    for name, shape, dt in specs:
+        nbytes = int(np.prod(shape)) * torch.empty((), dtype=dt).element_size()
+        offs.append((name, shape, dt, total, nbytes))
+        total += (nbytes + 255) // 256 * 256
+    buf = torch.empty(max(total, 256), dtype=torch.uint8, device=dev)
+    for name, shape, dt, o, n in offs:
+        views[name] = buf[o:o + n].view(dt).view(shape)
+    return buf, views
+
+
 class DeviceStep:
     """Resident state of one workload: per-layer pools (history already stored through the
-    library), this step's inputs, outputs and workspaces."""
+    library), workspaces, and one or more sets of this step's input and output buffers."""
 
     def __init__(self, w, dev, fused_append=False, mixed="split"):
         import torch
@@ -202,32 +216,42 @@ class DeviceStep:
         self.w = w
         self.dev = dev
         i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
-        self.bt = i32(w.block_tables)
-        self.ctx = i32(w.context_lens)
+        self.n_pre_rows = int(w.prefill_query_start_loc[-1]) if w.num_prefill else 0
+        self.n_rows = self.n_pre_rows + w.num_decode
+        self.n_new = int(w.new_lens.sum())
+        # every per-step input (queries, new K/V of each layer, block tables, context
+        # lengths) lives in one device buffer, every output in another
+        bf = torch.bfloat16
+        self.in_specs = []
+        for layer in range(w.layers):
+            self.in_specs += [(f"q{layer}", (self.n_rows, w.num_q_heads, w.head_dim), bf),
+                              (f"k{layer}", (self.n_new, w.num_kv_heads, w.head_dim), bf),
+                              (f"v{layer}", (self.n_new, w.num_kv_heads, w.head_dim), bf)]
+        self.in_specs += [("bt", tuple(w.block_tables.shape), torch.int32),
+                          ("ctx", (w.num_seqs,), torch.int32)]
+        self.out_specs = [(f"o{layer}", (self.n_rows, w.num_q_heads, w.head_dim), bf)
+                          for layer in range(w.layers)]
+        self.sets = [self._carve_set()]
+        S = self.sets[0]
+        S["bt"].copy_(i32(w.block_tables))
+        S["ctx"].copy_(i32(w.context_lens))
         self.new_qsl = i32(w.new_start_loc)
         self.one_token_each = bool((w.new_lens == 1).all())
         # one new token per decode sequence and no prefill: the store can ride in the decode
         self.fused_append = bool(fused_append and self.one_token_each and w.num_prefill == 0)
-        self.n_new = int(w.new_lens.sum())
-        self.bt_dec = self.bt[w.num_prefill:].contiguous()
-        self.ctx_dec = self.ctx[w.num_prefill:].contiguous()
-        self.bt_pre = self.bt[: w.num_prefill].contiguous()
-        self.ctx_pre = self.ctx[: w.num_prefill].contiguous()
         self.pre_qsl = i32(w.prefill_query_start_loc)
         self.max_ctx_dec = int(w.decode_context_lens.max()) if w.num_decode else 0
         self.max_q_pre = int(w.new_lens[: w.num_prefill].max()) if w.num_prefill else 0
         # unified: one varlen call serves the chunks (first) and the decode rows of a step
         self.unified = bool(mixed == "unified" and w.num_prefill and w.num_decode
                             and self.one_token_each is False)
-        n_pre_rows = int(w.prefill_query_start_loc[-1]) if w.num_prefill else 0
         self.all_qsl = i32(np.concatenate([w.prefill_query_start_loc[: w.num_prefill + 1]
                                            if w.num_prefill else [0],
-                                           n_pre_rows + np.arange(1, w.num_decode + 1)]))
-        self.n_rows = n_pre_rows + w.num_decode
+                                           self.n_pre_rows + np.arange(1, w.num_decode + 1)]))
         self.status = pa.new_device_status(dev)
         self.slots = torch.empty(self.n_new, dtype=torch.int64, device=dev)
         shape = (w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim)
-        self.layers = []
+        self.pools = []
         hist_ctx = i32(w.hist_lens)
         hist_qsl = i32(w.hist_start_loc)
         n_hist = int(w.hist_lens.sum())
@@ -236,21 +260,16 @@ class DeviceStep:
             kc = torch.full(shape, float("nan"), dtype=torch.bfloat16, device=dev)
             vc = torch.full(shape, float("nan"), dtype=torch.bfloat16, device=dev)
             if n_hist:
-                hs = pa.pa_compute_slot_mapping(self.bt, hist_ctx, hist_qsl, n_hist, kc,
+                hs = pa.pa_compute_slot_mapping(S["bt"], hist_ctx, hist_qsl, n_hist, kc,
                                                 device_status=self.status)
                 pa.pa_reshape_and_cache(vals["hist_k"], vals["hist_v"], hs, kc, vc,
                                         device_status=self.status)
                 del hs
-            # queries and outputs of all rows in one buffer (chunks first, then decode rows);
-            # the per-kind tensors are views into it
-            q_all = torch.cat([vals["q_prefill"], vals["q_decode"]]).contiguous()
-            out_all = torch.empty_like(q_all)
-            self.layers.append({
-                "kc": kc, "vc": vc, "new_k": vals["new_k"], "new_v": vals["new_v"],
-                "q_all": q_all, "out_all": out_all,
-                "q_pre": q_all[:n_pre_rows], "q_dec": q_all[n_pre_rows:],
-                "out_pre": out_all[:n_pre_rows], "out_dec": out_all[n_pre_rows:],
-            })
+            self.pools.append((kc, vc))
+            L = S["layers"][layer]
+            L["q_all"].copy_(torch.cat([vals["q_prefill"], vals["q_decode"]]))
+            L["new_k"].copy_(vals["new_k"])
+            L["new_v"].copy_(vals["new_v"])
             del vals
             torch.cuda.synchronize(dev)
         # the library merges split-KV pieces inside the decode kernel up to 8192-token
@@ -264,6 +283,33 @@ class DeviceStep:
                                                self.max_ctx_dec, w.partition_tokens)
             self.ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
         assert pa.pa_check_device_status(self.status) == pa.PA_OK
+
+    def _carve_set(self) -> dict:
+        """One set of step buffers: queries / new K/V / tables in one device buffer, outputs
+        in another; queries and outputs of all rows per layer, chunks first, the per-kind
+        tensors being views."""
+        torch, dev, w, npre = self.torch, self.dev, self.w, self.n_pre_rows
+        inbuf, inv = carve(torch, dev, self.in_specs)
+        outbuf, outv = carve(torch, dev, self.out_specs)
+        S = {"inbuf": inbuf, "outbuf": outbuf, "bt": inv["bt"], "ctx": inv["ctx"], "layers": []}
+        S["bt_dec"], S["ctx_dec"] = S["bt"][w.num_prefill:], S["ctx"][w.num_prefill:]
+        S["bt_pre"], S["ctx_pre"] = S["bt"][: w.num_prefill], S["ctx"][: w.num_prefill]
+        for layer in range(w.layers):
+            q_all, out_all = inv[f"q{layer}"], outv[f"o{layer}"]
+            S["layers"].append({
+                "new_k": inv[f"k{layer}"], "new_v": inv[f"v{layer}"],
+                "q_all": q_all, "out_all": out_all,
+                "q_pre": q_all[:npre], "q_dec": q_all[npre:],
+                "out_pre": out_all[:npre], "out_dec": out_all[npre:],
+            })
+        return S
+
+    def add_buffer_set(self) -> int:
+        """A second set of step buffers holding the same inputs (for overlapped copies)."""
+        S = self._carve_set()
+        S["inbuf"].copy_(self.sets[0]["inbuf"])
+        self.sets.append(S)
+        return len(self.sets) - 1
 
     def launches_per_step(self) -> int:
         w = self.w
@@ -284,28 +330,32 @@ class DeviceStep:
         keys = (n * h + n * (n + 1) / 2).sum()
         return float(keys * w.num_q_heads * 4 * w.head_dim * w.layers)
 
-    def step(self, dec_events=None, pre_events=None):
+    def step(self, dec_events=None, pre_events=None, set_idx=0):
         pa, w = self.pa, self.w
+        S = self.sets[set_idx]
         if self.fused_append:
-            for li, L in enumerate(self.layers):
+            for li, L in enumerate(S["layers"]):
+                kc, vc = self.pools[li]
                 if dec_events is not None:
                     dec_events[li][0].record()
-                pa.pa_decode_append(L["out_dec"], L["q_dec"], L["new_k"], L["new_v"], L["kc"],
-                                    L["vc"], self.bt_dec, self.ctx_dec, w.scale,
-                                    self.max_ctx_dec, w.partition_tokens, workspace=self.ws)
+                pa.pa_decode_append(L["out_dec"], L["q_dec"], L["new_k"], L["new_v"], kc, vc,
+                                    S["bt_dec"], S["ctx_dec"], w.scale, self.max_ctx_dec,
+                                    w.partition_tokens, workspace=self.ws)
                 if dec_events is not None:
                     dec_events[li][1].record()
             return
-        pa.pa_compute_slot_mapping(self.bt, self.ctx, None if self.one_token_each else self.new_qsl,
-                                   self.n_new, self.layers[0]["kc"], slot_mapping=self.slots)
-        for li, L in enumerate(self.layers):
-            pa.pa_reshape_and_cache(L["new_k"], L["new_v"], self.slots, L["kc"], L["vc"])
+        pa.pa_compute_slot_mapping(S["bt"], S["ctx"],
+                                   None if self.one_token_each else self.new_qsl, self.n_new,
+                                   self.pools[0][0], slot_mapping=self.slots)
+        for li, L in enumerate(S["layers"]):
+            kc, vc = self.pools[li]
+            pa.pa_reshape_and_cache(L["new_k"], L["new_v"], self.slots, kc, vc)
             if self.unified:
                 if dec_events is not None:
                     dec_events[li][0].record()
                 pa.pa_attention_varlen(L["out_all"], L["q_all"], self.all_qsl,
-                                       max(self.max_q_pre, 1), L["kc"], L["vc"], self.bt,
-                                       self.ctx, w.scale, workspace=self.ws_var)
+                                       max(self.max_q_pre, 1), kc, vc, S["bt"], S["ctx"],
+                                       w.scale, workspace=self.ws_var)
                 if dec_events is not None:
                     dec_events[li][1].record()
                 continue
@@ -313,15 +363,14 @@ class DeviceStep:
                 if pre_events is not None:
                     pre_events[li][0].record()
                 pa.pa_prefill_chunk(L["out_pre"], L["q_pre"], self.pre_qsl, self.max_q_pre,
-                                    L["kc"], L["vc"], self.bt_pre, self.ctx_pre, w.scale)
+                                    kc, vc, S["bt_pre"], S["ctx_pre"], w.scale)
                 if pre_events is not None:
                     pre_events[li][1].record()
             if w.num_decode:
                 if dec_events is not None:
                     dec_events[li][0].record()
-                pa.pa_decode(L["out_dec"], L["q_dec"], L["kc"], L["vc"], self.bt_dec,
-                             self.ctx_dec, w.scale, self.max_ctx_dec, w.partition_tokens,
-                             workspace=self.ws)
+                pa.pa_decode(L["out_dec"], L["q_dec"], kc, vc, S["bt_dec"], S["ctx_dec"],
+                             w.scale, self.max_ctx_dec, w.partition_tokens, workspace=self.ws)
                 if dec_events is not None:
                     dec_events[li][1].record()
 
@@ -472,45 +521,65 @@ def run_gpu(args, rank, world):
 
 def run_e2e(st: DeviceStep, steps: int, dev, graph=None) -> dict:
     """Each step: pinned host -> device copy of the step's inputs (queries, new K/V, block
-    tables, context lengths), the step through the C ABI, device -> host copy of the
-    attention outputs.  Timed on the device with events around the whole loop."""
+    tables, context lengths of every layer: one buffer), the step through the C ABI, and
+    a device -> host copy of its attention outputs (one buffer).  As a serving loop would,
+    two buffer sets alternate so that the copies of one step overlap the attention of its
+    neighbour: inputs of step k+1 go up and outputs of step k-1 come down on two copy
+    streams while step k computes.  Timed on the device from the first upload to the last
+    download."""
     import torch
-    w = st.w
+    n_sets = 2
+    while len(st.sets) < n_sets:
+        st.add_buffer_set()
+    graphs = [graph] + [None] * (n_sets - 1)
+    if graph is not None:
+        from paged_kv_cache_299_gb300 import graphs as gmod
+        for i in range(1, n_sets):
+            graphs[i] = gmod.StepGraph(lambda i=i: st.step(set_idx=i))
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
-    host_in, host_out = [], []
-    for L in st.layers:
-        for key in ("q_dec", "q_pre", "new_k", "new_v"):
-            if L[key].numel():
-                host_in.append((pin(L[key]), L[key]))
-        for key in ("out_dec", "out_pre"):
-            if L[key].numel():
-                host_out.append((torch.empty(L[key].shape, dtype=L[key].dtype, pin_memory=True),
-                                 L[key]))
-    for t in (st.bt, st.ctx):
-        host_in.append((pin(t), t))
-    h2d = sum(h.numel() * h.element_size() for h, _ in host_in)
-    d2h = sum(h.numel() * h.element_size() for h, _ in host_out)
+    host_in = [pin(S["inbuf"]) for S in st.sets[:n_sets]]
+    host_out = [torch.empty(S["outbuf"].shape, dtype=S["outbuf"].dtype, pin_memory=True)
+                for S in st.sets[:n_sets]]
+    h2d = host_in[0].numel() * host_in[0].element_size()
+    d2h = host_out[0].numel() * host_out[0].element_size()
+    compute = torch.cuda.current_stream(dev)
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(n_sets)]
+    ev_done = [torch.cuda.Event() for _ in range(n_sets)]
+    ev_out = [torch.cuda.Event() for _ in range(n_sets)]
 
-    def one():
-        for h, d in host_in:
-            d.copy_(h, non_blocking=True)
-        if graph is not None:
-            graph.replay()
-        else:
-            st.step()
-        for h, d in host_out:
-            h.copy_(d, non_blocking=True)
+    def run(k0, k1):
+        for k in range(k0, k1):
+            i = k % n_sets
+            S = st.sets[i]
+            with torch.cuda.stream(up):
+                if k >= n_sets:  # step k - n_sets has finished with this set and its download
+                    up.wait_event(ev_out[i])
+                S["inbuf"].copy_(host_in[i], non_blocking=True)
+                ev_in[i].record(up)
+            compute.wait_event(ev_in[i])
+            if graphs[i] is not None:
+                graphs[i].replay()
+            else:
+                st.step(set_idx=i)
+            ev_done[i].record(compute)
+            with torch.cuda.stream(down):
+                down.wait_event(ev_done[i])
+                host_out[i].copy_(S["outbuf"], non_blocking=True)
+                ev_out[i].record(down)
+        compute.wait_stream(down)
 
-    for _ in range(2):
-        one()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    run(0, 2)
     torch.cuda.synchronize(dev)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(steps):
-        one()
-    b.record()
+    up.wait_stream(compute)
+    start.record(compute)
+    up.wait_event(start)
+    run(0, steps)
+    end.record(compute)
     torch.cuda.synchronize(dev)
-    return {"step_ms": a.elapsed_time(b) / steps, "h2d": h2d, "d2h": d2h}
+    return {"step_ms": start.elapsed_time(end) / steps, "h2d": h2d, "d2h": d2h}
 
 
 # ----------------------------------------------------------------------------------------
