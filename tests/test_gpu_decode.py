@@ -248,3 +248,16 @@ def test_a_wait_that_runs_out_reports_timeout_and_leaves_the_context_usable():
     w = wl.random_small(77, num_seqs=2, max_ctx=50)
     step = GpuStep(w)
     assert torch.isfinite(step.decode().float()).all()
+
+
+def test_the_largest_batch_one_call_accepts():
+    """4096 sequences (the per-call maximum) of 1..80 tokens: every (sequence, head) row,
+    stores bit-exact; 4097 is refused on the host."""
+    rng = np.random.default_rng(77)
+    ctx = rng.integers(1, 81, size=4096)
+    w = wl.make_workload("max_batch", ctx - 1, np.ones_like(ctx), seed=77, pool_slack=0.05)
+    full_check(w)
+    step = GpuStep(wl.make_workload("over", [3] * 4097, [1] * 4097, seed=1, pool_slack=0.0))
+    out = torch.empty_like(step.vals["q_decode"])
+    with pytest.raises(pa.PagedKVError):
+        pa.pa_decode(out, step.vals["q_decode"], step.kc, step.vc, step.bt, step.ctx, 0.125, 4)

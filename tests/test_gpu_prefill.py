@@ -122,3 +122,21 @@ def test_bad_block_is_flagged_not_fatal():
                         step.vc, bt, step.ctx, w.scale, device_status=status)
     assert pa.pa_check_device_status(status) == pa.PA_ERR_DEVICE_INDEX
     assert torch.isfinite(step.prefill().float()).all()  # context still usable
+
+
+def test_long_chunk_sampled_rows():
+    """One 4100-row chunk over 4000 prior tokens (129 query tiles, up to 127 key tiles):
+    rows at both ends and across tile edges against the oracle's causal definition."""
+    w = wl.make_workload("long_chunk", [4000], [4100], num_prefill=1, seed=21, pool_slack=0.1)
+    step = GpuStep(w)
+    out = step.prefill()
+    assert step.check_status() == pa.PA_OK
+    hv = host_vals(step.vals)
+    kc, vc = oracle_pools(w, hv)
+    rows = [0, 1, 31, 32, 63, 64, 1000, 2047, 2048, 4063, 4064, 4098, 4099]
+    ctx = [4000 + i + 1 for i in rows]
+    q = wl.bf16_bits(hv["q_prefill"])[rows]
+    ref, err = oracle.decode(q, kc, vc, np.repeat(w.block_tables, len(rows), axis=0),
+                             np.array(ctx, np.int32), w.scale)
+    assert err == 0
+    check(out[torch.tensor(rows, device="cuda")], ref, "long chunk rows")
