@@ -185,11 +185,15 @@ __device__ __forceinline__ void attend_tile(const uint8_t* __restrict__ kt,
                                             int dq, int valid_tokens,
                                             const float2 (&qf)[GROUP][4], float& m, float& l,
                                             float2 (&o)[GROUP][4]) {
+  // all K loads of the tile first, so their latencies overlap
+  uint4 kr[kPasses];
+#pragma unroll
+  for (int j = 0; j < kPasses; ++j) kr[j] = lds128(kt + (tg + 4 * j) * kRowBytes + dq * 16);
   float s[kPasses];
 #pragma unroll
   for (int j = 0; j < kPasses; ++j) {
     float2 kf[4];
-    unpack4(lds128(kt + (tg + 4 * j) * kRowBytes + dq * 16), kf);
+    unpack4(kr[j], kf);
     float a[GROUP];
 #pragma unroll
     for (int h = 0; h < GROUP; ++h) {
@@ -201,6 +205,9 @@ __device__ __forceinline__ void attend_tile(const uint8_t* __restrict__ kt,
     s[j] = score_for_own_head<GROUP>(a, dq);
     if (TAIL && tg + 4 * j >= valid_tokens) s[j] = -INFINITY;
   }
+  uint4 vr[kPasses];  // V loads overlap the softmax below
+#pragma unroll
+  for (int j = 0; j < kPasses; ++j) vr[j] = lds128(vt + (tg + 4 * j) * kRowBytes + dq * 16);
   const float mt = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
   const bool grow = mt - m > kRescaleThreshold;  // first tile: m = -inf
   if (__any_sync(0xffffffffu, grow)) {
@@ -226,7 +233,7 @@ __device__ __forceinline__ void attend_tile(const uint8_t* __restrict__ kt,
   l += (pr[0] + pr[1]) + (pr[2] + pr[3]);
 #pragma unroll
   for (int j = 0; j < kPasses; ++j) {
-    uint4 va = lds128(vt + (tg + 4 * j) * kRowBytes + dq * 16);
+    uint4 va = vr[j];
     if (TAIL && tg + 4 * j >= valid_tokens) va = make_uint4(0, 0, 0, 0);  // may hold NaN
     float2 vf[4];
     unpack4(va, vf);
