@@ -116,8 +116,8 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t 
  * over all context_lens[s] cached tokens:
  *   out[s][h][:] = sum_j softmax_j(scale * q[s][h] . K_s[j][h / group]) V_s[j][h / group]
  * where K_s[j] / V_s[j] is the token at logical position j found through block_tables.
- * The (sequence, K/V head, block) tiles are split evenly over the SMs (or into runs of
- * partition_tokens tokens); runs that end inside a sequence leave (running max, running
+ * The (sequence, K/V head, block) tiles are split evenly over the SMs (or into runs of at
+ * most partition_tokens tokens); runs that end inside a sequence leave (running max, running
  * sum, unnormalised output) partials.  With partition_tokens == 0 and max_context_len <=
  * 8192 the warp that finishes the last piece of a sequence merges them inside the same
  * kernel; otherwise a second kernel merges them.
@@ -126,8 +126,9 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t 
  *   block_tables     int32 [num_seqs][max_blocks_per_seq]
  *   context_lens     int32 [num_seqs]; 0 gives a zero output row
  *   max_context_len  host-known upper bound of context_lens (sizes the grid)
- *   partition_tokens 0 = split evenly over the device; else a multiple of 16 giving
- *                    the run length in tokens
+ *   partition_tokens 0 = split evenly over the device; else a multiple of 16 bounding
+ *                    the run length in tokens (runs are then as even as the bound allows,
+ *                    in equal numbers per streaming warp)
  *   workspace        zero-initialised device buffer of >= pa_decode_workspace_size(...)
  *                    bytes (see pa_decode_workspace_size)
  * num_seqs == 0 is a no-op.  At most 4096 sequences per call. */

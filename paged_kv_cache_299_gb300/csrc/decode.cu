@@ -64,6 +64,7 @@ struct KParams {
   int32_t grid;      // runs of the decomposition (warp w of the grid serves runs
                      // w, w + warps, ...)
   int32_t chunk;     // tiles per run, 0 = balanced split into `grid` runs
+  int64_t tile_bound;  // > 0: the host's upper bound of the tile count (partitioned runs)
   int64_t* ws_total;    // total tiles, written by CTA 0
   int32_t* ws_seq_base; // [num_seqs + 1] blocks-per-head prefix, written by CTA 0
   float* partials;      // [runs][2][GROUP][kPartialFloats]
@@ -451,7 +452,8 @@ paged_decode_kernel(const KParams p) {
     for (int i = tid; i <= S; i += kThreads) p.ws_seq_base[i] = seq_base[i];
     if (tid == 0) {
       *p.ws_total = total;
-      if (p.chunk > 0 && static_cast<int64_t>(p.grid) * p.chunk < total)
+      if ((p.chunk > 0 && static_cast<int64_t>(p.grid) * p.chunk < total) ||
+          (p.tile_bound > 0 && total > p.tile_bound))
         flag_error(p.status, PA_DEVFLAG_BAD_CONTEXT);  // contexts beyond max_context_len
     }
   }
@@ -846,6 +848,7 @@ cudaError_t launch(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t str
   p.q_scale = a.scale * 1.4426950408889634f;
   p.grid = plan.runs;
   p.chunk = plan.chunk;
+  p.tile_bound = plan.tile_bound;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   p.ws_total = reinterpret_cast<int64_t*>(ws);
   p.ws_seq_base = reinterpret_cast<int32_t*>(ws + 16);
@@ -889,9 +892,17 @@ cudaError_t plan_decode(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_he
   const int64_t tiles_upper = static_cast<int64_t>(num_seqs) * num_kv_heads * blocks_max;
   const int64_t resident = static_cast<int64_t>(sms) * ctas_per_sm;
   int64_t runs;
+  plan->tile_bound = 0;
   if (partition_tokens > 0) {
-    plan->chunk = partition_tokens / kBlockSize;
-    runs = (tiles_upper + plan->chunk - 1) / plan->chunk;
+    // Runs of at most partition_tokens tokens, as many as every streaming warp of the grid
+    // can take in equal numbers (a multiple of the warp count once there are more runs than
+    // warps), split evenly over the real tile count: no warp ends a whole run after the rest.
+    const int64_t max_tiles = partition_tokens / kBlockSize;
+    runs = (tiles_upper + max_tiles - 1) / max_tiles;
+    const int64_t warps = resident * kWarps;
+    if (runs > warps) runs = (runs + warps - 1) / warps * warps;
+    plan->chunk = 0;
+    plan->tile_bound = tiles_upper;
   } else {
     plan->chunk = 0;
     runs = resident * kWarps;

@@ -32,6 +32,7 @@ struct DecodePlan {
   int grid;           // CTAs of the attention kernel (persistent, <= resident capacity)
   int runs;           // units of the tile decomposition; CTA c serves runs c, c + grid, ...
   int chunk;          // tiles per run (fixed mode), 0 = balanced split of the real total
+  int64_t tile_bound; // > 0: host upper bound of the tile count, checked on the device
   size_t smem_bytes;  // dynamic shared memory of the attention kernel
   bool fused_merge;          // split segments merged inside the attention kernel
   size_t ws_count_offset;    // offset of the per-segment piece counters (must start zeroed)
