@@ -298,10 +298,59 @@ __device__ __forceinline__ int64_t segment_piece_run(const SegmentPieces& sp, in
 // overlap; chunks of 32 pieces are combined with a running maximum.  Partials were written
 // by other warps in this launch, so they are read through L2 (__ldcg), after the caller's
 // acquire fence.
+constexpr int kFewPieces = 4;  // segments of up to this many pieces merge in one load round
+
 template <int GROUP>
 __device__ void merge_segment_in_warp(const KParams& p, const SegmentPieces& sp, int64_t x0,
                                       int64_t x1, int64_t total, int s, int g, int lane) {
   const int n = segment_piece_count(sp, x0, x1, total, p.grid);
+  if (n <= kFewPieces) {
+    // Few pieces (the usual case): every lane loads the (max, sum) of all pieces and its
+    // own output slice of each, all in one round of loads, and combines them in registers.
+    float mk[kFewPieces][GROUP], lk[kFewPieces][GROUP];
+    float2 vk[kFewPieces][GROUP];
+#pragma unroll
+    for (int k = 0; k < kFewPieces; ++k) {
+      if (k < n) {
+        const int64_t c = segment_piece_run(sp, x0, k, total, p.grid, p.chunk);
+        const int slot = k == 0 ? sp.first_slot : 0;
+        const float* rec = p.partials + (c * 2 + slot) * GROUP * kPartialFloats;
+#pragma unroll
+        for (int h = 0; h < GROUP; ++h) {
+          mk[k][h] = __ldcg(rec + h * kPartialFloats + kHeadDim);
+          lk[k][h] = __ldcg(rec + h * kPartialFloats + kHeadDim + 1);
+          vk[k][h] = __ldcg(reinterpret_cast<const float2*>(rec + h * kPartialFloats) + lane);
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < GROUP; ++h) {
+          mk[k][h] = -INFINITY;
+          lk[k][h] = 0.f;
+          vk[k][h] = make_float2(0.f, 0.f);
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < GROUP; ++h) {
+      float mh = mk[0][h];
+#pragma unroll
+      for (int k = 1; k < kFewPieces; ++k) mh = fmaxf(mh, mk[k][h]);
+      float lh = 0.f;
+      float2 ah = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < kFewPieces; ++k) {
+        const float wgt = k < n ? fast_exp2(mk[k][h] - mh) : 0.f;
+        lh += wgt * lk[k][h];
+        ah.x += wgt * vk[k][h].x;
+        ah.y += wgt * vk[k][h].y;
+      }
+      const float inv = 1.f / lh;
+      __nv_bfloat16* out =
+          p.out + (static_cast<int64_t>(s) * p.num_q_heads + g * GROUP + h) * kHeadDim;
+      reinterpret_cast<__nv_bfloat162*>(out)[lane] = __floats2bfloat162_rn(ah.x * inv, ah.y * inv);
+    }
+    return;
+  }
   float M[GROUP], L[GROUP];
   float2 acc[GROUP];
 #pragma unroll
