@@ -300,7 +300,18 @@ __device__ __forceinline__ int64_t segment_piece_run(const SegmentPieces& sp, in
 // acquire fence.
 constexpr int kFewPieces = 4;  // segments of up to this many pieces merge in one load round
 
-template <int GROUP>
+// Partials written by warps of this CTA (published with CTA-scope ordering) are read with
+// plain loads; partials from other SMs through L2.
+template <bool kLocal>
+__device__ __forceinline__ float ld_partial(const float* a) {
+  return kLocal ? *a : __ldcg(a);
+}
+template <bool kLocal>
+__device__ __forceinline__ float2 ld_partial2(const float2* a) {
+  return kLocal ? *a : __ldcg(a);
+}
+
+template <int GROUP, bool kLocal>
 __device__ void merge_segment_in_warp(const KParams& p, const SegmentPieces& sp, int64_t x0,
                                       int64_t x1, int64_t total, int s, int g, int lane) {
   const int n = segment_piece_count(sp, x0, x1, total, p.grid);
@@ -317,9 +328,9 @@ __device__ void merge_segment_in_warp(const KParams& p, const SegmentPieces& sp,
         const float* rec = p.partials + (c * 2 + slot) * GROUP * kPartialFloats;
 #pragma unroll
         for (int h = 0; h < GROUP; ++h) {
-          mk[k][h] = __ldcg(rec + h * kPartialFloats + kHeadDim);
-          lk[k][h] = __ldcg(rec + h * kPartialFloats + kHeadDim + 1);
-          vk[k][h] = __ldcg(reinterpret_cast<const float2*>(rec + h * kPartialFloats) + lane);
+          mk[k][h] = ld_partial<kLocal>(rec + h * kPartialFloats + kHeadDim);
+          lk[k][h] = ld_partial<kLocal>(rec + h * kPartialFloats + kHeadDim + 1);
+          vk[k][h] = ld_partial2<kLocal>(reinterpret_cast<const float2*>(rec + h * kPartialFloats) + lane);
         }
       } else {
 #pragma unroll
@@ -372,8 +383,8 @@ __device__ void merge_segment_in_warp(const KParams& p, const SegmentPieces& sp,
     float mk[GROUP], lk[GROUP], wk[GROUP];
 #pragma unroll
     for (int h = 0; h < GROUP; ++h) {
-      mk[h] = valid ? __ldcg(rec + h * kPartialFloats + kHeadDim) : -INFINITY;
-      lk[h] = valid ? __ldcg(rec + h * kPartialFloats + kHeadDim + 1) : 0.f;
+      mk[h] = valid ? ld_partial<kLocal>(rec + h * kPartialFloats + kHeadDim) : -INFINITY;
+      lk[h] = valid ? ld_partial<kLocal>(rec + h * kPartialFloats + kHeadDim + 1) : 0.f;
     }
 #pragma unroll
     for (int h = 0; h < GROUP; ++h) {
@@ -405,7 +416,7 @@ __device__ void merge_segment_in_warp(const KParams& p, const SegmentPieces& sp,
         for (int h = 0; h < GROUP; ++h) {
           w[u][h] = __shfl_sync(0xffffffffu, wk[h], j);
           if (j0 + u >= cnt) w[u][h] = 0.f;
-          v[u][h] = __ldcg(reinterpret_cast<const float2*>(rj + h * kPartialFloats) + lane);
+          v[u][h] = ld_partial2<kLocal>(reinterpret_cast<const float2*>(rj + h * kPartialFloats) + lane);
         }
       }
 #pragma unroll
@@ -447,6 +458,10 @@ paged_decode_kernel(const KParams p) {
   int32_t* seq_base = reinterpret_cast<int32_t*>(bars + kWarps * kStagesPerWarp) +
                       kWarps * kStagesPerWarp;
   __shared__ int64_t warp_sums[kWarps];
+  // piece counters of split segments whose pieces all run on this CTA, by the segment's
+  // first run modulo kWarps (two such segments never share a first run)
+  __shared__ int cta_seg_count[kWarps];
+  if (tid < kWarps) cta_seg_count[tid] = 0;
 
   if (lane == 0) {
     for (int i = 0; i < kStagesPerWarp; ++i) mbar_init(&full_bar[i], 1);
@@ -716,19 +731,37 @@ paged_decode_kernel(const KParams p) {
     }
     if (!whole && p.fused_merge) {
       // Publish this piece; the warp that publishes the segment's last piece merges it.
-      __threadfence();
-      __syncwarp();
+      // When every piece of the segment runs on this CTA (one round of runs, all its runs
+      // among this CTA's kWarps), publishing needs only CTA-scope ordering and a shared
+      // counter; otherwise device-scope fences and the workspace counter.
       const int64_t x0 = static_cast<int64_t>(seq_base[pc.s]) * KV + static_cast<int64_t>(pc.g) * pc.nb;
       const SegmentPieces sp = segment_pieces(x0, x0 + pc.nb, total, p.grid, p.chunk);
+      const bool local = p.grid <= total_warps && sp.c_first / kWarps == sp.c_last / kWarps;
       int last = 0;
-      if (lane == 0) {
-        const int n = segment_piece_count(sp, x0, x0 + pc.nb, total, p.grid);
-        last = atomicAdd(&p.seg_count[pc.s * KV + pc.g], 1) == n - 1;
-      }
-      if (__shfl_sync(0xffffffffu, last, 0)) {
-        __threadfence();  // acquire the other pieces' partials
-        merge_segment_in_warp<GROUP>(p, sp, x0, x0 + pc.nb, total, pc.s, pc.g, lane);
-        if (lane == 0) p.seg_count[pc.s * KV + pc.g] = 0;  // ready for the next call
+      if (local) {
+        __threadfence_block();
+        __syncwarp();
+        if (lane == 0) {
+          const int n = segment_piece_count(sp, x0, x0 + pc.nb, total, p.grid);
+          last = atomicAdd(&cta_seg_count[sp.c_first % kWarps], 1) == n - 1;
+        }
+        if (__shfl_sync(0xffffffffu, last, 0)) {
+          __threadfence_block();  // acquire the other pieces' partials
+          merge_segment_in_warp<GROUP, true>(p, sp, x0, x0 + pc.nb, total, pc.s, pc.g, lane);
+          if (lane == 0) cta_seg_count[sp.c_first % kWarps] = 0;
+        }
+      } else {
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+          const int n = segment_piece_count(sp, x0, x0 + pc.nb, total, p.grid);
+          last = atomicAdd(&p.seg_count[pc.s * KV + pc.g], 1) == n - 1;
+        }
+        if (__shfl_sync(0xffffffffu, last, 0)) {
+          __threadfence();  // acquire the other pieces' partials
+          merge_segment_in_warp<GROUP, false>(p, sp, x0, x0 + pc.nb, total, pc.s, pc.g, lane);
+          if (lane == 0) p.seg_count[pc.s * KV + pc.g] = 0;  // ready for the next call
+        }
       }
     }
     y += ntiles;
