@@ -10,23 +10,25 @@
 // GB300 design (decode is HBM-bound: each (block, kv head) tile of 2 KiB of K + 2 KiB of
 // V is read once and feeds 4 query heads):
 //   * The flattened space of (sequence, kv head, block) tiles is cut into contiguous runs
-//     of equal length, one per warp of a persistent grid (or runs of `chunk` tiles when
-//     the caller fixes the partition), so every warp streams the same number of bytes
-//     whatever the length mix.
+//     of equal length, one per warp of a persistent grid, so every warp streams the same
+//     number of bytes whatever the length mix.  With partition_tokens the runs are at most
+//     that long, in equal numbers per warp.
 //   * Each warp streams its own run through a private 4-stage ring in shared memory: lane
 //     0 issues cp.async.bulk (TMA, non-tensor) copies of the K and V tile, completing on
 //     the stage's mbarrier, and refills a stage as soon as the warp has consumed it.  The
 //     block-table entries are fetched 32 at a time, one window ahead.  No producer warp,
 //     no release barriers, no block-wide synchronisation while streaming.
-//   * Lane (tg, dq) owns tokens tg and tg+8 of a tile and a quarter of the 64 dims; q for
-//     all GROUP heads stays in registers (pre-scaled by scale*log2 e).  The 4-lane dot
-//     products are finished by a reduce-scatter that leaves each lane one head's score,
-//     whose online softmax (running max, running sum) it keeps; the reference max is
-//     raised only when a score exceeds it by more than 2^8.
-//   * When a run ends or crosses into the next (sequence, kv head), the warp's eight
-//     token-group states are combined through shared memory (log-sum-exp weights) and
-//     either the final bf16 rows are written (whole sequence in one run) or an
-//     unnormalised (o, max, sum) partial, which merge_partials_kernel combines.
+//   * Lane 8 tg + dq owns 4 tokens of a tile (tg, tg + 4, tg + 8, tg + 12) and 8 of the
+//     64 dims; q for all GROUP heads stays in registers (pre-scaled by scale * log2 e).
+//     The 8-lane dot products are finished by a reduce-scatter that leaves each lane one
+//     head's score, whose online softmax (running max, running sum) it keeps; the
+//     reference max is raised only when a score exceeds it by more than 2^8.
+//   * When a piece ends, the warp's 4 token-group states are combined by shuffles and
+//     either the final bf16 rows are written (the whole segment in one piece) or an
+//     unnormalised (o, max, sum) partial.  The warp that publishes a segment's last piece
+//     merges its partials (log-sum-exp weights) inside this kernel, with CTA-scope
+//     ordering when all the segment's pieces ran on its CTA; beyond 8192-token contexts
+//     or with fixed partitions merge_partials_kernel does it.
 #include <math.h>
 
 #include "common.cuh"
