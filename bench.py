@@ -52,6 +52,10 @@ def parse_args():
                     help="time the step as eager C-ABI calls or as one CUDA-graph replay")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--flush", choices=["write-read", "write"], default="write-read",
+                    help="L2 flush between steps of workloads smaller than 4x L2: rewrite a "
+                         "2x L2 buffer, then read another (so the step starts from clean "
+                         "lines), or only rewrite it")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the workload's layer count (small cases for profilers)")
     return ap.parse_args()
@@ -389,6 +393,15 @@ def run_gpu(args, rank, world):
     kv_bytes = w.decode_kv_bytes()
     flush = kv_bytes < 4 * l2
     flush_buf = torch.empty(2 * l2 // 4 + 1024, dtype=torch.int32, device=dev) if flush else None
+    flush_rd = (torch.zeros(2 * l2 // 4 + 1024, dtype=torch.int32, device=dev)
+                if flush and args.flush == "write-read" else None)
+
+    def flush_l2(k):
+        # rewrite a buffer of twice the L2 size; then read another one, so that the dirty
+        # lines are written back before the step rather than during it
+        flush_buf.fill_(k)
+        if flush_rd is not None:
+            flush_rd.sum()
 
     def barrier():
         if world > 1:
@@ -419,7 +432,7 @@ def run_gpu(args, rank, world):
     t_wall = time.perf_counter()
     for k in range(K):
         if flush:
-            flush_buf.fill_(k)  # rewrite a buffer of twice the L2 size between steps
+            flush_l2(k)
         step_ev[k][0].record()
         if graph is not None:
             graph.replay()
@@ -430,7 +443,7 @@ def run_gpu(args, rank, world):
     if graph is not None:  # per-kernel timing: an eager pass right after, same workload
         for k in range(min(K, 20)):
             if flush:
-                flush_buf.fill_(k)
+                flush_l2(k)
             st.step(dec_ev[k] if w.num_decode else None, pre_ev[k] if pre_ev else None)
         torch.cuda.synchronize(dev)
     barrier()
@@ -451,7 +464,7 @@ def run_gpu(args, rank, world):
     # ---- end to end through the public API with host buffers ----
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(st, max(3, min(K, 50)), dev, graph)
+        e2e = run_e2e(st, max(3, min(K, 50)), dev, graph, flush_l2 if flush else None)
         e2e["step_ms"] = max_over_ranks(e2e["step_ms"], dev)
 
     if rank != 0:
@@ -465,7 +478,9 @@ def run_gpu(args, rank, world):
         "dtype": "bf16", "data": "synthetic",
         "config": dict(describe(w), parallelism=f"replicas{world}" if world > 1 else "single",
                        accumulate="f32",
-                       l2=("flushed between steps (2x L2 rewrite)" if flush
+                       l2=(("flushed between steps (2x L2 rewrite, then 2x L2 read)"
+                            if args.flush == "write-read" else
+                            "flushed between steps (2x L2 rewrite)") if flush
                            else "inputs larger than L2 (%.1f GB KV per step)" % (kv_bytes / 1e9)),
                        launch=("CUDA graph: one replay per step (kernel times from an "
                                "eager pass right after)" if graph is not None
@@ -519,14 +534,16 @@ def run_gpu(args, rank, world):
     print(json.dumps(res), flush=True)
 
 
-def run_e2e(st: DeviceStep, steps: int, dev, graph=None) -> dict:
+def run_e2e(st: DeviceStep, steps: int, dev, graph=None, flush_l2=None) -> dict:
     """Each step: pinned host -> device copy of the step's inputs (queries, new K/V, block
     tables, context lengths of every layer: one buffer), the step through the C ABI, and
     a device -> host copy of its attention outputs (one buffer).  As a serving loop would,
     two buffer sets alternate so that the copies of one step overlap the attention of its
     neighbour: inputs of step k+1 go up and outputs of step k-1 come down on two copy
     streams while step k computes.  Timed on the device from the first upload to the last
-    download."""
+    download.  For workloads that must have L2 flushed between steps (flush_l2 given) the
+    steps run one after the other instead, each timed from its upload to its download with
+    the flush outside."""
     import torch
     n_sets = 2
     while len(st.sets) < n_sets:
@@ -569,6 +586,25 @@ def run_e2e(st: DeviceStep, steps: int, dev, graph=None) -> dict:
                 ev_out[i].record(down)
         compute.wait_stream(down)
 
+    if flush_l2 is not None:
+        S = st.sets[0]
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for k in range(2 + steps):
+            flush_l2(k)
+            if k >= 2:
+                evs[k - 2][0].record(compute)
+            S["inbuf"].copy_(host_in[0], non_blocking=True)
+            if graphs[0] is not None:
+                graphs[0].replay()
+            else:
+                st.step(set_idx=0)
+            host_out[0].copy_(S["outbuf"], non_blocking=True)
+            if k >= 2:
+                evs[k - 2][1].record(compute)
+        torch.cuda.synchronize(dev)
+        return {"step_ms": sum(a.elapsed_time(b) for a, b in evs) / steps, "h2d": h2d,
+                "d2h": d2h}
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     run(0, 2)
