@@ -470,6 +470,22 @@ paged_decode_kernel(const KParams p) {
     fence_barrier_init();
   }
 
+  // Query rows (and, with the fused append, the new K/V rows) are read when a piece starts,
+  // often in the middle of a warp's stream: bring all of them into L2 now, one 128-byte row
+  // per thread of the grid.
+  {
+    const int64_t q_rows = static_cast<int64_t>(S) * p.num_q_heads;
+    const int64_t kv_rows = p.k_new != nullptr ? static_cast<int64_t>(S) * KV : 0;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + tid; i < q_rows + 2 * kv_rows;
+         i += static_cast<int64_t>(gridDim.x) * kThreads) {
+      const uint8_t* row =
+          i < q_rows ? reinterpret_cast<const uint8_t*>(p.q) + i * kRowBytes
+          : i < q_rows + kv_rows ? p.k_new + (i - q_rows) * kRowBytes
+                                 : p.v_new + (i - q_rows - kv_rows) * kRowBytes;
+      prefetch_l2(row);
+    }
+  }
+
   // ---- per-sequence block counts and their exclusive prefix (the tile index space) ----
   for (int i = tid; i < S; i += kThreads) {
     const int32_t L = p.context_lens[i];

@@ -17,16 +17,19 @@
 //     four 16-row TMA boxes at the physical blocks named by the block table (128-byte
 //     swizzle), into a 4-stage ring; the block table is read in prefetched 32-entry windows.
 //   * Warp 4 (one thread) issues S = Q K^T (M128 N64 K64 into one of two fp32 S buffers,
-//     so the next tile's scores are computed during this tile's softmax) and O += P V
-//     (M128 N64 K64, V read N-major).  Both A operands come from TMEM: Q is copied there
-//     once by the row warps and P is written there per tile, so each MMA streams only its
-//     K or V tile from shared memory.
+//     so the next tile's scores are computed during this tile's softmax) and
+//     [O | l] += P [V | 1] (M128 N80 K64, V read N-major): 16 extra columns of the B operand
+//     come from a constant shared-memory atom of bf16 ones, one leading-byte offset from
+//     each V slice, so the tensor core also accumulates the row sums l of exactly the bf16
+//     P that weights V.  Both A operands come from TMEM: Q is copied there once by the row
+//     warps and P is written per tile over the first half of its own S buffer, so each MMA
+//     streams only its K or V tile from shared memory.
 //   * Warps 0-3 own one TMEM lane = one query row each: they read S, mask by absolute
-//     position (diagonal tiles only), keep the running max / sum in registers (O in TMEM is
+//     position (diagonal tiles only), keep the running max in registers ([O | l] in TMEM is
 //     rescaled only when the max grows by more than 2^8), write P as packed bf16 into TMEM,
-//     and finally normalise O and store bf16 rows.
-// TMEM per CTA (256 columns): S buffers 0..63 and 64..127, O 128..191, Q 192..223,
-// P 224..255.
+//     and finally divide O by l and store bf16 rows.
+// TMEM per CTA (256 columns): S buffers 0..63 and 64..127 (P over 0..31 / 64..95), O
+// 128..191, l 192..207, Q 224..255.
 // Every mbarrier wait is bounded; on timeout the CTA records PA_DEVFLAG_TIMEOUT, drains
 // its own copies and MMAs, frees its tensor memory and returns.
 #include <cudaTypedefs.h>
@@ -47,17 +50,20 @@ constexpr int kBlocksPerTile = kTileN / kBlockSize;
 constexpr int kStages = 4;                        // K/V ring depth
 constexpr int kQBytes = kTileM * kRowBytes;       // 16 KiB
 constexpr int kKVBytes = kTileN * kRowBytes;      // 8 KiB per K (or V) tile
+constexpr int kOnesBytes = 16 * kRowBytes;        // 16 key rows of bf16 1.0: the row-sum atom
 constexpr int kNumBars = 1 + 2 * kStages + 2 + 4; // q, kv full/empty, s x2, p, o, drain, q_tmem
-constexpr int kSmemBytes = kQBytes + 2 * kStages * kKVBytes + 8 * 16 + 16 + 16;
+constexpr int kSmemBytes = kQBytes + 2 * kStages * kKVBytes + kOnesBytes + 8 * 16 + 16 + 16;
 static_assert(kNumBars <= 16, "barrier area");
 static_assert(32 % kBlocksPerTile == 0, "block-table windows hold whole K/V tiles");
 // Two CTAs fit on one SM (2 x (kSmemBytes + 1 KiB reserved) <= 228 KiB, 2 x 256 TMEM
 // columns = 512, <= 168 registers per thread), so one CTA's softmax overlaps the other's MMAs.
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kSCol = 0;     // two S buffers (fp32): columns 0..63 and 64..127
-constexpr uint32_t kOCol = 128;   // O (fp32): columns 128..191
-constexpr uint32_t kQCol = 192;   // Q (bf16 pairs): columns 192..223, the A operand of S = Q K^T
-constexpr uint32_t kPCol = 224;   // P (bf16 pairs): columns 224..255, the A operand of O += P V
+constexpr uint32_t kSCol = 0;     // two S buffers (fp32): columns 0..63 and 64..127; P (bf16
+                                  // pairs) of a tile overwrites the first 32 of its S buffer
+constexpr uint32_t kOCol = 128;   // O (fp32): columns 128..191, then 16 row-sum columns
+constexpr uint32_t kLCol = kOCol + kHeadDim;  // row sum l (columns 192..207 hold 16 copies)
+constexpr uint32_t kQCol = 224;   // Q (bf16 pairs): columns 224..255, the A operand of S = Q K^T
+constexpr int kPVN = kHeadDim + 16;  // PV MMA width: 64 output dims + 16 ones columns
 constexpr int kThreads = 192;
 constexpr float kRescaleThreshold = 8.0f;
 
@@ -140,7 +146,8 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
   uint8_t* sq = smem;
   uint8_t* sk = sq + kQBytes;
   uint8_t* sv = sk + kStages * kKVBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sv + kStages * kKVBytes);
+  uint8_t* sones = sv + kStages * kKVBytes;  // 1 KiB aligned (whole tiles before it)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sones + kOnesBytes);
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = kv_full + kStages;
@@ -176,6 +183,11 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
     prefetch_tensormap(&tmap_k);
     prefetch_tensormap(&tmap_v);
   }
+  // The ones atom: every bf16 of it is 1.0, so the 16 extra columns of O += P [V | 1] each
+  // accumulate the row sum of P, exactly the bf16 values that weight V.
+  for (int i = tid; i < kOnesBytes / 16; i += kThreads)
+    reinterpret_cast<uint4*>(sones)[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+  fence_proxy_async_smem();  // generic writes before the tensor core's reads
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -242,12 +254,15 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
   } else if (warp == 4) {
     // ================================ MMA issuer ==================================
     // Both A operands live in tensor memory (Q copied there once, P written there by the
-    // row warps), so each MMA streams only its B tile (K or V, 2 KiB per K16 step) from
-    // shared memory.  Order: S(0), S(1), PV(0), S(2), PV(1), ...: the scores of the next
-    // tile are on the tensor core while the row warps run the softmax of the current one.
+    // row warps over its tile's scores), so each MMA streams only its B tile (K or V,
+    // 2 KiB per K16 step) from shared memory.  Order: S(0), S(1), PV(0), S(2), PV(1), ...:
+    // the scores of the next tile are on the tensor core while the row warps run the
+    // softmax of the current one; S(j+2) reuses the buffer of P(j) only after PV(j) (the
+    // tensor core runs one thread's MMAs in order).
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(kTileM, kTileN, false);
-      constexpr uint32_t kIdescO = idesc_bf16_f32(kTileM, kHeadDim, true);
+      constexpr uint32_t kIdescO = idesc_bf16_f32(kTileM, kPVN, true);
+      const uint32_t ones_addr = smem_addr(sones);
       auto issue_s = [&](int j) -> bool {
         const int st = j % kStages;
         if (!wait_or_abort(&kv_full[st], static_cast<uint32_t>((j / kStages) & 1), &abort_flag,
@@ -266,10 +281,14 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
       };
       auto issue_pv = [&](int j) {
         const uint32_t v_base = smem_addr(sv + (j % kStages) * kKVBytes);
+        const uint32_t p_tmem = tmem + kSCol + (j & 1) * kTileN;
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk) {
-          const uint64_t b = sw128_desc(v_base + kk * 16 * kRowBytes, 16, 1024);
-          umma_bf16_ts(tmem + kOCol, tmem + kPCol + kk * 8, b, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+          // B = [V rows kk*16 .. +15 | ones]: output dims 0..63 from the V tile (N-major,
+          // 128-byte swizzle), columns 64..79 from the ones atom, one leading-byte offset away
+          const uint32_t b_addr = v_base + kk * 16 * kRowBytes;
+          const uint64_t b = sw128_desc(b_addr, ones_addr - b_addr, 1024);
+          umma_bf16_ts(tmem + kOCol, p_tmem + kk * 8, b, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(o_done);
         umma_commit(&kv_empty[j % kStages]);
@@ -300,7 +319,6 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
     const int pos_lo = L - q_len + tok0;  // smallest position among this CTA's rows
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     float m = -INFINITY;
-    float l = 0.f;
     bool ok = wait_or_abort(q_full, 0, &abort_flag, p.status);
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
@@ -357,18 +375,16 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
         alpha = fast_exp2(m - m_new);
         m = m_new;
       }
-      // p = 2^(s * scale - m) two at a time, packed to bf16 into v[0]
+      // p = 2^(s * scale - m) two at a time, packed to bf16 into v[0] (the row sum comes
+      // from the tensor core's ones columns)
       const float2 qs2 = make_float2(p.qk_scale, p.qk_scale);
       const float2 nm2 = make_float2(-m, -m);
-      float2 sum2 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int i = 0; i < kTileN / 2; ++i) {
         const float2 x = __ffma2_rn(make_float2(__uint_as_float(v[i >> 4][(2 * i) & 31]),
                                                 __uint_as_float(v[i >> 4][(2 * i + 1) & 31])),
                                     qs2, nm2);
-        const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-        sum2 = __fadd2_rn(sum2, e);
-        const __nv_bfloat162 b2 = __floats2bfloat162_rn(e.x, e.y);
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(fast_exp2(x.x), fast_exp2(x.y));
         v[0][i] = *reinterpret_cast<const uint32_t*>(&b2);
       }
       if (j == n_kv - 1 && kb + kTileN > keys) {
@@ -384,31 +400,36 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
         fence_proxy_async_smem();
       }
       if (j > 0) {
-        // P(j-1) must be consumed before P(j) overwrites it, and O may need rescaling
+        // Every phase of o_done is observed in order (a parity wait cannot tell phases two
+        // apart).  PV(j-1) is done with O and its row sum before they are rescaled; P(j)
+        // itself needs no wait: PV(j-2), the last reader of this S buffer, completed before
+        // S(j) did.
         ok = wait_or_abort(o_done, static_cast<uint32_t>((j - 1) & 1), &abort_flag, p.status);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after_sync();
-        if (__any_sync(0xffffffffu, grow)) {
-          uint32_t(&o)[32] = v[1];  // the raw scores there are spent
-          const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            tmem_ld32(lane_addr + kOCol + 32 * c, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float2 x = __fmul2_rn(
-                  make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), a2);
-              o[2 * i] = __float_as_uint(x.x);
-              o[2 * i + 1] = __float_as_uint(x.y);
-            }
-            tmem_st32(lane_addr + kOCol + 32 * c, o);
-          }
-        }
       }
-      tmem_st32(lane_addr + kPCol, v[0]);
-      l = l * alpha + (sum2.x + sum2.y);
+      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+        uint32_t(&o)[32] = v[1];  // the raw scores there are spent
+        const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          tmem_ld32(lane_addr + kOCol + 32 * c, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 x = __fmul2_rn(
+                make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), a2);
+            o[2 * i] = __float_as_uint(x.x);
+            o[2 * i + 1] = __float_as_uint(x.y);
+          }
+          tmem_st32(lane_addr + kOCol + 32 * c, o);
+        }
+        const uint32_t lsum = tmem_ld1(lane_addr + kLCol);
+        tmem_wait_ld();
+        tmem_st1(lane_addr + kLCol, __float_as_uint(__uint_as_float(lsum) * alpha));
+      }
+      tmem_st32(lane_addr + kSCol + (j & 1) * kTileN, v[0]);  // P(j) over S(j)
       tmem_wait_st();
       tc_fence_before_sync();
       mbar_arrive(p_ready);
@@ -420,7 +441,9 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
     if (ok) {
       tc_fence_after_sync();
       __syncwarp();
-      const float inv = 1.f / l;
+      const uint32_t lsum = tmem_ld1(lane_addr + kLCol);
+      tmem_wait_ld();
+      const float inv = 1.f / __uint_as_float(lsum);  // l >= 1: the max key weighs >= 1
       __nv_bfloat16* dst = p.out + (static_cast<int64_t>(q0 + token) * p.num_q_heads +
                                     g * kGroup + hh) * kHeadDim;
 #pragma unroll 1
