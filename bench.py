@@ -449,6 +449,12 @@ def run_gpu(args, rank, world):
     barrier()
     wall = time.perf_counter() - t_wall
     clocks = sampler.stop()
+    # the in-run read reference: one launch reading as many bytes as one decode launch,
+    # under the same L2 rule, timed the same way
+    stream_ref = None
+    if w.num_decode and not st.unified:
+        stream_ref = measure_stream_read(dev, kv_bytes // w.layers, flush_l2 if flush else None,
+                                         max(3, min(K, 20)))
     step_ms = sum(a.elapsed_time(b) for a, b in step_ev) / K
     n_kernel_steps = min(K, 20) if graph is not None else K
     dec_ms = None
@@ -517,6 +523,10 @@ def run_gpu(args, rank, world):
                       "8192-token contexts, else + merge_partials_kernel)",
             "peak_source": f"{peak_src} hbm_gbs", "pct_of_8tbs": round(100 * achieved / 8000, 2),
             "launch_ms": round(dec_ms, 5), "algorithmic_bytes_per_launch": int(per_launch)}
+    if stream_ref and "roofline" in res:
+        res["roofline"]["stream_read"] = dict(
+            stream_ref, decode_frac_of_stream=round(res["roofline"]["achieved"] /
+                                                    stream_ref["achieved"], 4))
     if pre_ms:
         tfl = st.prefill_flops() / w.layers / (pre_ms * 1e-3) / 1e12
         bf16_peak, bf16_src = measured_bf16_peak()
@@ -532,6 +542,35 @@ def run_gpu(args, rank, world):
     if not args.no_cpu_baseline and world == 1:
         res["cpu_baseline"] = cpu_baseline(w, args.config, target_s=10.0)
     print(json.dumps(res), flush=True)
+
+
+def measure_stream_read(dev, nbytes: int, flush_l2, reps: int) -> dict:
+    """pa_stream_read over `nbytes` (one decode launch's KV bytes): 16-byte vector loads of a
+    contiguous buffer in one launch, CUDA events around each launch (L2 flushed before each
+    when the decode's workload is flushed)."""
+    import torch
+    from paged_kv_cache_299_gb300 import binding as pa
+
+    nbytes -= nbytes % 16
+    buf = torch.zeros(nbytes // 4, dtype=torch.int32, device=dev)
+    x = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        pa.pa_stream_read(buf, x)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    for k, (a, b) in enumerate(evs):
+        if flush_l2 is not None:
+            flush_l2(k)
+        a.record()
+        pa.pa_stream_read(buf, x)
+        b.record()
+    torch.cuda.synchronize(dev)
+    ms = sum(a.elapsed_time(b) for a, b in evs) / reps
+    del buf
+    return {"achieved": round(nbytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "bytes": nbytes,
+            "launch_ms": round(ms, 5),
+            "kernel": "pa_stream_read: one launch of 16-byte streaming loads over a contiguous "
+                      "buffer of one decode launch's KV bytes"}
 
 
 def run_e2e(st: DeviceStep, steps: int, dev, graph=None, flush_l2=None) -> dict:

@@ -283,6 +283,15 @@ int32_t pa_bm_block_table(const pa_block_manager* bm, int64_t seq_id, int32_t* o
 pa_status pa_selftest_wait_timeout(int32_t* device_status, int32_t limit_ms,
                                    pa_stream_t stream);
 
+/* Measurement support: read `bytes` (a multiple of 16) of device memory at `buf` once with
+ * 16-byte streaming loads, in one kernel launch, and XOR all its 32-bit words into
+ * *xor_out (a device uint32; zero it first to obtain the XOR of the buffer), so the reads
+ * cannot be skipped and the result can be checked.  It is the in-run read-only reference
+ * against which the decode kernel's KV bandwidth is reported (same bytes, same launch
+ * conditions).  bytes == 0 launches nothing (buf may then be NULL).  No counterpart on the
+ * pages. */
+pa_status pa_stream_read(const void* buf, size_t bytes, uint32_t* xor_out, pa_stream_t stream);
+
 /* Synchronise `stream`, read *device_status and translate it: PA_OK when zero,
  * PA_ERR_DEVICE_TIMEOUT when the timeout bit is set, else PA_ERR_DEVICE_INDEX. */
 pa_status pa_check_device_status(const int32_t* device_status, pa_stream_t stream);

@@ -46,7 +46,7 @@ EXPORTED = ("pa_compute_slot_mapping", "pa_reshape_and_cache", "pa_decode_worksp
             "pa_bm_destroy", "pa_bm_num_free_blocks", "pa_bm_ref_count", "pa_bm_add_sequence",
             "pa_bm_fork", "pa_bm_append_tokens", "pa_bm_free_sequence", "pa_bm_num_tokens",
             "pa_bm_block_table", "pa_decode_append", "pa_selftest_wait_timeout",
-            "pa_varlen_workspace_size", "pa_attention_varlen")
+            "pa_varlen_workspace_size", "pa_attention_varlen", "pa_stream_read")
 
 
 def library_path() -> str:
@@ -113,6 +113,8 @@ def load(path: str | None = None):
     lib.pa_bm_block_table.restype = i32
     lib.pa_selftest_wait_timeout.argtypes = [P, i32, P]
     lib.pa_selftest_wait_timeout.restype = st
+    lib.pa_stream_read.argtypes = [P, sz, P, P]
+    lib.pa_stream_read.restype = st
     lib.pa_check_device_status.argtypes = [P, P]
     lib.pa_check_device_status.restype = st
     lib.pa_status_string.argtypes = [st]
@@ -424,6 +426,19 @@ class BlockManager:
         if n < 0:
             _check(n, "pa_bm_block_table")
         return [int(out[i]) for i in range(max_blocks)], n
+
+
+def pa_stream_read(buf, xor_out, stream=None):
+    """Read every byte of `buf` once (the in-run read-bandwidth reference) and XOR its 32-bit
+    words into xor_out (int32 [1] on the device, zeroed by the caller); see
+    include/pagedkv.h."""
+    if not buf.is_contiguous() or buf.device.type != "cuda":
+        raise ValueError("buf must be a contiguous CUDA tensor")
+    _need(xor_out, "xor_out", torch.int32, 1)
+    nbytes = buf.numel() * buf.element_size()
+    _check(load().pa_stream_read(_ptr(buf), nbytes, _ptr(xor_out), _stream(stream)),
+           "pa_stream_read")
+    return xor_out
 
 
 def pa_selftest_wait_timeout(device_status, limit_ms=50, stream=None):

@@ -333,6 +333,16 @@ pa_status pa_selftest_wait_timeout(int32_t* device_status, int32_t limit_ms,
                    "timeout self-test launch");
 }
 
+pa_status pa_stream_read(const void* buf, size_t bytes, uint32_t* xor_out, pa_stream_t stream) {
+  if (!xor_out || (reinterpret_cast<uintptr_t>(xor_out) & 3u) != 0)
+    return fail(PA_ERR_INVALID_ARG, "null or misaligned xor_out");
+  if (bytes % 16 != 0) return fail(PA_ERR_INVALID_ARG, "bytes %zu not a multiple of 16", bytes);
+  if (bytes > 0 && (!buf || !aligned16(buf)))
+    return fail(PA_ERR_INVALID_ARG, "null or misaligned buffer");
+  return from_cuda(pkv::launch_stream_read(buf, bytes, xor_out, reinterpret_cast<cudaStream_t>(stream)),
+                   "stream read launch");
+}
+
 pa_status pa_check_device_status(const int32_t* device_status, pa_stream_t stream) {
   if (!device_status) return fail(PA_ERR_INVALID_ARG, "null status pointer");
   int32_t word = 0;

@@ -21,6 +21,7 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value,
                                      cudaStream_t stream);
 
 cudaError_t launch_wait_timeout_selftest(int32_t* status, int32_t limit_ms, cudaStream_t stream);
+cudaError_t launch_stream_read(const void* buf, size_t bytes, uint32_t* x, cudaStream_t stream);
 
 cudaError_t launch_copy_blocks(void* key_cache, void* value_cache, const int64_t* block_mapping,
                                int32_t num_pairs, int32_t num_blocks, int32_t num_kv_heads,

@@ -82,6 +82,10 @@ def test_host_rejects_bad_arguments_without_touching_the_device():
                                 32, ctypes.c_float(0.125), None, None) == pa.PA_ERR_INVALID_ARG
     assert lib.pa_decode_workspace_size(2, 8, 24, 64, 0) == 0
     assert lib.pa_check_device_status(None, None) == pa.PA_ERR_INVALID_ARG
+    # stream read: null, misaligned, size not a multiple of 16
+    assert lib.pa_stream_read(None, 64, fake, None) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_stream_read(P(0x1008), 64, fake, None) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_stream_read(fake, 24, fake, None) == pa.PA_ERR_INVALID_ARG
 
 
 def test_build_targets_sm103a_only():
