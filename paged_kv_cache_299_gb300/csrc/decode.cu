@@ -48,7 +48,8 @@ constexpr int kMinTilesPerRun = 4;
 // (many pieces per segment) go to the parallel merge kernel.
 constexpr int kFusedMergeMaxContext = 8192;
 constexpr int kMaxSeqs = 4096;
-constexpr int kMergeThreads = 256;
+constexpr int kMergeThreads = 512;
+constexpr int kMergeUnroll = 4;  // partials whose loads one warp has in flight at once
 
 struct KParams {
   __nv_bfloat16* out;
@@ -835,7 +836,10 @@ merge_partials_kernel(const KParams p) {
     const int slot = k == 0 ? first_slot : 0;
     return p.partials + ((c * 2 + slot) * GROUP + h) * kPartialFloats;
   };
+  // With at least one tile per run (the usual case) no run is empty and the test is skipped.
+  const bool maybe_empty = total < p.grid;
   auto empty_run = [&](int k) -> bool {
+    if (!maybe_empty) return false;
     const int64_t c = c_first + k;
     return run_start(c, total, p.grid, p.chunk) == run_start(c + 1, total, p.grid, p.chunk);
   };
@@ -869,16 +873,38 @@ merge_partials_kernel(const KParams p) {
     acc[h] = make_float2(0.f, 0.f);
     lacc[h] = 0.f;
   }
-  for (int k = warp; k < n; k += kWarps) {
-    if (empty_run(k)) continue;
+  // Each warp takes kMergeUnroll partials per round and issues all their loads before
+  // combining them, so a round costs one memory latency.
+  for (int k0 = warp * kMergeUnroll; k0 < n; k0 += kWarps * kMergeUnroll) {
+    float mk[kMergeUnroll][GROUP], lk[kMergeUnroll][GROUP];
+    float2 vk[kMergeUnroll][GROUP];
 #pragma unroll
-    for (int h = 0; h < GROUP; ++h) {
-      const float* r = record(k, h);
-      const float wgt = fast_exp2(r[kHeadDim] - s_M[h]);
-      lacc[h] += wgt * r[kHeadDim + 1];
-      const float2 v = *reinterpret_cast<const float2*>(r + 2 * lane);
-      acc[h].x += wgt * v.x;
-      acc[h].y += wgt * v.y;
+    for (int u = 0; u < kMergeUnroll; ++u) {
+      const int k = k0 + u;
+      const bool use = k < n && !empty_run(k);
+#pragma unroll
+      for (int h = 0; h < GROUP; ++h) {
+        if (use) {
+          const float* r = record(k, h);
+          mk[u][h] = r[kHeadDim];
+          lk[u][h] = r[kHeadDim + 1];
+          vk[u][h] = *reinterpret_cast<const float2*>(r + 2 * lane);
+        } else {
+          mk[u][h] = -INFINITY;
+          lk[u][h] = 0.f;
+          vk[u][h] = make_float2(0.f, 0.f);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kMergeUnroll; ++u) {
+#pragma unroll
+      for (int h = 0; h < GROUP; ++h) {
+        const float wgt = fast_exp2(mk[u][h] - s_M[h]);  // 0 for unused slots (-inf)
+        lacc[h] += wgt * lk[u][h];
+        acc[h].x += wgt * vk[u][h].x;
+        acc[h].y += wgt * vk[u][h].y;
+      }
     }
   }
 #pragma unroll
