@@ -240,6 +240,29 @@ def test_split_segments_merged_in_kernel_and_workspace_reuse():
     assert_close(outs[0], ref["decode"], "long contexts, in-kernel merge")
 
 
+@pytest.mark.parametrize("partition_tokens", [16, 32])
+def test_merge_kernel_many_partials_and_workspace_reuse(partition_tokens):
+    """Short partitions of contexts up to 3000 tokens give segments of up to about 190
+    partials, and more runs than tiles (empty runs) for partitions of one tile; the merge
+    kernel combines them, and a reused workspace must give the same result."""
+    w = wl.make_workload("merge2", [2999, 40, 1777, 3000, 700, 1], [1, 1, 1, 1, 1, 1], seed=21,
+                         pool_slack=0.1)
+    step = GpuStep(w)
+    mx = int(w.context_lens.max())
+    need = pa.pa_decode_workspace_size(6, 8, 32, mx, partition_tokens)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(3):
+        out = torch.empty_like(step.vals["q_decode"])
+        pa.pa_decode(out, step.vals["q_decode"], step.kc, step.vc, step.bt, step.ctx, w.scale,
+                     mx, partition_tokens, workspace=ws, device_status=step.status)
+        outs.append(out)
+    assert step.check_status() == pa.PA_OK
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    ref = oracle_step(w, host_vals(step.vals))
+    assert_close(outs[0], ref["decode"], f"merge kernel, partitions of {partition_tokens}")
+
+
 def test_a_wait_that_runs_out_reports_timeout_and_leaves_the_context_usable():
     status = pa.new_device_status()
     pa.pa_selftest_wait_timeout(status, limit_ms=50)
