@@ -5,7 +5,7 @@ One step = one pass of the whole path over one batch: slot mapping of the step's
 tokens, then for every layer the KV store of the new tokens and paged attention (decode,
 plus causal chunked prefill where the workload has chunks).  The default workload is
 decode batch 256 with lognormal contexts (median 1024, sigma 0.8, clipped to [1, 8192])
-and 16 layers of KV pools resident; other workloads are reachable with --config.
+and 16 layers of KV pools resident; other workloads are reachable with --workload.
 
 Prints ONE JSON line (rank 0).  ``value`` is KV-read GB/s: the live K+V bytes the decode
 attention must read in a step (sum of context lengths x 2048 B x layers), divided by the
@@ -41,7 +41,9 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--workload", default="decode_b256",
+                    choices=["single_seq_300", "decode_b64", "decode_b256", "long_context_b4",
+                             "mixed_step"])
     ap.add_argument("--mixed", choices=["split", "unified"], default="split",
                     help="steps with prefill chunks and decode rows: pa_prefill_chunk + "
                          "pa_decode, or one pa_attention_varlen over all sequences")
@@ -61,7 +63,7 @@ def parse_args():
     return ap.parse_args()
 
 
-def ncu_traffic(cfg: int):
+def ncu_traffic(key: str):
     """DRAM bytes per decode launch from the committed ncu summary, if it was taken on
     this workload with the current decode source (else None)."""
     import hashlib
@@ -71,12 +73,12 @@ def ncu_traffic(cfg: int):
         digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
         fields = {}
         for line in open(summary):
-            if "=" in line and line.strip().startswith(("source_sha256", "config")):
-                k, v = line.split("=", 1)
+            k, eq, v = line.strip().partition("=")
+            if eq and (k.strip() == "source_sha256" or k.strip().endswith("_dram_bytes_per_launch")):
                 fields[k.strip()] = v.strip()
         if fields.get("source_sha256") != digest:
             return None
-        v = fields.get(f"config{cfg}_dram_bytes_per_launch")
+        v = fields.get(f"{key}_dram_bytes_per_launch")
         return int(v) if v else None
     except Exception:
         return None
@@ -117,9 +119,9 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def workload(cfg: int, layers=None, seed_offset=0):
+def workload(key: str, layers=None, seed_offset=0):
     from paged_kv_cache_299_gb300 import workloads as wl
-    make = wl.CONFIGS[cfg]
+    make = wl.WORKLOADS[key]
     w = make() if not seed_offset else make(seed=make().seed + seed_offset)
     if layers is not None:
         w.layers = int(layers)
@@ -387,7 +389,7 @@ def run_gpu(args, rank, world):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     # weak scaling: every rank serves its own batch (seed offset per rank)
-    w = workload(args.config, args.layers, 100 * rank if world > 1 else 0)
+    w = workload(args.workload, args.layers, 100 * rank if world > 1 else 0)
     st = DeviceStep(w, dev, fused_append=args.append == "fused", mixed=args.mixed)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     kv_bytes = w.decode_kv_bytes()
@@ -518,7 +520,7 @@ def run_gpu(args, rank, world):
         achieved = per_launch / (dec_ms * 1e-3) / 1e9
         res["roofline"] = {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.config),
+            "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload),
             "kernel": "pa_decode: paged_decode_kernel (split-KV merge in-kernel up to "
                       "8192-token contexts, else + merge_partials_kernel)",
             "peak_source": f"{peak_src} hbm_gbs", "pct_of_8tbs": round(100 * achieved / 8000, 2),
@@ -540,7 +542,7 @@ def run_gpu(args, rank, world):
                       "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
                       "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e["step_ms"], 4)}
     if not args.no_cpu_baseline and world == 1:
-        res["cpu_baseline"] = cpu_baseline(w, args.config, target_s=10.0)
+        res["cpu_baseline"] = cpu_baseline(w, target_s=10.0)
     print(json.dumps(res), flush=True)
 
 
@@ -692,7 +694,7 @@ def oracle_sample(w, max_seqs: int):
     return sw, step, sw.decode_kv_bytes()
 
 
-def cpu_baseline(w, cfg: int, target_s: float) -> dict:
+def cpu_baseline(w, target_s: float) -> dict:
     sw, step, kv = oracle_sample(w, 32)
     step()  # warm
     reps, t0 = 0, time.perf_counter()
@@ -713,7 +715,7 @@ def cpu_baseline(w, cfg: int, target_s: float) -> dict:
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    w = workload(args.config, args.layers)
+    w = workload(args.workload, args.layers)
     sw, step, kv = oracle_sample(w, 4)
     for _ in range(args.warmup):
         step()

@@ -174,41 +174,41 @@ def make_workload(name, hist_lens, new_lens, num_prefill=0, seed=0, pool_slack=0
                     block_tables=tables, seed=int(seed), layers=int(layers), **kw)
 
 
-# ---- the five workloads -------------------------------------------------------------
+# ---- the five workloads of the benchmark and the parity tests --------------------------
 
-def config1(seed=1001) -> Workload:
+def single_sequence_300(seed=1001) -> Workload:
     """One sequence of 300 tokens (19 blocks) at a seeded permutation of a 64-block pool;
     all 300 tokens are stored this step, then one decode query attends them."""
-    return make_workload("c1_single_seq_300", [0], [300], seed=seed, pool_blocks=64)
+    return make_workload("single_seq_300", [0], [300], seed=seed, pool_blocks=64)
 
 
-def config2(seed=1002) -> Workload:
+def decode_batch64_uniform(seed=1002) -> Workload:
     """Decode batch 64, contexts uniform in [128, 2048], pool = blocks needed + 10%."""
     rng = np.random.default_rng(seed)
     ctx = rng.integers(128, 2048, size=64, endpoint=True)
-    return make_workload("c2_decode_b64_u128_2048", ctx - 1, np.ones(64, np.int32),
+    return make_workload("decode_b64_u128_2048", ctx - 1, np.ones(64, np.int32),
                          seed=seed)
 
 
-def config3(seed=1003, layers=16) -> Workload:
+def decode_batch256_lognormal(seed=1003, layers=16) -> Workload:
     """Decode batch 256, contexts lognormal (median 1024, sigma 0.8) clipped to [1, 8192],
     16 layers of pools resident (one pool per layer, shared block tables)."""
     rng = np.random.default_rng(seed)
     z = rng.standard_normal(256)
     ctx = np.clip(np.round(np.exp(np.log(1024.0) + 0.8 * z)), 1, 8192).astype(np.int32)
-    return make_workload("c3_decode_b256_lognormal_16L", ctx - 1, np.ones(256, np.int32),
+    return make_workload("decode_b256_lognormal_16L", ctx - 1, np.ones(256, np.int32),
                          seed=seed, layers=layers)
 
 
-def config4(seed=1004) -> Workload:
+def long_context_batch4(seed=1004) -> Workload:
     """Long-context decode: 4 sequences of 131072 tokens, 1% of key vectors x8,
     split-KV partitions of 512 tokens."""
     ctx = np.full(4, 131072, dtype=np.int32)
-    return make_workload("c4_decode_b4_131072", ctx - 1, np.ones(4, np.int32), seed=seed,
+    return make_workload("decode_b4_131072", ctx - 1, np.ones(4, np.int32), seed=seed,
                          big_key_fraction=0.01, partition_tokens=512)
 
 
-def config5(seed=1005) -> Workload:
+def mixed_prefill_decode(seed=1005) -> Workload:
     """Mixed step: 8 prefill sequences append a 512-token causal chunk over 0..2048 prior
     tokens; 248 decode sequences with contexts uniform in [1, 4096]."""
     rng = np.random.default_rng(seed)
@@ -216,11 +216,14 @@ def config5(seed=1005) -> Workload:
     dctx = rng.integers(1, 4096, size=248, endpoint=True)
     hist = np.concatenate([prior, dctx - 1])
     new = np.concatenate([np.full(8, 512), np.ones(248)])
-    return make_workload("c5_mixed_8x512_prefill_248_decode", hist, new, num_prefill=8,
+    return make_workload("mixed_8x512_prefill_248_decode", hist, new, num_prefill=8,
                          seed=seed)
 
 
-CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}
+# by the short names bench.py takes (--workload)
+WORKLOADS = {"single_seq_300": single_sequence_300, "decode_b64": decode_batch64_uniform,
+             "decode_b256": decode_batch256_lognormal, "long_context_b4": long_context_batch4,
+             "mixed_step": mixed_prefill_decode}
 
 
 def random_small(seed, num_seqs=3, max_ctx=64, num_prefill=0, max_chunk=40,

@@ -16,7 +16,7 @@ def run(args, env_extra=None):
 
 
 def test_reference_arm_prints_the_contract_line():
-    res = run(["--impl", "reference", "--config", "1", "--steps", "2", "--warmup", "3"])
+    res = run(["--impl", "reference", "--workload", "single_seq_300", "--steps", "2", "--warmup", "3"])
     assert res.returncode == 0, res.stderr
     lines = [l for l in res.stdout.splitlines() if l.strip()]
     assert len(lines) == 1
@@ -29,11 +29,11 @@ def test_reference_arm_prints_the_contract_line():
     assert d["value"] > 0 and d["unit"] == "GB/s" and d["higher_is_better"] is True
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
-    assert d["config"]["workload"].startswith("c1_")
+    assert d["config"]["workload"] == "single_seq_300"
 
 
 def test_reference_arm_other_ranks_do_no_work():
-    res = run(["--impl", "reference", "--config", "1", "--steps", "1", "--warmup", "3"],
+    res = run(["--impl", "reference", "--workload", "single_seq_300", "--steps", "1", "--warmup", "3"],
               {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert res.returncode == 0, res.stderr
     assert res.stdout.strip() == ""

@@ -46,7 +46,7 @@ def test_fused_append_all_tail_lengths(partition_tokens):
 
 
 def test_fused_append_decode_batch64_against_oracle():
-    w = wl.config2()
+    w = wl.decode_batch64_uniform()
     step, out = both_paths(w)
     ref = oracle_step(w, host_vals(step.vals))
     mx, mean = errors(out.float().cpu().numpy(), ref["decode"])
@@ -54,4 +54,4 @@ def test_fused_append_decode_batch64_against_oracle():
 
 
 def test_fused_append_batch256_layer():
-    both_paths(wl.config3(layers=1))
+    both_paths(wl.decode_batch256_lognormal(layers=1))

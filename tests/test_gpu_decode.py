@@ -53,20 +53,20 @@ def test_every_tail_length():
 
 
 def test_config1_single_sequence():
-    full_check(wl.config1())
+    full_check(wl.single_sequence_300())
 
 
 def test_config2_decode_batch64():
-    full_check(wl.config2())
+    full_check(wl.decode_batch64_uniform())
 
 
 @pytest.mark.parametrize("layer", [0, 15])
 def test_config3_decode_batch256_layer(layer):
-    full_check(wl.config3(layers=16), layer=layer)
+    full_check(wl.decode_batch256_lognormal(layers=16), layer=layer)
 
 
 def test_config4_long_context_split512():
-    w = wl.config4()
+    w = wl.long_context_batch4()
     step = GpuStep(w)
     out = step.decode()  # partition_tokens = 512 from the workload
     assert step.check_status() == pa.PA_OK
@@ -77,7 +77,7 @@ def test_config4_long_context_split512():
 
 
 def test_config5_decode_part():
-    w = wl.config5()
+    w = wl.mixed_prefill_decode()
     step = GpuStep(w)
     out = step.decode()
     assert step.check_status() == pa.PA_OK

@@ -13,7 +13,7 @@ pytestmark = pytest.mark.gpu
 
 
 def test_captured_decode_step_replays_bit_identically():
-    w = wl.config2()
+    w = wl.decode_batch64_uniform()
     step = GpuStep(w, store_new=False)
     max_ctx = int(w.context_lens.max())
     need = pa.pa_decode_workspace_size(w.num_seqs, 8, 32, max_ctx, 0)

@@ -90,7 +90,7 @@ def test_config5_prefill_sampled_rows():
     """Mixed-step workload: 8 chunks of 512 over 0..2048 prior tokens.  Rows spread over
     every chunk (first, tile edges, last) are checked against the oracle's causal
     definition, each as one query over keys 0..pos."""
-    w = wl.config5()
+    w = wl.mixed_prefill_decode()
     step = GpuStep(w)
     out = step.prefill()
     assert step.check_status() == pa.PA_OK

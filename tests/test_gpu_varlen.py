@@ -65,7 +65,7 @@ def test_mixed_step_bit_identical_to_chunk_kernel():
     """The mixed continuous-batching step (8 chunks of 512 and 248 decode rows) in one
     varlen call equals pa_prefill_chunk on the same rows, and its decode rows agree with
     the decode kernel within the attention tolerance."""
-    w = wl.config5()
+    w = wl.mixed_prefill_decode()
     step = GpuStep(w)
     nd = w.num_decode
     qsl_pre = w.prefill_query_start_loc

@@ -23,7 +23,7 @@ def _rank_main(rank, world, port, results):
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
         import bench
-        w = bench.workload(3, layers=1, seed_offset=100 * rank)
+        w = bench.workload("decode_b256", layers=1, seed_offset=100 * rank)
         local_ms = 1.5 + rank  # rank 1 is slower
         step_ms = bench.max_over_ranks(local_ms, "cpu")
         lens = torch.from_numpy(w.context_lens.astype(np.int64))

@@ -27,7 +27,7 @@ def test_300_tokens_fill_19_blocks_and_leave_4_slots():
     """Store a 300-token sequence through the oracle: exactly 19 physical blocks are
     touched and exactly 4 slots (per head) of the last one keep their sentinel."""
     g = {r[0]: int(r[1]) for r in read_golden("block_arithmetic.txt")}
-    w = wl.config1()
+    w = wl.single_sequence_300()
     vals = w.values(0, "cpu")
     kc, vc = oracle_pools(w, vals)
     touched = ~np.all(kc == wl.NAN_BF16, axis=(1, 2, 3))

@@ -33,7 +33,7 @@ def _static_decode(step, partition_tokens):
 
 
 def test_static_scratch_matches_workspace_decode_on_two_calls_in_a_row():
-    a = GpuStep(wl.config2())                                  # 64 sequences, balanced split
+    a = GpuStep(wl.decode_batch64_uniform())                                  # 64 sequences, balanced split
     b = GpuStep(wl.random_small(17, num_seqs=9, max_ctx=700))  # ragged, fixed 64-token runs
     out_a = _static_decode(a, 0)
     out_b = _static_decode(b, 64)  # second call: reuses the scratch the first one wrote
