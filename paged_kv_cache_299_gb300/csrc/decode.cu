@@ -43,7 +43,7 @@ constexpr int kStagesPerWarp = 4;   // private ring depth: 16 KiB in flight per 
 constexpr int kWindow = 32;         // block-table entries fetched per window
 constexpr int kPartialFloats = kHeadDim + 2;  // o[64], max (log2 units), sum
 constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale when max grows > 2^8
-constexpr int kMinTilesPerRun = 4;
+constexpr int kMinTilesPerRun = 2;
 // Longest context whose split segments are merged inside the attention kernel; longer ones
 // (many pieces per segment) go to the parallel merge kernel.
 constexpr int kFusedMergeMaxContext = 8192;
