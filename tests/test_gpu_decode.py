@@ -220,6 +220,36 @@ def test_group_sizes_one_and_two():
         assert mx <= ATOL_MAX and mean <= ATOL_MEAN
 
 
+@pytest.mark.parametrize("partition_tokens", [0, 16, 512])
+def test_group_sizes_one_and_two_long_context(partition_tokens):
+    """Group sizes 1 and 2 over a 1500-token context: split segments merged in the attention
+    kernel (balanced runs) or, with partitions, by the merge kernel's GROUP 1 and 2 forms
+    (94 one-tile partials at 16 tokens), against SDPA in float64."""
+    for hq, hkv in ((8, 8), (16, 8)):
+        rng = np.random.default_rng(hq + partition_tokens)
+        L = 1500
+        nb = 110
+        table = rng.permutation(nb)[:94].astype(np.int32)[None]
+        k = torch.randn(L, hkv, 64, device="cuda").to(torch.bfloat16)
+        v = torch.randn(L, hkv, 64, device="cuda").to(torch.bfloat16)
+        q = torch.randn(1, hq, 64, device="cuda").to(torch.bfloat16)
+        kc = torch.full((nb, hkv, 16, 64), float("nan"), dtype=torch.bfloat16, device="cuda")
+        vc = kc.clone()
+        bt = i32(table)
+        ctx = i32([L])
+        status = pa.new_device_status()
+        slots = pa.pa_compute_slot_mapping(bt, ctx, i32([0, L]), L, kc, device_status=status)
+        pa.pa_reshape_and_cache(k, v, slots, kc, vc, device_status=status)
+        out = torch.empty_like(q)
+        pa.pa_decode(out, q, kc, vc, bt, ctx, 0.125, L, partition_tokens, device_status=status)
+        assert pa.pa_check_device_status(status) == pa.PA_OK
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            q.double().cpu()[:, :, None, :], k.double().cpu().transpose(0, 1)[None],
+            v.double().cpu().transpose(0, 1)[None], scale=0.125, enable_gqa=True)[0, :, 0, :]
+        mx, mean = errors(out.float().cpu().numpy()[0], ref.numpy())
+        assert mx <= ATOL_MAX and mean <= ATOL_MEAN, (hq, hkv, partition_tokens, mx, mean)
+
+
 def test_split_segments_merged_in_kernel_and_workspace_reuse():
     """Contexts up to 8192 tokens are split over many warps and merged inside the attention
     kernel through per-segment counters; a reused workspace must give the same result."""
