@@ -53,6 +53,11 @@ def parse_args():
     ap.add_argument("--launch", choices=["eager", "graph"], default="graph",
                     help="time the step as eager C-ABI calls or as one CUDA-graph replay")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernels-only", action="store_true",
+                    help="time only the standalone store and copy-on-write kernels (a short "
+                         "run for profilers) and print their figures")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the other workloads and the standalone store measurement")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--flush", choices=["write-read", "write"], default="write-read",
                     help="L2 flush between steps of workloads smaller than 4x L2: rewrite a "
@@ -63,22 +68,19 @@ def parse_args():
     return ap.parse_args()
 
 
-def ncu_traffic(key: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on
-    this workload with the current decode source (else None)."""
+def ncu_traffic(kernel: str, workload_key: str):
+    """DRAM bytes per launch of `kernel` on `workload_key` from the committed ncu figures in
+    profiles/dram_traffic.json, if they were taken with the kernel's current source (else
+    None: the counters no longer describe the kernel that runs)."""
     import hashlib
-    src = os.path.join(ROOT, "paged_kv_cache_299_gb300", "csrc", "decode.cu")
-    summary = os.path.join(ROOT, "profiles", "paged_decode_kernel.md")
     try:
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
-        fields = {}
-        for line in open(summary):
-            k, eq, v = line.strip().partition("=")
-            if eq and (k.strip() == "source_sha256" or k.strip().endswith("_dram_bytes_per_launch")):
-                fields[k.strip()] = v.strip()
-        if fields.get("source_sha256") != digest:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+            entry = json.load(f)[kernel]
+        with open(os.path.join(ROOT, entry["source"]), "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+        if entry["source_sha256"] != digest:
             return None
-        v = fields.get(f"{key}_dram_bytes_per_launch")
+        v = entry["workloads"].get(workload_key, {}).get("dram_bytes_per_launch")
         return int(v) if v else None
     except Exception:
         return None
@@ -159,7 +161,7 @@ class ClockSampler:
             self.file = tempfile.TemporaryFile(mode="w+")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.file, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -381,6 +383,115 @@ class DeviceStep:
                     dec_events[li][1].record()
 
 
+def make_flush(dev, kv_bytes: int, mode: str):
+    """L2 flush between steps for workloads smaller than 4x L2 (None for larger ones):
+    rewrite a buffer of twice the L2 size, then (write-read) read another one, so that the
+    dirty lines are written back before the step rather than during it."""
+    import torch
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    if kv_bytes >= 4 * l2:
+        return None
+    buf = torch.empty(2 * l2 // 4 + 1024, dtype=torch.int32, device=dev)
+    rd = torch.zeros(2 * l2 // 4 + 1024, dtype=torch.int32, device=dev) \
+        if mode == "write-read" else None
+
+    def flush_l2(k):
+        buf.fill_(k)
+        if rd is not None:
+            rd.sum()
+    return flush_l2
+
+
+def time_steps(st, dev, K: int, warmup: int, flush_l2, use_graph: bool, barrier=None,
+               sampler=None) -> dict:
+    """W untimed steps, then K timed steps (one CUDA-graph replay or eager C-ABI calls each,
+    events on the launching stream, L2 flushed before each when flush_l2 is given); then
+    per-kernel event times from an eager pass of min(K, 20) steps of the same workload."""
+    import torch
+    w = st.w
+    barrier = barrier or (lambda: None)
+    for _ in range(warmup):
+        st.step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    n_kernel = min(K, 20) if use_graph else K
+    mk = lambda: [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+    dec_ev = [[mk() for _ in range(w.layers)] for _ in range(K)]
+    pre_ev = [[mk() for _ in range(w.layers)] for _ in range(K)] \
+        if w.num_prefill and not st.unified else None
+    step_ev = [mk() for _ in range(K)]
+    if sampler is not None:
+        sampler.start()
+        time.sleep(0.3)
+    torch.cuda.synchronize(dev)
+    barrier()
+    graph = None
+    if use_graph:
+        from paged_kv_cache_299_gb300 import graphs
+        graph = graphs.StepGraph(st.step)
+    t_wall = time.perf_counter()
+    for k in range(K):
+        if flush_l2 is not None:
+            flush_l2(k)
+        step_ev[k][0].record()
+        if graph is not None:
+            graph.replay()
+        else:
+            st.step(dec_ev[k] if w.num_decode else None, pre_ev[k] if pre_ev else None)
+        step_ev[k][1].record()
+    torch.cuda.synchronize(dev)
+    if graph is not None:  # per-kernel timing: an eager pass right after, same workload
+        for k in range(n_kernel):
+            if flush_l2 is not None:
+                flush_l2(k)
+            st.step(dec_ev[k] if w.num_decode else None, pre_ev[k] if pre_ev else None)
+        torch.cuda.synchronize(dev)
+    barrier()
+    wall = time.perf_counter() - t_wall
+    res = {"step_ms": sum(a.elapsed_time(b) for a, b in step_ev) / K, "wall": wall,
+           "graph": graph, "clocks": None, "dec_ms": None, "pre_ms": None}
+    if w.num_decode:
+        res["dec_ms"] = sum(a.elapsed_time(b) for row in dec_ev[:n_kernel] for a, b in row) / (
+            n_kernel * w.layers)
+    if pre_ev:
+        res["pre_ms"] = sum(a.elapsed_time(b) for row in pre_ev[:n_kernel] for a, b in row) / (
+            n_kernel * w.layers)
+    return res
+
+
+def decode_roofline(st, workload_key: str, dec_ms: float, peak: float, peak_src: str) -> dict:
+    w = st.w
+    if st.unified:
+        # the varlen launch reads the K/V of every sequence of the step at least once
+        per_launch = float(np.sum(w.context_lens)) * w.num_kv_heads * w.head_dim * 2 * 2
+        achieved = per_launch / (dec_ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "kernel": "pa_attention_varlen: varlen_plan_kernel + paged_prefill_kernel "
+                          "(tcgen05) over the chunks and decode rows",
+                "peak_source": f"{peak_src} hbm_gbs", "launch_ms": round(dec_ms, 5),
+                "algorithmic_bytes_per_launch": int(per_launch)}
+    per_launch = w.decode_kv_bytes() / w.layers
+    achieved = per_launch / (dec_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": ncu_traffic("paged_decode_kernel", workload_key),
+            "kernel": "pa_decode: paged_decode_kernel (split-KV merge in-kernel up to "
+                      "8192-token contexts, else + merge_partials_kernel)",
+            "peak_source": f"{peak_src} hbm_gbs", "pct_of_8tbs": round(100 * achieved / 8000, 2),
+            "launch_ms": round(dec_ms, 5), "algorithmic_bytes_per_launch": int(per_launch)}
+
+
+def prefill_roofline(st, pre_ms: float) -> dict:
+    w = st.w
+    tfl = st.prefill_flops() / w.layers / (pre_ms * 1e-3) / 1e12
+    bf16_peak, bf16_src = measured_bf16_peak()
+    return {"bound": "tensor", "achieved": round(tfl, 1), "peak": bf16_peak, "unit": "TFLOP/s",
+            "frac": round(tfl / bf16_peak, 4), "kernel": "paged_prefill_kernel (tcgen05)",
+            "peak_source": f"{bf16_src} bf16_tflops_sustained", "launch_ms": round(pre_ms, 5),
+            "algorithmic_flops_per_launch": round(st.prefill_flops() / w.layers)}
+
+
 def run_gpu(args, rank, world):
     import torch
     import torch.distributed as dist
@@ -391,89 +502,33 @@ def run_gpu(args, rank, world):
     # weak scaling: every rank serves its own batch (seed offset per rank)
     w = workload(args.workload, args.layers, 100 * rank if world > 1 else 0)
     st = DeviceStep(w, dev, fused_append=args.append == "fused", mixed=args.mixed)
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     kv_bytes = w.decode_kv_bytes()
-    flush = kv_bytes < 4 * l2
-    flush_buf = torch.empty(2 * l2 // 4 + 1024, dtype=torch.int32, device=dev) if flush else None
-    flush_rd = (torch.zeros(2 * l2 // 4 + 1024, dtype=torch.int32, device=dev)
-                if flush and args.flush == "write-read" else None)
-
-    def flush_l2(k):
-        # rewrite a buffer of twice the L2 size; then read another one, so that the dirty
-        # lines are written back before the step rather than during it
-        flush_buf.fill_(k)
-        if flush_rd is not None:
-            flush_rd.sum()
+    flush_l2 = make_flush(dev, kv_bytes, args.flush)
 
     def barrier():
         if world > 1:
             dist.barrier()
 
-    for _ in range(args.warmup):
-        st.step()
-    torch.cuda.synchronize(dev)
-    barrier()
-
     K = args.steps
-    dec_ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-               for _ in range(w.layers)] for _ in range(K)]
-    step_ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-               for _ in range(K)]
-    pre_ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-               for _ in range(w.layers)] for _ in range(K)] if w.num_prefill and not st.unified \
-        else None
+    # clocks are sampled from just before the timed steps to the end of the end-to-end
+    # loop, so that short timed regions still get several samples under load
     sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
-    torch.cuda.synchronize(dev)
-    barrier()
-    graph = None
-    if args.launch == "graph":
-        from paged_kv_cache_299_gb300 import graphs
-        graph = graphs.StepGraph(st.step)
-    t_wall = time.perf_counter()
-    for k in range(K):
-        if flush:
-            flush_l2(k)
-        step_ev[k][0].record()
-        if graph is not None:
-            graph.replay()
-        else:
-            st.step(dec_ev[k] if w.num_decode else None, pre_ev[k] if pre_ev else None)
-        step_ev[k][1].record()
-    torch.cuda.synchronize(dev)
-    if graph is not None:  # per-kernel timing: an eager pass right after, same workload
-        for k in range(min(K, 20)):
-            if flush:
-                flush_l2(k)
-            st.step(dec_ev[k] if w.num_decode else None, pre_ev[k] if pre_ev else None)
-        torch.cuda.synchronize(dev)
-    barrier()
-    wall = time.perf_counter() - t_wall
-    clocks = sampler.stop()
+    t = time_steps(st, dev, K, args.warmup, flush_l2, args.launch == "graph", barrier, sampler)
+    graph = t["graph"]
     # the in-run read reference: one launch reading as many bytes as one decode launch,
     # under the same L2 rule, timed the same way
     stream_ref = None
     if w.num_decode and not st.unified:
-        stream_ref = measure_stream_read(dev, kv_bytes // w.layers, flush_l2 if flush else None,
-                                         max(3, min(K, 20)))
-    step_ms = sum(a.elapsed_time(b) for a, b in step_ev) / K
-    n_kernel_steps = min(K, 20) if graph is not None else K
-    dec_ms = None
-    if w.num_decode:
-        dec_ms = sum(a.elapsed_time(b) for row in dec_ev[:n_kernel_steps] for a, b in row) / (
-            n_kernel_steps * w.layers)
-    pre_ms = None
-    if pre_ev:
-        pre_ms = sum(a.elapsed_time(b) for row in pre_ev[:n_kernel_steps] for a, b in row) / (
-            n_kernel_steps * w.layers)
-    step_ms = max_over_ranks(step_ms, dev)
+        stream_ref = measure_stream_read(dev, kv_bytes // w.layers, flush_l2, max(3, min(K, 20)))
+    step_ms = max_over_ranks(t["step_ms"], dev)
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(st, max(3, min(K, 50)), dev, graph, flush_l2 if flush else None)
+        e2e = run_e2e(st, max(3, min(K, 50)), dev, graph, flush_l2)
         e2e["step_ms"] = max_over_ranks(e2e["step_ms"], dev)
+    t["clocks"] = dict(sampler.stop(), window="from the timed steps to the end of the "
+                                              "end-to-end loop")
 
     if rank != 0:
         return
@@ -488,7 +543,7 @@ def run_gpu(args, rank, world):
                        accumulate="f32",
                        l2=(("flushed between steps (2x L2 rewrite, then 2x L2 read)"
                             if args.flush == "write-read" else
-                            "flushed between steps (2x L2 rewrite)") if flush
+                            "flushed between steps (2x L2 rewrite)") if flush_l2
                            else "inputs larger than L2 (%.1f GB KV per step)" % (kv_bytes / 1e9)),
                        launch=("CUDA graph: one replay per step (kernel times from an "
                                "eager pass right after)" if graph is not None
@@ -501,49 +556,153 @@ def run_gpu(args, rank, world):
         "tokens_per_s": round(w.num_decode * world / (step_ms * 1e-3), 1),
         "pct_of_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "gpu_launches": st.launches_per_step() * K,
-        "wall_s_timed": round(wall, 3),
-        "clocks": clocks,
+        "wall_s_timed": round(t["wall"], 3),
+        "clocks": t["clocks"],
     }
-    if dec_ms and st.unified:
-        # the varlen launch reads the K/V of every sequence of the step at least once
-        per_launch = float(np.sum(w.context_lens)) * w.num_kv_heads * w.head_dim * 2 * 2
-        achieved = per_launch / (dec_ms * 1e-3) / 1e9
-        res["roofline"] = {
-            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": None,
-            "kernel": "pa_attention_varlen: varlen_plan_kernel + paged_prefill_kernel "
-                      "(tcgen05) over the chunks and decode rows",
-            "peak_source": f"{peak_src} hbm_gbs", "launch_ms": round(dec_ms, 5),
-            "algorithmic_bytes_per_launch": int(per_launch)}
-    elif dec_ms:
-        per_launch = kv_bytes / w.layers
-        achieved = per_launch / (dec_ms * 1e-3) / 1e9
-        res["roofline"] = {
-            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload),
-            "kernel": "pa_decode: paged_decode_kernel (split-KV merge in-kernel up to "
-                      "8192-token contexts, else + merge_partials_kernel)",
-            "peak_source": f"{peak_src} hbm_gbs", "pct_of_8tbs": round(100 * achieved / 8000, 2),
-            "launch_ms": round(dec_ms, 5), "algorithmic_bytes_per_launch": int(per_launch)}
+    if t["dec_ms"]:
+        res["roofline"] = decode_roofline(st, args.workload, t["dec_ms"], peak, peak_src)
     if stream_ref and "roofline" in res:
         res["roofline"]["stream_read"] = dict(
             stream_ref, decode_frac_of_stream=round(res["roofline"]["achieved"] /
                                                     stream_ref["achieved"], 4))
-    if pre_ms:
-        tfl = st.prefill_flops() / w.layers / (pre_ms * 1e-3) / 1e12
-        bf16_peak, bf16_src = measured_bf16_peak()
-        res["prefill_roofline"] = {
-            "bound": "tensor", "achieved": round(tfl, 1), "peak": bf16_peak, "unit": "TFLOP/s",
-            "frac": round(tfl / bf16_peak, 4), "kernel": "paged_prefill_kernel (tcgen05)",
-            "peak_source": f"{bf16_src} bf16_tflops_sustained", "launch_ms": round(pre_ms, 5),
-            "algorithmic_flops_per_launch": round(st.prefill_flops() / w.layers)}
+    if t["pre_ms"]:
+        res["prefill_roofline"] = prefill_roofline(st, t["pre_ms"])
     if e2e:
         res["e2e"] = {"value": round(whole_job_gbs(kv_bytes, world, e2e["step_ms"]), 1),
                       "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
                       "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e["step_ms"], 4)}
+    del st, graph, t
+    torch.cuda.empty_cache()
+    if not args.no_secondary and world == 1:
+        res["secondary"] = run_secondary(args, dev, local, peak, peak_src)
     if not args.no_cpu_baseline and world == 1:
         res["cpu_baseline"] = cpu_baseline(w, target_s=10.0)
+        res["cpu_baseline_all_cores"] = cpu_baseline_all_cores(w, target_s=10.0)
     print(json.dumps(res), flush=True)
+
+
+# The other workloads, measured in the same invocation with the same method (graph-replayed
+# step, eager per-kernel events, in-run stream read of one decode launch's bytes), and a
+# standalone KV store: (bench name, timed steps).
+SECONDARY = (("decode_b64", 100), ("long_context_b4", 30), ("mixed_step", 30))
+
+
+def run_secondary(args, dev, local: int, peak: float, peak_src: str) -> dict:
+    import torch
+    out = {}
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.2)
+    for key, K in SECONDARY:
+        if key == args.workload:
+            continue
+        w = workload(key)
+        st = DeviceStep(w, dev, fused_append=True, mixed="split")
+        kv = w.decode_kv_bytes()
+        flush_l2 = make_flush(dev, kv, "write-read")
+        t = time_steps(st, dev, K, 3, flush_l2, True)
+        d = {"kv_read_bytes_per_step": kv, "steps": K, "ms_per_step": round(t["step_ms"], 5),
+             "step_gbs": round(kv / (t["step_ms"] * 1e-3) / 1e9, 1),
+             "step_pct_of_8tbs": round(100 * kv / (t["step_ms"] * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 2),
+             "l2": "flushed between steps" if flush_l2 else "inputs larger than L2",
+             "store": ("fused into decode (pa_decode_append)" if st.fused_append
+                       else "pa_compute_slot_mapping + pa_reshape_and_cache")}
+        if t["dec_ms"]:
+            d["roofline"] = decode_roofline(st, key, t["dec_ms"], peak, peak_src)
+            sr = measure_stream_read(dev, kv // w.layers, flush_l2, 20)
+            d["roofline"]["stream_read"] = dict(
+                sr, decode_frac_of_stream=round(d["roofline"]["achieved"] / sr["achieved"], 4))
+        if t["pre_ms"]:
+            d["prefill_roofline"] = prefill_roofline(st, t["pre_ms"])
+        out[key] = d
+        del st, t
+        torch.cuda.empty_cache()
+    out["reshape_and_cache"] = measure_store(dev, peak, peak_src)
+    out["copy_blocks"] = measure_copy_blocks(dev, peak, peak_src)
+    out["clocks"] = sampler.stop()
+    return out
+
+
+def _event_ms(dev, fn, reps: int, flush_l2=None) -> float:
+    """Mean CUDA-event time of fn() over reps launches (3 untimed first)."""
+    import torch
+    for _ in range(3):
+        fn()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    for i, (a, b) in enumerate(evs):
+        if flush_l2 is not None:
+            flush_l2(i)
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize(dev)
+    return sum(a.elapsed_time(b) for a, b in evs) / reps
+
+
+def measure_copy_blocks(dev, peak: float, peak_src: str, pairs: int = 8192) -> dict:
+    """pa_copy_blocks alone: `pairs` copy-on-write block copies (source and destination
+    blocks drawn without replacement from a shuffled pool of 2 x pairs + 10 % blocks).
+    Algorithmic bytes per pair: the K and V blocks (8 heads x 16 x 64 bf16 = 16 KiB each)
+    read and written, 64 KiB."""
+    import torch
+    from paged_kv_cache_299_gb300 import binding as pa
+    nb = int(2 * pairs * 1.1)
+    perm = np.random.default_rng(88).permutation(nb)[: 2 * pairs].astype(np.int64)
+    mapping = torch.from_numpy(perm.reshape(pairs, 2)).to(dev)
+    shape = (nb, 8, 16, 64)
+    kc = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+    nbytes = pairs * 4 * 8 * 16 * 64 * 2
+    flush_l2 = make_flush(dev, nbytes, "write-read")
+    ms = _event_ms(dev, lambda: pa.pa_copy_blocks(kc, vc, mapping), 50, flush_l2)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del kc, vc
+    torch.cuda.empty_cache()
+    return {"pairs": pairs, "algorithmic_bytes_per_launch": nbytes, "launch_ms": round(ms, 5),
+            "achieved": round(gbs, 1), "unit": "GB/s", "frac": round(gbs / peak, 4),
+            "peak_source": f"{peak_src} hbm_gbs", "pct_of_8tbs": round(100 * gbs / NOMINAL_HBM_GBS, 2),
+            "traffic": ncu_traffic("copy_blocks_kernel", f"pairs_{pairs}"),
+            "l2": "flushed before each launch" if flush_l2 else "inputs larger than L2"}
+
+
+def measure_store(dev, peak: float, peak_src: str) -> dict:
+    """pa_reshape_and_cache alone, CUDA events per launch: the mixed step's 4344 new tokens
+    (the largest per-step store of the workloads; L2 flushed before each launch) and a bulk
+    store of 65536 tokens (8 prompts of 8192, e.g. a large prefill).  Algorithmic bytes per
+    token: 2 x 1024 B read (K and V rows of 8 heads) + 2 x 1024 B written."""
+    import torch
+    from paged_kv_cache_299_gb300 import binding as pa
+    from paged_kv_cache_299_gb300 import workloads as wl
+    res = {}
+    cases = (("mixed_step_4344_tokens", wl.mixed_prefill_decode()),
+             ("bulk_65536_tokens", wl.make_workload("bulk_store", [0] * 8, [8192] * 8,
+                                                    num_prefill=8, seed=77)))
+    for name, w in cases:
+        vals = w.values(0, dev)
+        k, v = vals["new_k"], vals["new_v"]
+        del vals
+        shape = (w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim)
+        kc = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+        vc = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+        bt = torch.from_numpy(w.block_tables).to(dev)
+        ctx = torch.from_numpy(w.context_lens).to(dev)
+        qsl = torch.from_numpy(w.new_start_loc).to(dev)
+        n = int(w.new_lens.sum())
+        slots = pa.pa_compute_slot_mapping(bt, ctx, qsl, n, kc)
+        nbytes = n * w.num_kv_heads * w.head_dim * 2 * 2 * 2
+        flush_l2 = make_flush(dev, nbytes, "write-read")
+        ms = _event_ms(dev, lambda: pa.pa_reshape_and_cache(k, v, slots, kc, vc), 50, flush_l2)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[name] = {"tokens": n, "algorithmic_bytes_per_launch": nbytes,
+                     "launch_ms": round(ms, 5), "achieved": round(gbs, 1), "unit": "GB/s",
+                     "frac": round(gbs / peak, 4), "peak_source": f"{peak_src} hbm_gbs",
+                     "pct_of_8tbs": round(100 * gbs / NOMINAL_HBM_GBS, 2),
+                     "traffic": ncu_traffic("reshape_and_cache_kernel", name),
+                     "l2": "flushed before each launch" if flush_l2 else "inputs larger than L2"}
+        del k, v, kc, vc, slots
+        torch.cuda.empty_cache()
+    return res
 
 
 def measure_stream_read(dev, nbytes: int, flush_l2, reps: int) -> dict:
@@ -662,9 +821,14 @@ def run_e2e(st: DeviceStep, steps: int, dev, graph=None, flush_l2=None) -> dict:
 # ----------------------------------------------------------------------------------------
 # the CPU oracle (baseline leg and --impl reference)
 # ----------------------------------------------------------------------------------------
-def oracle_sample(w, max_seqs: int):
+def oracle_sample(w, max_seqs: int, threads: int = 1):
     """A bounded sample of the workload: its first sequences (same length law), one layer,
-    drawn on the host; returns a callable doing one oracle step and its KV bytes."""
+    drawn on the host; returns a callable doing one oracle step and its KV bytes.  With
+    threads > 1 the step's attention runs on that many host threads, each over a disjoint
+    slice of the sequences (the oracle itself is unchanged: ctypes releases the GIL during
+    each call and the oracle keeps no shared state)."""
+    import concurrent.futures as cf
+
     import oracle
     from paged_kv_cache_299_gb300 import workloads as wl
 
@@ -680,22 +844,42 @@ def oracle_sample(w, max_seqs: int):
                              kc, vc)
     new_k, new_v = wl.bf16_bits(vals["new_k"]), wl.bf16_bits(vals["new_v"])
     qd, qp = wl.bf16_bits(vals["q_decode"]), wl.bf16_bits(vals["q_prefill"])
+    dbt, dctx = sw.decode_block_tables, sw.decode_context_lens
+    qsl = sw.prefill_query_start_loc
+    pool = cf.ThreadPoolExecutor(max_workers=threads) if threads > 1 else None
+    # units of work: one per prefill sequence, and decode slices of about equal size
+    nd = sw.num_decode
+    per = max(1, -(-nd // (4 * threads))) if nd else 1
+
+    def prefill_one(s):
+        oracle.prefill_chunk(qp[qsl[s]:qsl[s + 1]], np.array([0, qsl[s + 1] - qsl[s]], np.int32),
+                             kc, vc, sw.block_tables[s:s + 1], sw.context_lens[s:s + 1], sw.scale)
+
+    def decode_slice(a):
+        b = min(nd, a + per)
+        oracle.decode(qd[a:b], kc, vc, dbt[a:b], dctx[a:b], sw.scale)
 
     def step():
         slots, _ = oracle.slot_mapping(sw.block_tables, sw.context_lens, sw.new_start_loc,
                                        sw.num_blocks)
         oracle.reshape_and_cache(new_k, new_v, slots, kc, vc)
-        if sw.num_prefill:
-            oracle.prefill_chunk(qp, sw.prefill_query_start_loc, kc, vc,
-                                 sw.block_tables[:npre], sw.context_lens[:npre], sw.scale)
-        if sw.num_decode:
-            oracle.decode(qd, kc, vc, sw.decode_block_tables, sw.decode_context_lens, sw.scale)
+        if pool is None:
+            if sw.num_prefill:
+                oracle.prefill_chunk(qp, qsl, kc, vc, sw.block_tables[:npre],
+                                     sw.context_lens[:npre], sw.scale)
+            if nd:
+                oracle.decode(qd, kc, vc, dbt, dctx, sw.scale)
+            return
+        futs = [pool.submit(prefill_one, s) for s in range(sw.num_prefill)]
+        futs += [pool.submit(decode_slice, a) for a in range(0, nd, per)]
+        for f in futs:
+            f.result()
 
     return sw, step, sw.decode_kv_bytes()
 
 
-def cpu_baseline(w, target_s: float) -> dict:
-    sw, step, kv = oracle_sample(w, 32)
+def _timed_oracle(w, max_seqs: int, threads: int, target_s: float):
+    sw, step, kv = oracle_sample(w, max_seqs, threads)
     step()  # warm
     reps, t0 = 0, time.perf_counter()
     while True:
@@ -704,11 +888,29 @@ def cpu_baseline(w, target_s: float) -> dict:
         el = time.perf_counter() - t0
         if el >= target_s:
             break
-    gbs = kv * reps / el / 1e9
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+    return sw, kv, reps, el
+
+
+def cpu_baseline(w, target_s: float) -> dict:
+    """The oracle as written: one host thread."""
+    sw, kv, reps, el = _timed_oracle(w, 32, 1, target_s)
+    return {"value": round(kv * reps / el / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"one layer of the first {sw.num_seqs} sequences of {w.name} "
                       f"({int(sw.context_lens.sum())} cached tokens), {reps} repetitions, "
                       f"{el:.1f} s single-threaded",
+            "tokens_per_s": round(sw.num_decode * reps / el, 3)}
+
+
+def cpu_baseline_all_cores(w, target_s: float) -> dict:
+    """The same oracle on every host core: the step's sequences split over os.cpu_count()
+    threads (disjoint slices, no shared state)."""
+    cores = os.cpu_count() or 1
+    sw, kv, reps, el = _timed_oracle(w, 256, cores, target_s)
+    return {"value": round(kv * reps / el / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"one layer of the first {sw.num_seqs} sequences of {w.name} "
+                      f"({int(sw.context_lens.sum())} cached tokens), {reps} repetitions, "
+                      f"{el:.1f} s on {cores} threads (disjoint sequence slices)",
             "tokens_per_s": round(sw.num_decode * reps / el, 3)}
 
 
@@ -716,7 +918,8 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     w = workload(args.workload, args.layers)
-    sw, step, kv = oracle_sample(w, 4)
+    cores = os.cpu_count() or 1
+    sw, step, kv = oracle_sample(w, 64, cores)
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
@@ -731,21 +934,50 @@ def run_reference(args, rank, world):
         "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": describe(w),
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle",
                          "sample": f"each step: one layer of the first {sw.num_seqs} sequences "
-                                   f"of {w.name} ({int(sw.context_lens.sum())} cached tokens)"},
+                                   f"of {w.name} ({int(sw.context_lens.sum())} cached tokens), "
+                                   f"on {cores} host threads (disjoint sequence slices)"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(res), flush=True)
 
 
+def relaunch_with_torchrun(args_list, n: int) -> int:
+    """`bench.py --gpus N` started as one process: run it as N ranks on this node (one per
+    GPU) under torch.distributed.run, as the multi-GPU contract launches it."""
+    import socket
+    sock = socket.socket()
+    sock.bind(("127.0.0.1", 0))
+    port = sock.getsockname()[1]
+    sock.close()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.abspath(__file__), *args_list]
+    return subprocess.call(cmd)
+
+
 def main():
     args = parse_args()
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        sys.exit(relaunch_with_torchrun(sys.argv[1:], args.gpus))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.gpus != world:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
+        sys.exit(2)
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.kernels_only:
+        import torch
+        dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+        torch.cuda.set_device(dev)
+        peak, peak_src = measured_peaks()
+        print(json.dumps({"reshape_and_cache": measure_store(dev, peak, peak_src),
+                          "copy_blocks": measure_copy_blocks(dev, peak, peak_src)}), flush=True)
         return
     if world > 1:
         import torch.distributed as dist

@@ -106,9 +106,11 @@ pa_status pa_reshape_and_cache(const void* key, const void* value,
 /* Bytes of device workspace pa_decode needs for these sizes on the current device
  * (0 when the sizes are invalid).  The workspace holds the split-KV partial results, the
  * per-sequence block offsets and one piece counter per (sequence, kv head).  Zero-fill it
- * once before its first use; every completed call leaves the counters at zero again, so
- * the same buffer can be reused call after call (zero it again after a call that reported
- * a device-side error). */
+ * once before its first use.  Every call whose kernels run to the end leaves the counters
+ * at zero again, including calls that report a device-side error through device_status
+ * (bad block id, bad context, timeout: the affected pieces are still counted), so the same
+ * buffer is reused call after call without clearing.  Only a CUDA error that ends a kernel
+ * early (the context is then unusable) leaves the counters undefined. */
 size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_heads,
                                 int32_t max_context_len, int32_t partition_tokens);
 
@@ -213,17 +215,22 @@ pa_status pa_attention_varlen(void* out, const void* q, const int32_t* query_sta
  * the process exits.
  *   - Sizes whose pa_decode_workspace_size() exceeds that limit are rejected with
  *     PA_ERR_WORKSPACE before anything is launched (pa_last_error() names both sizes).
- *     Balanced splits (partition_tokens 0) fit for every supported sequence count;
- *     short fixed partitions over very long contexts may not.
- *   - The first call on a device looks up the array's device address (once per device,
- *     with that device current); make that first call before any stream capture.
+ *     Balanced splits (partition_tokens 0) need about 2.1 KB per streaming warp of the
+ *     device (12 per SM) plus the offsets and counters: for up to 4096 sequences and any
+ *     supported head counts they fit on GPUs of up to 280 SMs (a GB300 has 152).  Short
+ *     fixed partitions over very long contexts may not fit.
+ *   - The first call on a device looks up the array's device address with that device
+ *     current, and again whenever the device's CUDA context has changed (for example after
+ *     cudaDeviceReset); make the first call on a device before any stream capture.  A
+ *     failed lookup is reported (PA_ERR_CUDA) and retried by the next call.
  *   - All calls share the array and it keeps the last call's contents.  The only part
  *     that must start at zero, the per-segment piece counters, is zero when the library
- *     loads and every completed call leaves it at zero; everything else is written before
- *     it is read.  Calls that can overlap on the GPU (different streams, or different host
- *     threads) race on the array: order them on one stream.
+ *     loads, and every call whose kernels run to the end leaves it at zero, including
+ *     calls that report a device-side error through device_status; everything else is
+ *     written before it is read.  Calls that can overlap on the GPU (different streams,
+ *     or different host threads) race on the array: order them on one stream.
  *   - No allocation of any kind happens inside this call. */
-#define PA_DECODE_STATIC_SCRATCH_BYTES ((size_t)4 << 20)
+#define PA_DECODE_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
 pa_status pa_decode_static_scratch(void* out, const void* q, const void* key_cache,
                                    const void* value_cache, pa_cache_desc cd,
                                    const int32_t* block_tables, int32_t max_blocks_per_seq,

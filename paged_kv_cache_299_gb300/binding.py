@@ -38,6 +38,8 @@ PA_ERR_DEVICE_INDEX = -5
 PA_ERR_DEVICE_TIMEOUT = -6
 PA_ERR_OUT_OF_BLOCKS = -7
 DEVFLAG_BAD_BLOCK, DEVFLAG_BAD_SLOT, DEVFLAG_BAD_CONTEXT, DEVFLAG_TIMEOUT = 1, 2, 4, 8
+# Size of the library-owned device scratch of pa_decode_static_scratch (bytes).
+PA_DECODE_STATIC_SCRATCH_BYTES = 8 << 20
 
 # Every symbol include/pagedkv.h declares.
 EXPORTED = ("pa_compute_slot_mapping", "pa_reshape_and_cache", "pa_decode_workspace_size",

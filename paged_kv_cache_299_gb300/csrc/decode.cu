@@ -682,6 +682,12 @@ paged_decode_kernel(const KParams p) {
             uint8_t* pool = lane < 8 ? p.key_cache_w : p.value_cache_w;
             *reinterpret_cast<uint4*>(pool + static_cast<size_t>(t) * kTileBytes + off) = new_row;
           }
+          // This stage is refilled by a bulk copy (async proxy) after the tile is consumed.
+          // A generic-proxy write followed by an async-proxy write to the same shared memory
+          // is ordered only through a proxy fence: without it the new row could land after
+          // the refill and corrupt the next tile.  (Plain reads need no fence: their values
+          // have been consumed before the warp barrier that precedes the refill.)
+          fence_proxy_async_smem();
         }
         __syncwarp();
       }

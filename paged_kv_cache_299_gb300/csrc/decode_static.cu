@@ -1,6 +1,7 @@
 // pa_decode_static_scratch: paged decode attention for callers that cannot allocate device
 // memory.  It runs the same kernels as pa_decode; only the workspace differs: here it is
 // one library-owned array in device global memory, sized at compile time.
+#include <cuda.h>
 #include <mutex>
 #include <stdio.h>
 
@@ -17,14 +18,43 @@ constexpr size_t kScratchBytes = PA_DECODE_STATIC_SCRATCH_BYTES;
 constexpr int kMaxDevices = 64;
 
 // The scratch itself.  In host code this name only stands in for the array: its device
-// address comes from cudaGetSymbolAddress, looked up once per device below.
+// address comes from cudaGetSymbolAddress, looked up per device (and context) below.
 static __device__ __align__(256) uint8_t g_decode_scratch[kScratchBytes];
 
-std::once_flag g_setup_once[kMaxDevices];
-void* g_scratch_addr[kMaxDevices] = {};
-cudaError_t g_setup_status[kMaxDevices] = {};
+// Address cache, one entry per device index.  An entry is valid for the CUDA context it
+// was looked up in: after cudaDeviceReset the primary context is a new one and the address
+// is looked up again.  A failed lookup is not cached, so a later call retries it.
+struct ScratchEntry {
+  CUcontext ctx = nullptr;
+  void* addr = nullptr;
+};
+std::mutex g_mutex;
+ScratchEntry g_entry[kMaxDevices];
 
-// Device address of the scratch on the current device (set up on first use).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = []() -> CtxGetCurrentFn {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<CtxGetCurrentFn>(ptr);
+    return nullptr;
+  }();
+  return fn;
+}
+
+CUcontext current_context() {
+  CUcontext ctx = nullptr;
+  const CtxGetCurrentFn fn = ctx_get_current();
+  if (fn == nullptr || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+  return ctx;
+}
+
+// Device address of the scratch on the current device, looked up with that device current
+// the first time a context is seen (cudaGetSymbolAddress allocates nothing).
 pa_status scratch_on_current_device(void** addr) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
@@ -35,18 +65,26 @@ pa_status scratch_on_current_device(void** addr) {
     return pkv::record_error(PA_ERR_UNSUPPORTED,
                              "pa_decode_static_scratch: device index beyond 63");
   }
-  std::call_once(g_setup_once[dev], [dev]() {
-    void* p = nullptr;
-    g_setup_status[dev] = cudaGetSymbolAddress(&p, g_decode_scratch);
-    g_scratch_addr[dev] = p;
-  });
-  if (g_setup_status[dev] != cudaSuccess || g_scratch_addr[dev] == nullptr) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  ScratchEntry& ent = g_entry[dev];
+  const CUcontext ctx = current_context();
+  if (ctx != nullptr && ctx == ent.ctx && ent.addr != nullptr) {
+    *addr = ent.addr;
+    return PA_OK;
+  }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_decode_scratch);
+  if (e != cudaSuccess || p == nullptr) {
+    ent = ScratchEntry{};
     char msg[200];
     snprintf(msg, sizeof msg, "pa_decode_static_scratch: scratch address lookup failed: %s",
-             cudaGetErrorString(g_setup_status[dev]));
+             cudaGetErrorString(e));
     return pkv::record_error(PA_ERR_CUDA, msg);
   }
-  *addr = g_scratch_addr[dev];
+  // The lookup makes the device's primary context current if it was not yet.
+  ent.ctx = ctx != nullptr ? ctx : current_context();
+  ent.addr = p;
+  *addr = p;
   return PA_OK;
 }
 

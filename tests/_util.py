@@ -73,3 +73,59 @@ def errors(got, ref):
     ref = np.asarray(ref, dtype=np.float64)
     diff = np.abs(got - ref)
     return float(diff.max()) if diff.size else 0.0, float(diff.mean()) if diff.size else 0.0
+
+
+def oracle_prefill_rows(q_bits, query_start_loc, key_cache, value_cache, block_tables,
+                        context_lens, scale, rows_per_task=128):
+    """The oracle's causal chunk attention (pko_prefill_chunk) of every row, with the rows
+    split into ranges that run on all host threads (ctypes releases the GIL during each
+    call; the oracle keeps no shared state).  Rows [a, b) of a chunk of q_len rows over L
+    keys are themselves the chunk of b - a rows over the first L - q_len + b keys: row i
+    sits at position L - q_len + i either way.  Returns float64 [rows, Hq, D]."""
+    import concurrent.futures as cf
+
+    qsl = np.asarray(query_start_loc, dtype=np.int64)
+    ctx = np.asarray(context_lens, dtype=np.int64)
+    tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    out = np.zeros(q_bits.shape, dtype=np.float64)
+    tasks = []
+    for s in range(len(qsl) - 1):
+        q0, q1 = int(qsl[s]), int(qsl[s + 1])
+        q_len, L = q1 - q0, int(ctx[s])
+        for a in range(0, q_len, rows_per_task):
+            b = min(q_len, a + rows_per_task)
+            tasks.append((s, q0 + a, q0 + b, L - q_len + b))
+
+    def run(task):
+        s, r0, r1, keys = task
+        o, err = oracle.prefill_chunk(q_bits[r0:r1], np.array([0, r1 - r0], np.int32),
+                                      key_cache, value_cache, tables[s:s + 1],
+                                      np.array([keys], np.int32), scale)
+        assert err == 0, task
+        out[r0:r1] = o
+
+    with cf.ThreadPoolExecutor(max_workers=os.cpu_count() or 1) as ex:
+        list(ex.map(run, tasks))
+    return out
+
+
+def oracle_decode_rows(q_bits, key_cache, value_cache, block_tables, context_lens, scale,
+                       seqs_per_task=8):
+    """The oracle's decode attention (pko_decode) of every sequence, slices of sequences
+    run on all host threads.  Returns float64 [S, Hq, D]."""
+    import concurrent.futures as cf
+
+    tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+    out = np.zeros(q_bits.shape, dtype=np.float64)
+
+    def run(a):
+        b = min(len(ctx), a + seqs_per_task)
+        o, err = oracle.decode(q_bits[a:b], key_cache, value_cache, tables[a:b], ctx[a:b],
+                               scale)
+        assert err == 0, a
+        out[a:b] = o
+
+    with cf.ThreadPoolExecutor(max_workers=os.cpu_count() or 1) as ex:
+        list(ex.map(run, range(0, len(ctx), seqs_per_task)))
+    return out

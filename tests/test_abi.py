@@ -119,3 +119,10 @@ def test_varlen_workspace_size_and_host_checks():
     empty = list(args)
     empty[11] = 0
     assert lib.pa_attention_varlen(*empty, None, 0, None, None) == pa.PA_OK
+
+
+def test_static_scratch_size_matches_the_header():
+    text = open(HEADER).read()
+    m = re.search(r"#define PA_DECODE_STATIC_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)", text)
+    assert m, "PA_DECODE_STATIC_SCRATCH_BYTES not found in the header"
+    assert int(m.group(1)) << int(m.group(2)) == pa.PA_DECODE_STATIC_SCRATCH_BYTES

@@ -27,13 +27,35 @@ def test_reference_arm_prints_the_contract_line():
         assert key in d, key
     assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 3
     assert d["value"] > 0 and d["unit"] == "GB/s" and d["higher_is_better"] is True
-    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle"
+    assert d["cpu_baseline"]["cores"] == (os.cpu_count() or 1)
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
     assert d["config"]["workload"] == "single_seq_300"
 
 
 def test_reference_arm_other_ranks_do_no_work():
-    res = run(["--impl", "reference", "--workload", "single_seq_300", "--steps", "1", "--warmup", "3"],
-              {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    res = run(["--impl", "reference", "--workload", "single_seq_300", "--steps", "1", "--warmup", "3",
+               "--gpus", "2"], {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert res.returncode == 0, res.stderr
     assert res.stdout.strip() == ""
+
+
+def test_gpus_flag_disagreeing_with_the_launch_is_refused():
+    res = run(["--impl", "reference", "--workload", "single_seq_300", "--steps", "1",
+               "--gpus", "3"], {"RANK": "0", "WORLD_SIZE": "2", "LOCAL_RANK": "0"})
+    assert res.returncode == 2 and "--gpus 3" in res.stderr
+
+
+def test_gpus_flag_alone_starts_one_rank_per_gpu():
+    """`bench.py --gpus 2` started as a single process relaunches itself as two ranks under
+    torch.distributed.run; rank 0 alone prints the line, which reports n_gpus 2."""
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", "single_seq_300", "--steps", "1", "--warmup", "3",
+                          "--gpus", "2"], cwd=ROOT, capture_output=True, text=True, timeout=300,
+                         env=env)
+    assert res.returncode == 0, res.stderr
+    lines = [l for l in res.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1
+    assert json.loads(lines[0])["n_gpus"] == 2

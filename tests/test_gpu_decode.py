@@ -70,7 +70,14 @@ def test_config4_long_context_split512():
     step = GpuStep(w)
     out = step.decode()  # partition_tokens = 512 from the workload
     assert step.check_status() == pa.PA_OK
-    ref = oracle_step(w, host_vals(step.vals))
+    hv = host_vals(step.vals)
+    ref = oracle_step(w, hv)
+    # slot mapping and store of the 4 x 131072 tokens: bit-exact, NaN sentinels included
+    s_ref, err = oracle.slot_mapping(w.block_tables, w.context_lens, w.new_start_loc,
+                                     w.num_blocks)
+    assert err == 0 and np.array_equal(step.new_slots.cpu().numpy(), s_ref)
+    assert np.array_equal(bits(step.kc), ref["kc"]), "key pool differs from the oracle's"
+    assert np.array_equal(bits(step.vc), ref["vc"]), "value pool differs from the oracle's"
     assert_close(out, ref["decode"], "config 4 decode")
     out_auto = step.decode(0)
     assert_close(out_auto, ref["decode"], "config 4 decode, balanced split")

@@ -8,7 +8,7 @@ import oracle
 from paged_kv_cache_299_gb300 import binding as pa
 from paged_kv_cache_299_gb300 import workloads as wl
 from _gpu import GpuStep, host_vals, i32, oracle_step
-from _util import ATOL_MAX, ATOL_MEAN, errors, oracle_pools
+from _util import ATOL_MAX, ATOL_MEAN, errors, oracle_pools, oracle_prefill_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -86,29 +86,21 @@ def test_last_chunk_row_matches_decode_kernel():
     assert (out[-1].float() - dec[0].float()).abs().max().item() <= 1.6e-2
 
 
-def test_config5_prefill_sampled_rows():
-    """Mixed-step workload: 8 chunks of 512 over 0..2048 prior tokens.  Rows spread over
-    every chunk (first, tile edges, last) are checked against the oracle's causal
-    definition, each as one query over keys 0..pos."""
+def test_config5_prefill_every_row():
+    """Mixed-step workload: 8 chunks of 512 over 0..2048 prior tokens.  Every row of every
+    chunk (all 16 query tiles of each), all 32 heads, element by element against the
+    oracle's causal chunk attention."""
     w = wl.mixed_prefill_decode()
     step = GpuStep(w)
     out = step.prefill()
     assert step.check_status() == pa.PA_OK
     hv = host_vals(step.vals)
     kc, vc = oracle_pools(w, hv)
-    qsl = w.prefill_query_start_loc
-    rows, ctx, tables = [], [], []
-    for s in range(w.num_prefill):
-        L = int(w.context_lens[s])
-        q_len = int(qsl[s + 1] - qsl[s])
-        for i in (0, 1, 31, 32, 33, 127, 128, 255, 300, 447, 510, 511):
-            rows.append(qsl[s] + i)
-            ctx.append(L - q_len + i + 1)
-            tables.append(w.block_tables[s])
-    q = wl.bf16_bits(hv["q_prefill"])[rows]
-    ref, err = oracle.decode(q, kc, vc, np.stack(tables), np.array(ctx, np.int32), w.scale)
-    assert err == 0
-    check(out[torch.tensor(rows, device="cuda")], ref, "config 5 prefill rows")
+    ref = oracle_prefill_rows(wl.bf16_bits(hv["q_prefill"]), w.prefill_query_start_loc, kc, vc,
+                              w.block_tables[: w.num_prefill], w.context_lens[: w.num_prefill],
+                              w.scale)
+    assert ref.shape == (4096, 32, 64)
+    check(out, ref, "config 5 prefill, every row")
 
 
 def test_bad_block_is_flagged_not_fatal():
@@ -124,19 +116,15 @@ def test_bad_block_is_flagged_not_fatal():
     assert torch.isfinite(step.prefill().float()).all()  # context still usable
 
 
-def test_long_chunk_sampled_rows():
-    """One 4100-row chunk over 4000 prior tokens (129 query tiles, up to 127 key tiles):
-    rows at both ends and across tile edges against the oracle's causal definition."""
+def test_long_chunk_every_row():
+    """One 4100-row chunk over 4000 prior tokens (129 query tiles, the last one ragged, up
+    to 127 key tiles): every row against the oracle's causal chunk attention."""
     w = wl.make_workload("long_chunk", [4000], [4100], num_prefill=1, seed=21, pool_slack=0.1)
     step = GpuStep(w)
     out = step.prefill()
     assert step.check_status() == pa.PA_OK
     hv = host_vals(step.vals)
     kc, vc = oracle_pools(w, hv)
-    rows = [0, 1, 31, 32, 63, 64, 1000, 2047, 2048, 4063, 4064, 4098, 4099]
-    ctx = [4000 + i + 1 for i in rows]
-    q = wl.bf16_bits(hv["q_prefill"])[rows]
-    ref, err = oracle.decode(q, kc, vc, np.repeat(w.block_tables, len(rows), axis=0),
-                             np.array(ctx, np.int32), w.scale)
-    assert err == 0
-    check(out[torch.tensor(rows, device="cuda")], ref, "long chunk rows")
+    ref = oracle_prefill_rows(wl.bf16_bits(hv["q_prefill"]), w.prefill_query_start_loc, kc, vc,
+                              w.block_tables, w.context_lens, w.scale)
+    check(out, ref, "long chunk, every row")

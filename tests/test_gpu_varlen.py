@@ -10,7 +10,8 @@ import oracle
 from paged_kv_cache_299_gb300 import binding as pa
 from paged_kv_cache_299_gb300 import workloads as wl
 from _gpu import GpuStep, host_vals, i32
-from _util import ATOL_MAX, ATOL_MEAN, errors, oracle_pools
+from _util import (ATOL_MAX, ATOL_MEAN, errors, oracle_decode_rows, oracle_pools,
+                   oracle_prefill_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -84,6 +85,16 @@ def test_mixed_step_bit_identical_to_chunk_kernel():
     assert torch.equal(out, same)
     dec = step.decode()
     assert (out[tp:].float() - dec.float()).abs().max().item() <= 1.6e-2
+    # every row of the step against the oracle: the 4096 chunk rows (causal chunks) and the
+    # 248 decode rows (one query over the whole context)
+    hv = host_vals(step.vals)
+    kc, vc = oracle_pools(w, hv)
+    ref_pre = oracle_prefill_rows(wl.bf16_bits(hv["q_prefill"]), qsl_pre, kc, vc,
+                                  w.block_tables[: w.num_prefill],
+                                  w.context_lens[: w.num_prefill], w.scale)
+    ref_dec = oracle_decode_rows(wl.bf16_bits(hv["q_decode"]), kc, vc, w.decode_block_tables,
+                                 w.decode_context_lens, w.scale)
+    check(out, np.concatenate([ref_pre, ref_dec]), "mixed step, every row")
 
 
 def test_empty_sequences_and_one_long_chunk():

@@ -306,3 +306,28 @@ def test_copy_blocks_copies_whole_blocks_in_order():
         for b in (0, 1, 3):
             assert np.array_equal(pool[b], orig[b])
     assert oracle.copy_blocks(kc, vc, [(0, 9)]) == oracle.BAD_BLOCK
+
+
+def test_row_range_split_of_chunks_is_bit_identical_to_one_call():
+    """The threaded helpers the full-size GPU tests use: rows [a, b) of a chunk, taken as a
+    chunk of b - a rows over the first L - q_len + b keys, give bit for bit the rows of one
+    whole-batch oracle call (row i sits at position L - q_len + i either way); decode
+    slices likewise."""
+    from _util import oracle_decode_rows, oracle_prefill_rows
+    w = wl.random_small(31, num_seqs=5, max_ctx=400, num_prefill=3, max_chunk=90)
+    vals = w.values(0)
+    kc, vc = oracle_pools(w, vals)
+    q = wl.bf16_bits(vals["q_prefill"])
+    qsl = w.prefill_query_start_loc
+    whole, err = oracle.prefill_chunk(q, qsl, kc, vc, w.block_tables[:3], w.context_lens[:3],
+                                      w.scale)
+    assert err == 0
+    split = oracle_prefill_rows(q, qsl, kc, vc, w.block_tables[:3], w.context_lens[:3],
+                                w.scale, rows_per_task=7)
+    assert np.array_equal(whole, split)
+    qd = wl.bf16_bits(vals["q_decode"])
+    dec, err = oracle.decode(qd, kc, vc, w.decode_block_tables, w.decode_context_lens, w.scale)
+    assert err == 0
+    assert np.array_equal(dec, oracle_decode_rows(qd, kc, vc, w.decode_block_tables,
+                                                  w.decode_context_lens, w.scale,
+                                                  seqs_per_task=1))
