@@ -76,8 +76,11 @@ typedef struct pa_cache_desc {
   int32_t block_size;   /* tokens per block, must be 16 */
 } pa_cache_desc;
 
-/* Slot mapping (the step prepare_prefill / prepare_decode perform on the "Tiny-vLLM" page,
- * run here as a kernel).  Sequence s appends the tokens query_start_loc[s] ..
+/* Slot mapping.  Defined by: "Tiny-vLLM" (trendpick100.com), Q&A on how Tiny-vLLM splits
+ * complexity (prepare_prefill / prepare_decode publish a slot_mapping for the store), and
+ * "vLLM" (blog.rlaisqls.com), section PagedAttention (16-token blocks; the block table maps
+ * a logical block to its physical block).  Run here as a kernel.  Sequence s appends the
+ * tokens query_start_loc[s] ..
  * query_start_loc[s+1]-1, which are the last q_len of its context_lens[s] tokens; the
  * token at logical position p gets slot block_tables[s][p / 16] * 16 + p % 16.
  *   block_tables    int32 [num_seqs][max_blocks_per_seq]
@@ -94,7 +97,10 @@ pa_status pa_compute_slot_mapping(const int32_t* block_tables, int32_t max_block
                                   int64_t* slot_mapping, int32_t* device_status,
                                   pa_stream_t stream);
 
-/* KV store ("reshape_and_cache"): for every token t with slot_mapping[t] >= 0, copy
+/* KV store ("reshape_and_cache").  Defined by: "Tiny-vLLM" (trendpick100.com), Q&A on how
+ * Tiny-vLLM splits complexity (a store kernel writes each new token's key and value vector
+ * to the slot slot_mapping names), and "vLLM", section PagedAttention (the slot lies in a
+ * fixed 16-token physical block).  For every token t with slot_mapping[t] >= 0, copy
  * key[t][h][:] to key_cache[slot / 16][h][slot % 16][:] and value likewise, for all
  * heads h.  A bit-exact copy.  key/value bf16 [num_tokens][Hkv][D]; num_tokens == 0 is a
  * no-op.  Duplicate slots within one call are a caller error (the winner is undefined). */
@@ -105,17 +111,24 @@ pa_status pa_reshape_and_cache(const void* key, const void* value,
 
 /* Bytes of device workspace pa_decode needs for these sizes on the current device
  * (0 when the sizes are invalid).  The workspace holds the split-KV partial results, the
- * per-sequence block offsets and one piece counter per (sequence, kv head).  Zero-fill it
- * once before its first use.  Every call whose kernels run to the end leaves the counters
- * at zero again, including calls that report a device-side error through device_status
- * (bad block id, bad context, timeout: the affected pieces are still counted), so the same
- * buffer is reused call after call without clearing.  Only a CUDA error that ends a kernel
- * early (the context is then unusable) leaves the counters undefined. */
+ * per-sequence block offsets and one piece counter per (sequence, kv head); where the
+ * counters sit depends on num_seqs.  Zero-fill the buffer before its first use, and again
+ * before a call whose num_seqs or num_kv_heads differ from those of the previous call on
+ * it (the counters would then overlap that call's offsets or partials).  Every call whose
+ * kernels run to the end leaves its counters at zero again, including calls that report a
+ * device-side error through device_status (bad block id, bad context, timeout: the
+ * affected pieces are still counted), so calls of the same sizes reuse the buffer without
+ * clearing.  Only a CUDA error that ends a kernel early (the context is then unusable)
+ * leaves the counters undefined. */
 size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_heads,
                                 int32_t max_context_len, int32_t partition_tokens);
 
-/* Paged decode attention: one query per sequence (its newest token, already stored)
- * over all context_lens[s] cached tokens:
+/* Paged decode attention.  Defined by: "vLLM" (blog.rlaisqls.com), section Flash Attention
+ * (S = Q K^T, P = softmax(S), O = P V, evaluated block by block with a running max and sum),
+ * section PagedAttention (the K/V of a sequence are found through its block table), and
+ * "tiny-vllm (1)" (geonuchoi.com), section 2 (GQA: consecutive query heads share one K/V
+ * head).  One query per sequence (its newest token, already stored) over all
+ * context_lens[s] cached tokens:
  *   out[s][h][:] = sum_j softmax_j(scale * q[s][h] . K_s[j][h / group]) V_s[j][h / group]
  * where K_s[j] / V_s[j] is the token at logical position j found through block_tables.
  * The (sequence, K/V head, block) tiles are split evenly over the SMs (or into runs of at
@@ -157,7 +170,10 @@ pa_status pa_decode_append(void* out, const void* q, const void* key, const void
                            void* workspace, size_t workspace_bytes, int32_t* device_status,
                            pa_stream_t stream);
 
-/* Causal chunked-prefill attention over a paged prefix.  Sequence s has q_len =
+/* Causal chunked-prefill attention over a paged prefix.  Defined by: "tiny-vllm (1)"
+ * (geonuchoi.com), section 1 (decoder-only causal attention: position t attends positions
+ * <= t) and section 2 (GQA), and "vLLM" (blog.rlaisqls.com), sections Flash Attention
+ * (online softmax over key blocks) and PagedAttention (paged K/V).  Sequence s has q_len =
  * query_start_loc[s+1] - query_start_loc[s] query rows, the last q_len of its
  * context_lens[s] tokens (already stored); row i sits at position L - q_len + i and
  * attends keys 0 .. L - q_len + i.  QK^T and PV run on tcgen05 tensor cores.
@@ -224,11 +240,11 @@ pa_status pa_attention_varlen(void* out, const void* q, const int32_t* query_sta
  *     cudaDeviceReset); make the first call on a device before any stream capture.  A
  *     failed lookup is reported (PA_ERR_CUDA) and retried by the next call.
  *   - All calls share the array and it keeps the last call's contents.  The only part
- *     that must start at zero, the per-segment piece counters, is zero when the library
- *     loads, and every call whose kernels run to the end leaves it at zero, including
- *     calls that report a device-side error through device_status; everything else is
- *     written before it is read.  Calls that can overlap on the GPU (different streams,
- *     or different host threads) race on the array: order them on one stream.
+ *     that must start at zero, the per-segment piece counters, is cleared by each call on
+ *     its stream (an asynchronous memset of at most 1 MiB, before the kernels; nothing is
+ *     allocated), because their place in the array depends on num_seqs; everything else
+ *     is written before it is read.  Calls that can overlap on the GPU (different
+ *     streams, or different host threads) race on the array: order them on one stream.
  *   - No allocation of any kind happens inside this call. */
 #define PA_DECODE_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
 pa_status pa_decode_static_scratch(void* out, const void* q, const void* key_cache,

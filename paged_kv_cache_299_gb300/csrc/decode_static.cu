@@ -111,6 +111,24 @@ extern "C" pa_status pa_decode_static_scratch(
   if (num_seqs > 0) {
     const pa_status st = scratch_on_current_device(&scratch);
     if (st != PA_OK) return st;
+    // The piece counters of the in-kernel merge must start at zero.  A call leaves its own
+    // counters at zero, but where they sit depends on num_seqs: after a call of another
+    // size they would overlap that call's offsets or partials.  So clear them on the stream
+    // first (a memset node; nothing is allocated).
+    pkv::DecodePlan plan;
+    if (pkv::plan_decode(num_seqs, cd.num_kv_heads, num_q_heads, max_context_len,
+                         partition_tokens, &plan) == cudaSuccess &&
+        plan.ws_meta_bytes > plan.ws_count_offset) {
+      const cudaError_t e = cudaMemsetAsync(static_cast<uint8_t*>(scratch) + plan.ws_count_offset,
+                                            0, plan.ws_meta_bytes - plan.ws_count_offset,
+                                            reinterpret_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess) {
+        char msg[200];
+        snprintf(msg, sizeof msg, "pa_decode_static_scratch: clearing the counters failed: %s",
+                 cudaGetErrorString(e));
+        return pkv::record_error(PA_ERR_CUDA, msg);
+      }
+    }
   }
   // Same argument checks, plan and kernels as pa_decode; nothing is allocated.
   return pa_decode(out, q, key_cache, value_cache, cd, block_tables, max_blocks_per_seq,
