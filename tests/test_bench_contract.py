@@ -59,3 +59,24 @@ def test_gpus_flag_alone_starts_one_rank_per_gpu():
     lines = [l for l in res.stdout.splitlines() if l.strip().startswith("{")]
     assert len(lines) == 1
     assert json.loads(lines[0])["n_gpus"] == 2
+
+
+def test_traffic_figures_name_existing_kernels_and_sources():
+    """The committed DRAM figures name each kernel's source file and its hash; the bench
+    returns a byte count only while the source is unchanged, else None."""
+    sys.path.insert(0, ROOT)
+    import hashlib
+    import bench
+    with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+        figures = json.load(f)
+    for kernel, entry in figures.items():
+        if kernel.startswith("_"):
+            continue
+        src = os.path.join(ROOT, entry["source"])
+        assert os.path.exists(src), src
+        current = hashlib.sha256(open(src, "rb").read()).hexdigest() == entry["source_sha256"]
+        for workload, fig in entry["workloads"].items():
+            got = bench.ncu_traffic(kernel, workload)
+            assert got == (fig["dram_bytes_per_launch"] if current else None)
+            assert fig["dram_bytes_per_launch"] == fig["read"] + fig["write"]
+    assert bench.ncu_traffic("no_such_kernel", "decode_b256") is None
