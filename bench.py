@@ -323,8 +323,8 @@ class DeviceStep:
         w = self.w
         if self.fused_append:
             return w.layers * (2 if self.ws_merge_kernel else 1)
-        if self.unified:  # store, plan, attention
-            return 1 + 3 * w.layers
+        if self.unified:  # store; per layer the decode rows' kernel (+ merge) and the chunk kernel
+            return 1 + (3 if self.ws_merge_kernel else 2) * w.layers
         per_layer = 1 + ((2 if self.ws_merge_kernel else 1) if w.num_decode else 0) + \
             (1 if w.num_prefill else 0)
         return 1 + per_layer * w.layers
@@ -467,8 +467,8 @@ def decode_roofline(st, workload_key: str, dec_ms: float, peak: float, peak_src:
         achieved = per_launch / (dec_ms * 1e-3) / 1e9
         return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": None,
-                "kernel": "pa_attention_varlen: varlen_plan_kernel + paged_prefill_kernel "
-                          "(tcgen05) over the chunks and decode rows",
+                "kernel": "pa_attention_varlen: paged_decode_kernel over the decode rows, "
+                          "paged_prefill_kernel (tcgen05) over the chunks",
                 "peak_source": f"{peak_src} hbm_gbs", "launch_ms": round(dec_ms, 5),
                 "algorithmic_bytes_per_launch": int(per_launch)}
     per_launch = w.decode_kv_bytes() / w.layers
@@ -550,8 +550,8 @@ def run_gpu(args, rank, world):
                                else "eager (one C-ABI call per kernel group)"),
                        store=("fused into decode (pa_decode_append)" if st.fused_append
                               else "pa_compute_slot_mapping + pa_reshape_and_cache"),
-                       **({"attention": "pa_attention_varlen: one launch for chunks and "
-                                        "decode rows (plus its one-CTA plan kernel)"}
+                       **({"attention": "pa_attention_varlen: decode rows on the decode "
+                                        "kernel, chunks on the tensor-core kernel"}
                           if st.unified else {})),
         "tokens_per_s": round(w.num_decode * world / (step_ms * 1e-3), 1),
         "pct_of_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),

@@ -180,7 +180,8 @@ pa_status pa_decode_append(void* out, const void* q, const void* key, const void
  *   out / q          bf16 [num_query_tokens][num_q_heads][D]
  *   num_query_tokens == query_start_loc[num_seqs], the rows of q and out (host-known;
  *                    bounds the tensor-memory-access box reads of q)
- *   max_query_len    host-known upper bound of q_len (sizes the grid)
+ *   max_query_len    host-known upper bound of q_len (sizes the grid; with batches beyond
+ *                    2048 (sequence, 32-row tile) pairs, rows past it are not served)
  * Requires num_q_heads / num_kv_heads == 4.  num_seqs == 0 is a no-op. */
 pa_status pa_prefill_chunk(void* out, const void* q, const int32_t* query_start_loc,
                            int32_t num_query_tokens, int32_t max_query_len,
@@ -191,26 +192,31 @@ pa_status pa_prefill_chunk(void* out, const void* q, const int32_t* query_start_
                            int32_t num_q_heads, float scale, int32_t* device_status,
                            pa_stream_t stream);
 
-/* Bytes of device workspace pa_attention_varlen needs for a batch of num_seqs sequences
- * carrying num_query_tokens query rows in total: 16 + 8 x (num_query_tokens / 32 +
- * num_seqs + 1).  Returns 0 for negative arguments. */
+/* Bytes of device workspace pa_attention_varlen needs on the current device for a batch of
+ * num_seqs sequences carrying num_query_tokens query rows, for any head count and context
+ * length (the decode kernel's workspace, see below; it depends on the SM count).  16 when
+ * num_seqs is 0 or above 4096; 0 for negative arguments or without a device. */
 size_t pa_varlen_workspace_size(int32_t num_seqs, int32_t num_query_tokens);
 
-/* One continuous-batching step's attention in one attention launch ("vLLM", Continuous
- * Batching: sequences in the prefill and in the decode phase share a step).  Arguments,
- * semantics and results are exactly those of pa_prefill_chunk: a sequence with q_len = 1
- * is a decode row, q_len > 1 a causal chunk, q_len = 0 contributes nothing, and the
- * sequences may come in any order.  Instead of one CTA per (sequence, 32-row query tile,
- * KV head) over a padded grid, a one-CTA plan kernel lists the (sequence, tile) items that
- * exist, sorted by their number of 64-key tiles (heaviest first), and the tensor-core
- * kernel runs over that list, so a batch of mostly short decode rows launches no empty
- * CTAs and the longest spans start first.  Outputs are bit-identical to pa_prefill_chunk.
+/* One continuous-batching step's attention ("vLLM", Continuous Batching: sequences in the
+ * prefill and in the decode phase share a step).  Arguments and semantics are those of
+ * pa_prefill_chunk: a sequence with q_len = 1 is a decode row, q_len > 1 a causal chunk,
+ * q_len = 0 contributes nothing, and the sequences may come in any order.  Each kind runs on
+ * the kernel built for it: the decode rows on the CUDA-core decode kernel of pa_decode
+ * (balanced split, reading and writing their rows where query_start_loc puts them), the
+ * chunks on the tensor-core kernel of pa_prefill_chunk; both launch on `stream`, and the
+ * second is skipped when max_query_len is 1 (no chunk can exist).  Chunk rows are
+ * bit-identical to pa_prefill_chunk; decode rows equal pa_decode's up to the rounding of its
+ * split.  Batches of more than 4096 sequences run every row on the tensor-core kernel.
  *   workspace        device buffer of at least pa_varlen_workspace_size(num_seqs,
  *                    num_query_tokens) bytes, 16-byte aligned, caller-owned; no
- *                    initialisation needed; the call overwrites it.
+ *                    initialisation needed: each call clears the part that must start at
+ *                    zero on the stream (a memset; nothing is allocated).  Calls that can
+ *                    overlap on the GPU must not share a workspace.
  * Errors: those of pa_prefill_chunk; PA_ERR_WORKSPACE for a missing, misaligned or short
- * workspace.  A query_start_loc whose rows run past num_query_tokens is flagged on the
- * device (PA_DEVFLAG_BAD_CONTEXT) and those sequences are skipped. */
+ * workspace.  A query_start_loc whose rows run past num_query_tokens, or a context shorter
+ * than its rows, is flagged on the device (PA_DEVFLAG_BAD_CONTEXT) and that sequence is
+ * skipped. */
 pa_status pa_attention_varlen(void* out, const void* q, const int32_t* query_start_loc,
                               int32_t num_query_tokens, int32_t max_query_len,
                               const void* key_cache, const void* value_cache, pa_cache_desc cd,

@@ -283,6 +283,7 @@ pa_status pa_prefill_chunk(void* out, const void* q, const int32_t* query_start_
 
 size_t pa_varlen_workspace_size(int32_t num_seqs, int32_t num_query_tokens) {
   if (num_seqs < 0 || num_query_tokens < 0) return 0;
+  if (num_seqs == 0) return 16;
   return pkv::varlen_workspace_size(num_seqs, num_query_tokens);
 }
 
@@ -300,10 +301,13 @@ pa_status pa_attention_varlen(void* out, const void* q, const int32_t* query_sta
                             value_cache, cd, block_tables, max_blocks_per_seq, context_lens,
                             num_seqs, num_q_heads, scale, device_status, &a, &skip);
   if (st != PA_OK || skip) return st == PA_OK ? ok() : st;
-  const size_t need = pkv::varlen_workspace_size(num_seqs, num_query_tokens);
-  if (!workspace || !aligned16(workspace) || workspace_bytes < need)
-    return fail(PA_ERR_WORKSPACE, "varlen workspace %zu bytes at %p, need %zu (16-byte aligned)",
-                workspace_bytes, workspace, need);
+  if (!workspace || !aligned16(workspace))
+    return fail(PA_ERR_WORKSPACE, "varlen workspace at %p (needs a 16-byte aligned buffer)",
+                workspace);
+  const size_t need = pkv::varlen_workspace_need(a);
+  if (need == 0) return fail(PA_ERR_CUDA, "varlen: decode plan failed (no device?)");
+  if (workspace_bytes < need)
+    return fail(PA_ERR_WORKSPACE, "varlen workspace %zu bytes, need %zu", workspace_bytes, need);
   return from_cuda(pkv::launch_varlen(a, workspace, reinterpret_cast<cudaStream_t>(stream)),
                    "varlen launch");
 }

@@ -79,7 +79,17 @@ struct KParams {
   uint8_t* key_cache_w;    // writable views of the pools (fused append)
   uint8_t* value_cache_w;
   int32_t* status;
+  // Mixed batches (the varlen launch): sequence s's query and output row is q_rows[s], and
+  // only sequences with exactly one row (q_rows[s+1] - q_rows[s] == 1) are served here; the
+  // others are left alone (no tiles, nothing written).  nullptr: row s, every sequence.
+  const int32_t* q_rows;
+  int32_t num_query_tokens;
 };
+
+// Query / output row of sequence s.
+__device__ __forceinline__ int64_t row_of(const KParams& p, int s) {
+  return p.q_rows != nullptr ? p.q_rows[s] : s;
+}
 
 __device__ __forceinline__ int64_t run_start(int64_t c, int64_t total, int32_t grid,
                                              int32_t chunk) {
@@ -360,7 +370,7 @@ __device__ void merge_segment_in_warp(const KParams& p, const SegmentPieces& sp,
       }
       const float inv = 1.f / lh;
       __nv_bfloat16* out =
-          p.out + (static_cast<int64_t>(s) * p.num_q_heads + g * GROUP + h) * kHeadDim;
+          p.out + (row_of(p, s) * p.num_q_heads + g * GROUP + h) * kHeadDim;
       reinterpret_cast<__nv_bfloat162*>(out)[lane] = __floats2bfloat162_rn(ah.x * inv, ah.y * inv);
     }
     return;
@@ -436,7 +446,7 @@ __device__ void merge_segment_in_warp(const KParams& p, const SegmentPieces& sp,
   for (int h = 0; h < GROUP; ++h) {
     const float inv = 1.f / L[h];
     __nv_bfloat16* out =
-        p.out + (static_cast<int64_t>(s) * p.num_q_heads + g * GROUP + h) * kHeadDim;
+        p.out + (row_of(p, s) * p.num_q_heads + g * GROUP + h) * kHeadDim;
     reinterpret_cast<__nv_bfloat162*>(out)[lane] =
         __floats2bfloat162_rn(acc[h].x * inv, acc[h].y * inv);
   }
@@ -475,7 +485,7 @@ paged_decode_kernel(const KParams p) {
   // often in the middle of a warp's stream: bring all of them into L2 now, one 128-byte row
   // per thread of the grid.
   {
-    const int64_t q_rows = static_cast<int64_t>(S) * p.num_q_heads;
+    const int64_t q_rows = p.q_rows != nullptr ? 0 : static_cast<int64_t>(S) * p.num_q_heads;
     const int64_t kv_rows = p.k_new != nullptr ? static_cast<int64_t>(S) * KV : 0;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + tid; i < q_rows + 2 * kv_rows;
          i += static_cast<int64_t>(gridDim.x) * kThreads) {
@@ -491,7 +501,18 @@ paged_decode_kernel(const KParams p) {
   for (int i = tid; i < S; i += kThreads) {
     const int32_t L = p.context_lens[i];
     int32_t nb = 0;
-    if (L < 0 || static_cast<int64_t>(L) > static_cast<int64_t>(p.max_blocks_per_seq) * kBlockSize) {
+    bool serve = true;
+    if (p.q_rows != nullptr) {  // mixed batch: decode rows only, the same checks as chunks
+      const int32_t r0 = p.q_rows[i];
+      const int32_t q_len = p.q_rows[i + 1] - r0;
+      serve = q_len == 1;
+      if (serve && (r0 < 0 || r0 >= p.num_query_tokens || L < 1)) {
+        if (blockIdx.x == 0) flag_error(p.status, PA_DEVFLAG_BAD_CONTEXT);
+        serve = false;
+      }
+    }
+    if (!serve) {
+    } else if (L < 0 || static_cast<int64_t>(L) > static_cast<int64_t>(p.max_blocks_per_seq) * kBlockSize) {
       if (blockIdx.x == 0) flag_error(p.status, PA_DEVFLAG_BAD_CONTEXT);
     } else {
       nb = (L + kBlockSize - 1) / kBlockSize;
@@ -540,7 +561,8 @@ paged_decode_kernel(const KParams p) {
         flag_error(p.status, PA_DEVFLAG_BAD_CONTEXT);  // contexts beyond max_context_len
     }
   }
-  if (p.fused_merge && blockIdx.x == 0) {  // empty contexts: zero rows (no tile writes them)
+  if (p.fused_merge && blockIdx.x == 0 && p.q_rows == nullptr) {
+    // empty contexts: zero rows (no tile writes them)
     const int row_elems = p.num_q_heads * kHeadDim;
     for (int s0 = 0; s0 < S; ++s0) {
       if (seq_base[s0 + 1] != seq_base[s0]) continue;
@@ -636,7 +658,7 @@ paged_decode_kernel(const KParams p) {
 #pragma unroll
     for (int h = 0; h < GROUP; ++h) {
       const __nv_bfloat16* qrow =
-          p.q + (static_cast<int64_t>(pc.s) * p.num_q_heads + pc.g * GROUP + h) * kHeadDim;
+          p.q + (row_of(p, pc.s) * p.num_q_heads + pc.g * GROUP + h) * kHeadDim;
       float2 f[4];
       unpack4(ldg_nc128(qrow + dq * 8), f);
 #pragma unroll
@@ -733,7 +755,7 @@ paged_decode_kernel(const KParams p) {
       if (tg == 0) {
         if (whole) {
           const float inv = 1.f / hl;
-          const int64_t row = static_cast<int64_t>(pc.s) * p.num_q_heads + pc.g * GROUP + h;
+          const int64_t row = row_of(p, pc.s) * p.num_q_heads + pc.g * GROUP + h;
           uint32_t w[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -817,10 +839,11 @@ merge_partials_kernel(const KParams p) {
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int KV = p.num_kv_heads;
-  __nv_bfloat16* out = p.out + (static_cast<int64_t>(s) * p.num_q_heads + g * GROUP) * kHeadDim;
+  __nv_bfloat16* out = p.out + (row_of(p, s) * p.num_q_heads + g * GROUP) * kHeadDim;
   const int32_t base = p.ws_seq_base[s];
   const int nb = p.ws_seq_base[s + 1] - base;
   if (nb == 0) {
+    if (p.q_rows != nullptr) return;  // not a decode row of a mixed batch, or flagged
     for (int e = tid; e < GROUP * kHeadDim; e += kMergeThreads) out[e] = __float2bfloat16_rn(0.f);
     return;
   }
@@ -992,6 +1015,8 @@ cudaError_t launch(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t str
   p.key_cache_w = static_cast<uint8_t*>(const_cast<void*>(a.key_cache));
   p.value_cache_w = static_cast<uint8_t*>(const_cast<void*>(a.value_cache));
   p.status = a.status;
+  p.q_rows = a.q_rows;
+  p.num_query_tokens = a.num_query_tokens;
   paged_decode_kernel<GROUP><<<plan.grid, kWarps * 32, plan.smem_bytes, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess || plan.fused_merge) return e;

@@ -62,6 +62,9 @@ struct DecodeArgs {
   int32_t* status;
   const void* k_new = nullptr;  // fused append (pa_decode_append), else null
   const void* v_new = nullptr;
+  const int32_t* q_rows = nullptr;  // mixed batch: query/output row per sequence (prefix sums
+                                    // of q_len); only q_len == 1 sequences are served
+  int32_t num_query_tokens = 0;
 };
 
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream);
@@ -87,9 +90,13 @@ struct PrefillArgs {
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 
-// Unified varlen launch: a work-list plan kernel (items sorted by work) and the chunk
-// kernel over that list.  The workspace holds the item count and the items.
+// Unified varlen launch: the decode kernel serves the one-row sequences in place (the
+// workspace is its workspace), the chunk kernel the others.  Sizes on the current device:
+// an upper bound for any head count and context (the size query), and the exact need of
+// one call.
+int decode_max_seqs();
 size_t varlen_workspace_size(int32_t num_seqs, int32_t num_query_tokens);
+size_t varlen_workspace_need(const PrefillArgs& a);
 cudaError_t launch_varlen(const PrefillArgs& a, void* workspace, cudaStream_t stream);
 
 }  // namespace pkv

@@ -9,25 +9,34 @@
 //
 // GB300 design.  QK^T and PV are dense contractions, so they run on the 5th-generation
 // tensor cores with accumulators in tensor memory (TMEM):
-//   * One CTA per (32-token query tile, K/V head, sequence), two CTAs per SM.  Its 128 MMA
-//     rows are the 32 tokens x 4 query heads that share the K/V head (row = 4 * token +
-//     head), so each K/V tile feeds four heads.  The query-tile index is the slowest grid
-//     dimension, reversed, so the tiles with the longest causal spans start first.
-//   * Warp 5 loads the Q tile with one 3-D TMA box and gathers every 64-key K/V tile as
-//     four 16-row TMA boxes at the physical blocks named by the block table (128-byte
-//     swizzle), into a 4-stage ring; the block table is read in prefetched 32-entry windows.
+//   * A work unit is one (32-token query tile, K/V head) of one sequence: 128 MMA rows =
+//     32 tokens x 4 query heads sharing the K/V head (row = 4 * token + head), so each K/V
+//     tile feeds four heads.
+//   * Persistent grid, two CTAs per SM.  Every CTA first runs the same in-kernel plan: it
+//     lists the (sequence, query tile) pairs, sorts them by their number of 64-key tiles,
+//     heaviest first (a stable counting sort, identical in every CTA), and takes its share
+//     of the units as a snake over that order, so the SMs end together.  (Batches beyond
+//     the sort's size take the units in grid order instead.)  The CTA then serves its units
+//     back to back: barrier phases, the K/V ring and the two S buffers carry over from one
+//     unit to the next, the next unit's Q is loaded one unit ahead and written to TMEM
+//     during the current unit's last tile, so its first scores are computed while the
+//     current unit finishes.
+//   * Warp 5 loads Q with one 3-D TMA box per unit (two Q buffers) and gathers every 64-key
+//     K/V tile as four 16-row TMA boxes at the physical blocks named by the block table
+//     (128-byte swizzle), into a 4-stage ring; the block table is read in prefetched
+//     32-entry windows.
 //   * Warp 4 (one thread) issues S = Q K^T (M128 N64 K64 into one of two fp32 S buffers,
 //     so the next tile's scores are computed during this tile's softmax) and
 //     [O | l] += P [V | 1] (M128 N80 K64, V read N-major): 16 extra columns of the B operand
 //     come from a constant shared-memory atom of bf16 ones, one leading-byte offset from
 //     each V slice, so the tensor core also accumulates the row sums l of exactly the bf16
-//     P that weights V.  Both A operands come from TMEM: Q is copied there once by the row
-//     warps and P is written per tile over the first half of its own S buffer, so each MMA
+//     P that weights V.  Both A operands come from TMEM: Q is copied there by the row warps
+//     and P is written per tile over the first half of its own S buffer, so each MMA
 //     streams only its K or V tile from shared memory.
 //   * Warps 0-3 own one TMEM lane = one query row each: they read S, mask by absolute
 //     position (diagonal tiles only), keep the running max in registers ([O | l] in TMEM is
 //     rescaled only when the max grows by more than 2^8), write P as packed bf16 into TMEM,
-//     and finally divide O by l and store bf16 rows.
+//     and at the end of a unit divide O by l and store bf16 rows.
 // TMEM per CTA (256 columns): S buffers 0..63 and 64..127 (P over 0..31 / 64..95), O
 // 128..191, l 192..207, Q 224..255.
 // Every mbarrier wait is bounded; on timeout the CTA records PA_DEVFLAG_TIMEOUT, drains
@@ -98,6 +107,7 @@ struct PParams {
   int32_t num_query_tokens;
   int32_t num_seqs;
   int32_t q_tiles;  // query tiles of the longest chunk: ceil(max_query_len / 32)
+  int32_t skip_single;  // 1: sequences with exactly one query row are served elsewhere
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
@@ -181,7 +191,7 @@ __device__ __forceinline__ bool next_unit(const PParams& p, const Schedule& sc, 
     u.g = static_cast<int>(rem / p.num_seqs);
     u.s = static_cast<int>(rem % p.num_seqs);
     if (!sequence_ok(p, u.s, &u.q0, &u.q_len, &u.L, u.tile == 0 && u.g == 0)) continue;
-    if (u.tile * kTokensPerTile >= u.q_len) continue;
+    if (u.tile * kTokensPerTile >= u.q_len || (p.skip_single && u.q_len == 1)) continue;
     fill_unit(u);
     return true;
   }
@@ -231,7 +241,8 @@ __device__ int plan_units(const PParams& p, uint8_t* scratch, int* red, int32_t*
   for (int s0 = 0; s0 < p.num_seqs; s0 += kSortThreads) {
     const int s = s0 + tid;
     int q0 = 0, q_len = 0, L = 0, tiles = 0;
-    if (s < p.num_seqs && sequence_ok(p, s, &q0, &q_len, &L, blockIdx.x == 0))
+    if (s < p.num_seqs && sequence_ok(p, s, &q0, &q_len, &L, blockIdx.x == 0) &&
+        !(p.skip_single && q_len == 1))
       tiles = (q_len + kTokensPerTile - 1) / kTokensPerTile;
     int total;
     const int excl = block_exclusive_scan(tiles, red, &total);
@@ -842,16 +853,20 @@ cudaError_t prepare(const PrefillArgs& a, CUtensorMap* tq, CUtensorMap* tk, CUte
   p->num_query_tokens = a.num_query_tokens;
   p->num_seqs = a.num_seqs;
   p->q_tiles = (a.max_query_len + kTokensPerTile - 1) / kTokensPerTile;
+  p->skip_single = 0;
   return cudaSuccess;
 }
 
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
+namespace {
+
+cudaError_t launch_prefill_kernel(const PrefillArgs& a, bool skip_single, cudaStream_t stream) {
   CUtensorMap tq, tk, tv;
   PParams p;
   cudaError_t e = prepare(a, &tq, &tk, &tv, &p);
   if (e != cudaSuccess) return e;
+  p.skip_single = skip_single ? 1 : 0;
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
@@ -864,12 +879,76 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-size_t varlen_workspace_size(int32_t num_seqs, int32_t num_query_tokens) {
-  return 16 + 8 * (static_cast<size_t>(num_query_tokens) / kTokensPerTile + num_seqs + 1);
+// Decode plan of a mixed batch's one-row sequences: a balanced split over the device, every
+// context bounded by its block-table row.
+cudaError_t varlen_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_heads,
+                               int32_t max_blocks_per_seq, DecodePlan* plan) {
+  const int64_t max_ctx = static_cast<int64_t>(max_blocks_per_seq) * kBlockSize;
+  return plan_decode(num_seqs, num_kv_heads, num_q_heads,
+                     static_cast<int32_t>(max_ctx < 0x7fffffff ? max_ctx : 0x7fffffff), 0, plan);
 }
 
-cudaError_t launch_varlen(const PrefillArgs& a, void* /*workspace*/, cudaStream_t stream) {
-  return launch_prefill(a, stream);
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
+  return launch_prefill_kernel(a, false, stream);
+}
+
+bool varlen_routes_decode_rows(int32_t num_seqs) { return num_seqs <= decode_max_seqs(); }
+
+size_t varlen_workspace_need(const PrefillArgs& a) {
+  if (!varlen_routes_decode_rows(a.num_seqs)) return 16;
+  DecodePlan plan;
+  if (varlen_decode_plan(a.num_seqs, a.num_kv_heads, a.num_q_heads, a.max_blocks_per_seq,
+                         &plan) != cudaSuccess)
+    return 0;
+  return plan.workspace_bytes;
+}
+
+size_t varlen_workspace_size(int32_t num_seqs, int32_t num_query_tokens) {
+  (void)num_query_tokens;
+  if (!varlen_routes_decode_rows(num_seqs)) return 16;
+  // an upper bound for any head count (64 K/V heads) and context length
+  DecodePlan plan;
+  if (plan_decode(num_seqs, 64, 256, 0x7fffffff, 0, &plan) != cudaSuccess) return 0;
+  return plan.workspace_bytes;
+}
+
+cudaError_t launch_varlen(const PrefillArgs& a, void* workspace, cudaStream_t stream) {
+  if (!varlen_routes_decode_rows(a.num_seqs))  // every row on the tensor-core kernel
+    return launch_prefill_kernel(a, false, stream);
+  // Decode rows (q_len 1) on the CUDA-core decode kernel, reading and writing their rows in
+  // place; its workspace counters start at zero (cleared on the stream, nothing allocated).
+  DecodePlan plan;
+  cudaError_t e = varlen_decode_plan(a.num_seqs, a.num_kv_heads, a.num_q_heads,
+                                     a.max_blocks_per_seq, &plan);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(static_cast<uint8_t*>(workspace) + plan.ws_count_offset, 0,
+                      plan.ws_meta_bytes - plan.ws_count_offset, stream);
+  if (e != cudaSuccess) return e;
+  DecodeArgs d;
+  d.out = a.out;
+  d.q = a.q;
+  d.key_cache = a.key_cache;
+  d.value_cache = a.value_cache;
+  d.block_tables = a.block_tables;
+  d.max_blocks_per_seq = a.max_blocks_per_seq;
+  d.context_lens = a.context_lens;
+  d.num_seqs = a.num_seqs;
+  d.num_q_heads = a.num_q_heads;
+  d.num_kv_heads = a.num_kv_heads;
+  d.num_blocks = a.num_blocks;
+  d.scale = a.scale;
+  d.workspace = workspace;
+  d.status = a.status;
+  d.q_rows = a.query_start_loc;
+  d.num_query_tokens = a.num_query_tokens;
+  e = launch_decode(d, plan, stream);
+  if (e != cudaSuccess) return e;
+  // Chunks (q_len > 1) on the tensor-core kernel; none can exist when the host bound of
+  // q_len is 1 (a decode-only batch), and then nothing more is launched.
+  if (a.max_query_len <= 1) return cudaSuccess;
+  return launch_prefill_kernel(a, true, stream);
 }
 
 }  // namespace pkv

@@ -57,15 +57,19 @@ def test_mixed_batch_any_order_matches_oracle(seed):
                                     ctx.cpu().numpy(), w.scale)
     assert err == 0
     check(out, ref, w.name)
+    # chunk rows come from the same tensor-core kernel as pa_prefill_chunk: bit-identical;
+    # decode rows (q_len 1) from the CUDA-core decode kernel: equal within rounding
     same = torch.empty_like(q)
     pa.pa_prefill_chunk(same, q, i32(qsl), int(lens.max()), step.kc, step.vc, bt, ctx, w.scale)
-    assert torch.equal(out, same)
+    one = torch.from_numpy(np.repeat(lens == 1, lens)).cuda()
+    assert torch.equal(out[~one], same[~one])
+    assert (out[one].float() - same[one].float()).abs().max().item() <= 1.6e-2
 
 
-def test_mixed_step_bit_identical_to_chunk_kernel():
+def test_mixed_step_matches_chunk_and_decode_kernels_and_oracle():
     """The mixed continuous-batching step (8 chunks of 512 and 248 decode rows) in one
-    varlen call equals pa_prefill_chunk on the same rows, and its decode rows agree with
-    the decode kernel within the attention tolerance."""
+    varlen call: its chunk rows equal pa_prefill_chunk bit for bit, its decode rows agree
+    with pa_decode within the attention tolerance, and every row matches the oracle."""
     w = wl.mixed_prefill_decode()
     step = GpuStep(w)
     nd = w.num_decode
@@ -82,7 +86,7 @@ def test_mixed_step_bit_identical_to_chunk_kernel():
     assert step.check_status() == pa.PA_OK
     same = torch.empty_like(q)
     pa.pa_prefill_chunk(same, q, i32(qsl), 512, step.kc, step.vc, step.bt, step.ctx, w.scale)
-    assert torch.equal(out, same)
+    assert torch.equal(out[:tp], same[:tp])
     dec = step.decode()
     assert (out[tp:].float() - dec.float()).abs().max().item() <= 1.6e-2
     # every row of the step against the oracle: the 4096 chunk rows (causal chunks) and the
@@ -134,3 +138,43 @@ def test_rows_beyond_the_query_buffer_are_flagged_not_written():
     assert pa.pa_check_device_status(status) == pa.PA_ERR_DEVICE_INDEX
     assert torch.all(guard[q.shape[0]:] == 3.0)  # nothing written past the buffer
     assert torch.isfinite(out[0].float()).all()  # the valid sequence was still served
+
+
+def test_decode_only_batch_runs_on_the_decode_kernel():
+    """A batch of decode rows only (batch 256, lognormal contexts): every row comes from
+    the CUDA-core decode kernel and equals pa_decode within rounding and the oracle."""
+    w = wl.decode_batch256_lognormal(layers=1)
+    step = GpuStep(w)
+    q = step.vals["q_decode"]
+    qsl = np.arange(w.num_seqs + 1, dtype=np.int32)
+    out = torch.full_like(q, float("nan"))
+    pa.pa_attention_varlen(out, q, i32(qsl), 1, step.kc, step.vc, step.bt, step.ctx, w.scale,
+                           device_status=step.status)
+    assert step.check_status() == pa.PA_OK
+    dec = step.decode()
+    assert (out.float() - dec.float()).abs().max().item() <= 1.6e-2
+    hv = host_vals(step.vals)
+    kc, vc = oracle_pools(w, hv)
+    ref = oracle_decode_rows(wl.bf16_bits(hv["q_decode"]), kc, vc, w.block_tables,
+                             w.context_lens, w.scale)
+    check(out, ref, "decode-only varlen")
+
+
+def test_more_sequences_than_the_decode_kernel_takes():
+    """4100 one-row sequences (beyond the decode kernel's 4096): every row then runs on the
+    tensor-core chunk kernel, in grid order (the batch is beyond the in-kernel sort too)."""
+    rng = np.random.default_rng(41)
+    ctx = rng.integers(1, 48, size=4100)
+    w = wl.make_workload("many_rows", ctx - 1, np.ones(4100, np.int64), num_prefill=4100, seed=41,
+                         pool_slack=0.2)
+    step = GpuStep(w)
+    q = step.vals["q_prefill"]
+    out = torch.empty_like(q)
+    pa.pa_attention_varlen(out, q, i32(w.prefill_query_start_loc), 1, step.kc, step.vc, step.bt,
+                           step.ctx, w.scale, device_status=step.status)
+    assert step.check_status() == pa.PA_OK
+    hv = host_vals(step.vals)
+    kc, vc = oracle_pools(w, hv)
+    ref = oracle_decode_rows(wl.bf16_bits(hv["q_prefill"]), kc, vc, w.block_tables,
+                             w.context_lens, w.scale)
+    check(out, ref, "4100 rows")
