@@ -86,9 +86,12 @@ struct KParams {
   int32_t num_query_tokens;
 };
 
-// Query / output row of sequence s.
+// Query / output row of sequence s (kRows: the mixed-batch form, a separate instantiation
+// so that the plain decode path compiles without it).
+template <bool kRows>
 __device__ __forceinline__ int64_t row_of(const KParams& p, int s) {
-  return p.q_rows != nullptr ? p.q_rows[s] : s;
+  if (kRows) return p.q_rows[s];
+  return s;
 }
 
 __device__ __forceinline__ int64_t run_start(int64_t c, int64_t total, int32_t grid,
@@ -324,7 +327,7 @@ __device__ __forceinline__ float2 ld_partial2(const float2* a) {
   return kLocal ? *a : __ldcg(a);
 }
 
-template <int GROUP, bool kLocal>
+template <int GROUP, bool kLocal, bool kRows>
 __device__ void merge_segment_in_warp(const KParams& p, const SegmentPieces& sp, int64_t x0,
                                       int64_t x1, int64_t total, int s, int g, int lane) {
   const int n = segment_piece_count(sp, x0, x1, total, p.grid);
@@ -370,7 +373,7 @@ __device__ void merge_segment_in_warp(const KParams& p, const SegmentPieces& sp,
       }
       const float inv = 1.f / lh;
       __nv_bfloat16* out =
-          p.out + (row_of(p, s) * p.num_q_heads + g * GROUP + h) * kHeadDim;
+          p.out + (row_of<kRows>(p, s) * p.num_q_heads + g * GROUP + h) * kHeadDim;
       reinterpret_cast<__nv_bfloat162*>(out)[lane] = __floats2bfloat162_rn(ah.x * inv, ah.y * inv);
     }
     return;
@@ -446,13 +449,13 @@ __device__ void merge_segment_in_warp(const KParams& p, const SegmentPieces& sp,
   for (int h = 0; h < GROUP; ++h) {
     const float inv = 1.f / L[h];
     __nv_bfloat16* out =
-        p.out + (row_of(p, s) * p.num_q_heads + g * GROUP + h) * kHeadDim;
+        p.out + (row_of<kRows>(p, s) * p.num_q_heads + g * GROUP + h) * kHeadDim;
     reinterpret_cast<__nv_bfloat162*>(out)[lane] =
         __floats2bfloat162_rn(acc[h].x * inv, acc[h].y * inv);
   }
 }
 
-template <int GROUP>
+template <int GROUP, bool kRows>
 __global__ void __launch_bounds__(kWarps * 32, 1)
 paged_decode_kernel(const KParams p) {
   constexpr int kThreads = kWarps * 32;
@@ -485,7 +488,7 @@ paged_decode_kernel(const KParams p) {
   // often in the middle of a warp's stream: bring all of them into L2 now, one 128-byte row
   // per thread of the grid.
   {
-    const int64_t q_rows = p.q_rows != nullptr ? 0 : static_cast<int64_t>(S) * p.num_q_heads;
+    const int64_t q_rows = kRows ? 0 : static_cast<int64_t>(S) * p.num_q_heads;
     const int64_t kv_rows = p.k_new != nullptr ? static_cast<int64_t>(S) * KV : 0;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + tid; i < q_rows + 2 * kv_rows;
          i += static_cast<int64_t>(gridDim.x) * kThreads) {
@@ -502,7 +505,7 @@ paged_decode_kernel(const KParams p) {
     const int32_t L = p.context_lens[i];
     int32_t nb = 0;
     bool serve = true;
-    if (p.q_rows != nullptr) {  // mixed batch: decode rows only, the same checks as chunks
+    if (kRows) {  // mixed batch: decode rows only, the same checks as chunks
       const int32_t r0 = p.q_rows[i];
       const int32_t q_len = p.q_rows[i + 1] - r0;
       serve = q_len == 1;
@@ -561,7 +564,7 @@ paged_decode_kernel(const KParams p) {
         flag_error(p.status, PA_DEVFLAG_BAD_CONTEXT);  // contexts beyond max_context_len
     }
   }
-  if (p.fused_merge && blockIdx.x == 0 && p.q_rows == nullptr) {
+  if (p.fused_merge && blockIdx.x == 0 && !kRows) {
     // empty contexts: zero rows (no tile writes them)
     const int row_elems = p.num_q_heads * kHeadDim;
     for (int s0 = 0; s0 < S; ++s0) {
@@ -658,7 +661,7 @@ paged_decode_kernel(const KParams p) {
 #pragma unroll
     for (int h = 0; h < GROUP; ++h) {
       const __nv_bfloat16* qrow =
-          p.q + (row_of(p, pc.s) * p.num_q_heads + pc.g * GROUP + h) * kHeadDim;
+          p.q + (row_of<kRows>(p, pc.s) * p.num_q_heads + pc.g * GROUP + h) * kHeadDim;
       float2 f[4];
       unpack4(ldg_nc128(qrow + dq * 8), f);
 #pragma unroll
@@ -755,7 +758,7 @@ paged_decode_kernel(const KParams p) {
       if (tg == 0) {
         if (whole) {
           const float inv = 1.f / hl;
-          const int64_t row = row_of(p, pc.s) * p.num_q_heads + pc.g * GROUP + h;
+          const int64_t row = row_of<kRows>(p, pc.s) * p.num_q_heads + pc.g * GROUP + h;
           uint32_t w[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -794,7 +797,7 @@ paged_decode_kernel(const KParams p) {
         }
         if (__shfl_sync(0xffffffffu, last, 0)) {
           __threadfence_block();  // acquire the other pieces' partials
-          merge_segment_in_warp<GROUP, true>(p, sp, x0, x0 + pc.nb, total, pc.s, pc.g, lane);
+          merge_segment_in_warp<GROUP, true, kRows>(p, sp, x0, x0 + pc.nb, total, pc.s, pc.g, lane);
           if (lane == 0) cta_seg_count[sp.c_first % kWarps] = 0;
         }
       } else {
@@ -806,7 +809,7 @@ paged_decode_kernel(const KParams p) {
         }
         if (__shfl_sync(0xffffffffu, last, 0)) {
           __threadfence();  // acquire the other pieces' partials
-          merge_segment_in_warp<GROUP, false>(p, sp, x0, x0 + pc.nb, total, pc.s, pc.g, lane);
+          merge_segment_in_warp<GROUP, false, kRows>(p, sp, x0, x0 + pc.nb, total, pc.s, pc.g, lane);
           if (lane == 0) p.seg_count[pc.s * KV + pc.g] = 0;  // ready for the next call
         }
       }
@@ -825,7 +828,7 @@ paged_decode_kernel(const KParams p) {
 
 // Combines the partials of every (sequence, kv head) whose tiles were split across CTAs,
 // and writes zero rows for empty contexts.  One CTA per (kv head, sequence).
-template <int GROUP>
+template <int GROUP, bool kRows>
 __global__ void __launch_bounds__(kMergeThreads)
 merge_partials_kernel(const KParams p) {
   constexpr int kWarps = kMergeThreads / 32;
@@ -839,11 +842,11 @@ merge_partials_kernel(const KParams p) {
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int KV = p.num_kv_heads;
-  __nv_bfloat16* out = p.out + (row_of(p, s) * p.num_q_heads + g * GROUP) * kHeadDim;
+  __nv_bfloat16* out = p.out + (row_of<kRows>(p, s) * p.num_q_heads + g * GROUP) * kHeadDim;
   const int32_t base = p.ws_seq_base[s];
   const int nb = p.ws_seq_base[s + 1] - base;
   if (nb == 0) {
-    if (p.q_rows != nullptr) return;  // not a decode row of a mixed batch, or flagged
+    if (kRows) return;  // not a decode row of a mixed batch, or flagged
     for (int e = tid; e < GROUP * kHeadDim; e += kMergeThreads) out[e] = __float2bfloat16_rn(0.f);
     return;
   }
@@ -960,15 +963,15 @@ size_t smem_bytes(int num_seqs) {
   return decode_smem_fixed<GROUP>() + sizeof(int32_t) * (num_seqs + 1);
 }
 
-template <int GROUP>
-cudaError_t prepare_kernel() {
+template <int GROUP, bool kRows>
+cudaError_t prepare_one() {
   static bool done = false;  // benign race: the attribute call is idempotent
   if (done) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<GROUP>,
+  cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<GROUP, kRows>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem_bytes<GROUP>(kMaxSeqs)));
   if (e == cudaSuccess)  // the ring needs the full shared-memory carveout
-    e = cudaFuncSetAttribute(paged_decode_kernel<GROUP>,
+    e = cudaFuncSetAttribute(paged_decode_kernel<GROUP, kRows>,
                              cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess) done = true;
@@ -976,11 +979,18 @@ cudaError_t prepare_kernel() {
 }
 
 template <int GROUP>
+cudaError_t prepare_kernel() {
+  cudaError_t e = prepare_one<GROUP, false>();
+  return e == cudaSuccess ? prepare_one<GROUP, true>() : e;
+}
+
+// Both instantiations have the same resources; the plan sizes the grid from the plain one.
+template <int GROUP>
 cudaError_t occupancy(int num_seqs, int* ctas_per_sm) {
   cudaError_t e = prepare_kernel<GROUP>();
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      ctas_per_sm, paged_decode_kernel<GROUP>, kWarps * 32,
+      ctas_per_sm, paged_decode_kernel<GROUP, false>, kWarps * 32,
       smem_bytes<GROUP>(num_seqs));
 }
 
@@ -1017,10 +1027,17 @@ cudaError_t launch(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t str
   p.status = a.status;
   p.q_rows = a.q_rows;
   p.num_query_tokens = a.num_query_tokens;
-  paged_decode_kernel<GROUP><<<plan.grid, kWarps * 32, plan.smem_bytes, stream>>>(p);
+  if (a.q_rows != nullptr)
+    paged_decode_kernel<GROUP, true><<<plan.grid, kWarps * 32, plan.smem_bytes, stream>>>(p);
+  else
+    paged_decode_kernel<GROUP, false><<<plan.grid, kWarps * 32, plan.smem_bytes, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess || plan.fused_merge) return e;
-  merge_partials_kernel<GROUP><<<dim3(a.num_kv_heads, a.num_seqs), kMergeThreads, 0, stream>>>(p);
+  const dim3 mgrid(a.num_kv_heads, a.num_seqs);
+  if (a.q_rows != nullptr)
+    merge_partials_kernel<GROUP, true><<<mgrid, kMergeThreads, 0, stream>>>(p);
+  else
+    merge_partials_kernel<GROUP, false><<<mgrid, kMergeThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
