@@ -846,8 +846,10 @@ merge_partials_kernel(const KParams p) {
   const int32_t base = p.ws_seq_base[s];
   const int nb = p.ws_seq_base[s + 1] - base;
   if (nb == 0) {
-    if (kRows) return;  // not a decode row of a mixed batch, or flagged
-    for (int e = tid; e < GROUP * kHeadDim; e += kMergeThreads) out[e] = __float2bfloat16_rn(0.f);
+    // an empty context gives a zero row; in a mixed batch nb == 0 means the sequence is not
+    // a decode row (or was flagged), and its row is left alone
+    if (!kRows)
+      for (int e = tid; e < GROUP * kHeadDim; e += kMergeThreads) out[e] = __float2bfloat16_rn(0.f);
     return;
   }
   const int64_t total = *p.ws_total;

@@ -70,7 +70,7 @@ constexpr int kKOff = kQOff + 2 * kQBytes;
 constexpr int kVOff = kKOff + kStages * kKVBytes;
 constexpr int kOnesOff = kVOff + kStages * kKVBytes;
 constexpr int kBarOff = kOnesOff + kOnesBytes;
-constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 1 + 1 + 1 + 1 + 1;  // 19
+constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 1 + 1 + 1 + 1;  // 18
 constexpr int kMiscOff = kBarOff + 24 * 8;
 constexpr int kUnitOff = kMiscOff + 128;  // misc: TMEM address, abort flag, unit count, 24 ints of scratch
 constexpr int kSmemBytes = kUnitOff + 2 * kMaxUnitsPerCta * 4;
@@ -355,11 +355,13 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
   uint64_t* q_full = bars;         // [2] Q tile landed in buffer b
   uint64_t* q_empty = bars + 2;    // [2] Q buffer b copied into tensor memory
   uint64_t* kv_full = bars + 4;    // [kStages]
-  uint64_t* kv_empty = kv_full + kStages;
-  uint64_t* s_ready = kv_empty + kStages;  // [2]
+  // pv_done[st]: the P V of the tile held in stage st has completed.  One commit serves
+  // two readers: the producer (the stage may be refilled) and the row warps (O and its row
+  // sum are up to date).  Tile jt is phase jt / kStages of pv_done[jt % kStages].
+  uint64_t* pv_done = kv_full + kStages;
+  uint64_t* s_ready = pv_done + kStages;  // [2]
   uint64_t* p_ready = s_ready + 2;
-  uint64_t* o_done = p_ready + 1;
-  uint64_t* o_free = o_done + 1;   // the epilogue has read O out of tensor memory
+  uint64_t* o_free = p_ready + 1;  // the epilogue has read O out of tensor memory
   uint64_t* q_tmem = o_free + 1;   // this unit's Q is in tensor memory
   uint64_t* drain = q_tmem + 1;
   int* misc = reinterpret_cast<int*>(smem + kMiscOff);
@@ -378,10 +380,9 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
     }
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&pv_done[i], 1);
     }
     mbar_init(p_ready, kRowThreads);
-    mbar_init(o_done, 1);
     mbar_init(o_free, kRowThreads);
     mbar_init(q_tmem, kRowThreads);
     mbar_init(drain, 1);
@@ -470,7 +471,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
         if (lane == 0 && bad_mask != 0) flag_error(p.status, PA_DEVFLAG_BAD_BLOCK);
         int go = 1;
         if (lane == 0) {
-          go = wait_or_abort(&kv_empty[st], static_cast<uint32_t>((jt / kStages) & 1) ^ 1u,
+          go = wait_or_abort(&pv_done[st], static_cast<uint32_t>((jt / kStages) & 1) ^ 1u,
                              &abort_flag, p.status);
           if (go) mbar_arrive_expect_tx(&kv_full[st], __popc(mask) * 2u * kTileBytes);
         }
@@ -547,8 +548,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
           umma_bf16_ts(tmem + kOCol, p_tmem + kk * 8, v_desc + kk * kStep, kIdescO,
                        (!first || kk > 0) ? 1u : 0u);
         }
-        umma_commit(o_done);
-        umma_commit(&kv_empty[jt % kStages]);
+        umma_commit(&pv_done[jt % kStages]);
       };
       int k = 0;
       Unit cur, nxt;
@@ -698,11 +698,11 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
           fence_proxy_async_smem();
         }
         if (jt > 0) {
-          // Every phase of o_done is observed in order (a parity wait cannot tell phases two
-          // apart).  PV(jt-1) is done with O and its row sum before they are rescaled; P(jt)
-          // itself needs no wait: PV(jt-2), the last reader of this S buffer, completed
-          // before S(jt) did.
-          ok = wait_or_abort(o_done, static_cast<uint32_t>((jt - 1) & 1), &abort_flag, p.status);
+          // PV(jt-1) is done with O and its row sum before they are rescaled or P(jt) is
+          // published.  The barrier of its stage is at most one phase from the one waited
+          // for: PV(jt-2) has completed (before S(jt) did) and PV(jt+3) needs P(jt+3).
+          ok = wait_or_abort(&pv_done[(jt - 1) % kStages],
+                             static_cast<uint32_t>(((jt - 1) / kStages) & 1), &abort_flag, p.status);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           tc_fence_after_sync();
@@ -734,7 +734,8 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
       }
       if (!ok) break;
       // ---- epilogue: O / l of this unit, then release O to the next unit's first PV ----
-      ok = wait_or_abort(o_done, static_cast<uint32_t>((jt - 1) & 1), &abort_flag, p.status);
+      ok = wait_or_abort(&pv_done[(jt - 1) % kStages],
+                         static_cast<uint32_t>(((jt - 1) / kStages) & 1), &abort_flag, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after_sync();
