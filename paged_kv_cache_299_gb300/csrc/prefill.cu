@@ -90,7 +90,7 @@ constexpr uint32_t kLCol = kOCol + kHeadDim;  // row sum l (columns 192..207 hol
 constexpr uint32_t kQCol = 224;   // Q (bf16 pairs): columns 224..255, the A operand of S = Q K^T
 constexpr int kPVN = kHeadDim + 16;  // PV MMA width: 64 output dims + 16 ones columns
 constexpr int kThreads = 192;
-constexpr int kRowThreads = 128;
+constexpr int kRowWarps = 4;  // barriers the row warps signal count one arrival per warp
 constexpr float kRescaleThreshold = 8.0f;
 
 struct PParams {
@@ -375,16 +375,16 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
   if (tid == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(&q_full[b], 1);
-      mbar_init(&q_empty[b], kRowThreads);
+      mbar_init(&q_empty[b], kRowWarps);
       mbar_init(&s_ready[b], 1);
     }
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&pv_done[i], 1);
     }
-    mbar_init(p_ready, kRowThreads);
-    mbar_init(o_free, kRowThreads);
-    mbar_init(q_tmem, kRowThreads);
+    mbar_init(p_ready, kRowWarps);
+    mbar_init(o_free, kRowWarps);
+    mbar_init(q_tmem, kRowWarps);
     mbar_init(drain, 1);
     fence_barrier_init();
     abort_flag = 0;
@@ -622,8 +622,11 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
       tmem_st32(lane_addr + kQCol, qv);
       tmem_wait_st();
       tc_fence_before_sync();
-      mbar_arrive(&q_empty[b]);
-      mbar_arrive(q_tmem);
+      __syncwarp();  // every lane's tensor-memory store and fence precede the warp's arrival
+      if (lane == 0) {
+        mbar_arrive(&q_empty[b]);
+        mbar_arrive(q_tmem);
+      }
       return true;
     };
     bool ok = !have || copy_q(0);
@@ -730,7 +733,8 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
         tmem_st32(lane_addr + kSCol + (jt & 1) * kTileN, v[0]);  // P(jt) over S(jt)
         tmem_wait_st();
         tc_fence_before_sync();
-        mbar_arrive(p_ready);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_ready);
       }
       if (!ok) break;
       // ---- epilogue: O / l of this unit, then release O to the next unit's first PV ----
@@ -745,7 +749,8 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
       const uint32_t lsum = tmem_ld1(lane_addr + kLCol);
       tmem_wait_ld();
       tc_fence_before_sync();
-      mbar_arrive(o_free);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free);
       const float inv = 1.f / __uint_as_float(lsum);  // l >= 1: the max key weighs >= 1
       if (row_ok) {
         __nv_bfloat16* dst = p.out + (static_cast<int64_t>(cur.q0 + token) * p.num_q_heads +
