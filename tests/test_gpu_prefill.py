@@ -128,3 +128,24 @@ def test_long_chunk_every_row():
     ref = oracle_prefill_rows(wl.bf16_bits(hv["q_prefill"]), w.prefill_query_start_loc, kc, vc,
                               w.block_tables, w.context_lens, w.scale)
     check(out, ref, "long chunk, every row")
+
+
+def test_many_chunks_beyond_the_in_kernel_sort():
+    """2200 short chunks (2..60 rows over 0..120 prior tokens): more (sequence, query tile)
+    pairs than the in-kernel sort takes, so the persistent kernel serves its units in grid
+    order; every row against the oracle."""
+    rng = np.random.default_rng(55)
+    n = 2200
+    chunk = rng.integers(2, 61, size=n)
+    prior = rng.integers(0, 121, size=n)
+    w = wl.make_workload("many_chunks", prior, chunk, num_prefill=n, seed=55, pool_slack=0.2)
+    pairs = int(((chunk + 31) // 32).sum())
+    assert pairs > 2048
+    step = GpuStep(w)
+    out = step.prefill()
+    assert step.check_status() == pa.PA_OK
+    hv = host_vals(step.vals)
+    kc, vc = oracle_pools(w, hv)
+    ref = oracle_prefill_rows(wl.bf16_bits(hv["q_prefill"]), w.prefill_query_start_loc, kc, vc,
+                              w.block_tables, w.context_lens, w.scale)
+    check(out, ref, "many chunks, grid order")
