@@ -4,9 +4,10 @@ It serves callers that cannot allocate device memory, for example a plug-in whos
 program owns every device allocation, or code that must not call cudaMalloc while
 serving because that call can stall the device.  The tests call it through the C ABI and
 compare it with pa_decode (the entry point that takes a caller workspace) and with the
-oracle, on calls in a row: two balanced-split calls whose split sequences are merged
-inside the kernel (the second one relies on the piece counters the first one left at
-zero in the shared array), then a fixed-partition call.  This file sorts last so that a
+oracle, on calls in a row: two balanced-split calls of different batch sizes whose split
+sequences are merged inside the kernel (the second runs on the array the first one
+filled: where its piece counters sit depends on the batch size, so each call clears
+them), then a fixed-partition call.  This file sorts last so that a
 run stopping at the first failure has run every other test first.
 """
 import numpy as np
@@ -46,7 +47,7 @@ def test_static_scratch_matches_workspace_decode_and_oracle_on_calls_in_a_row():
     a = GpuStep(wl.decode_batch64_uniform())                   # 64 sequences, in-kernel merge
     b = GpuStep(wl.random_small(17, num_seqs=9, max_ctx=700))  # ragged, in-kernel merge
     outs = [(a, 0, _static_decode(a, 0)),
-            (b, 0, _static_decode(b, 0)),     # reuses the counters call 1 left at zero
+            (b, 0, _static_decode(b, 0)),     # counters where call 1 wrote offsets
             (b, 64, _static_decode(b, 64))]   # fixed 64-token runs, separate merge kernel
     torch.cuda.synchronize()
     refs = {id(s): oracle_step(s.w, host_vals(s.vals))["decode"] for s in (a, b)}
