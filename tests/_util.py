@@ -31,8 +31,8 @@ def read_golden(name):
 def oracle_pools(w: wl.Workload, vals: dict, include_new=True):
     """Build the oracle's own K/V pools: NaN-poisoned, history stored, then (optionally)
     this step's new tokens, each through the oracle's slot mapping and scatter."""
-    kc = wl.nan_pool(w.num_blocks)
-    vc = wl.nan_pool(w.num_blocks)
+    kc = wl.nan_pool(w.num_blocks, w.num_kv_heads)
+    vc = wl.nan_pool(w.num_blocks, w.num_kv_heads)
     hist_ctx = w.hist_lens
     slots, err = oracle.slot_mapping(w.block_tables, hist_ctx, w.hist_start_loc, w.num_blocks)
     assert err == 0

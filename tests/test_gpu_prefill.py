@@ -149,3 +149,24 @@ def test_many_chunks_beyond_the_in_kernel_sort():
     ref = oracle_prefill_rows(wl.bf16_bits(hv["q_prefill"]), w.prefill_query_start_loc, kc, vc,
                               w.block_tables, w.context_lens, w.scale)
     check(out, ref, "many chunks, grid order")
+
+
+@pytest.mark.parametrize("hkv", [1, 2, 16])
+def test_other_kv_head_counts(hkv):
+    """Chunks with 1, 2 and 16 K/V heads (4 query heads each): the work units are (query
+    tile, K/V head) pairs, so the head count changes how many units each persistent CTA
+    serves (16 heads: more units than CTAs).  Every row against the oracle."""
+    rng = np.random.default_rng(60 + hkv)
+    n = 6
+    prior = rng.integers(0, 400, size=n)
+    chunk = rng.integers(20, 160, size=n)
+    w = wl.make_workload(f"hkv{hkv}", prior, chunk, num_prefill=n, seed=60 + hkv,
+                         pool_slack=0.3, num_kv_heads=hkv, num_q_heads=4 * hkv)
+    step = GpuStep(w)
+    out = step.prefill()
+    assert step.check_status() == pa.PA_OK
+    hv = host_vals(step.vals)
+    kc, vc = oracle_pools(w, hv)
+    ref = oracle_prefill_rows(wl.bf16_bits(hv["q_prefill"]), w.prefill_query_start_loc, kc, vc,
+                              w.block_tables, w.context_lens, w.scale)
+    check(out, ref, w.name)

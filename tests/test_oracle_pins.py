@@ -331,3 +331,27 @@ def test_row_range_split_of_chunks_is_bit_identical_to_one_call():
     assert np.array_equal(dec, oracle_decode_rows(qd, kc, vc, w.decode_block_tables,
                                                   w.decode_context_lens, w.scale,
                                                   seqs_per_task=1))
+
+
+def test_oracle_handles_other_kv_head_counts():
+    """With 2 K/V heads and 8 query heads the oracle's chunk attention equals torch SDPA
+    (float64, causal over each chunk's positions) on dense K/V."""
+    w = wl.make_workload("hkv2", [30, 5], [12, 20], num_prefill=2, seed=9, pool_slack=0.5,
+                         num_kv_heads=2, num_q_heads=8)
+    vals = w.values(0)
+    kc, vc = oracle_pools(w, vals)
+    assert kc.shape[1] == 2
+    out, err = oracle.prefill_chunk(wl.bf16_bits(vals["q_prefill"]), w.prefill_query_start_loc,
+                                    kc, vc, w.block_tables, w.context_lens, w.scale)
+    assert err == 0
+    qsl = w.prefill_query_start_loc
+    for s in range(2):
+        k, v = dense_kv(w, vals, s)  # [Hkv, L, D]
+        L = int(w.context_lens[s])
+        q_len = int(qsl[s + 1] - qsl[s])
+        q = vals["q_prefill"][qsl[s]:qsl[s + 1]].to(torch.float64).transpose(0, 1)  # [Hq, q, D]
+        pos = torch.arange(L - q_len, L)[:, None]
+        mask = torch.arange(L)[None, :] <= pos
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            q[None], k[None], v[None], attn_mask=mask, scale=w.scale, enable_gqa=True)[0]
+        assert np.abs(out[qsl[s]:qsl[s + 1]] - ref.transpose(0, 1).numpy()).max() < 1e-12
