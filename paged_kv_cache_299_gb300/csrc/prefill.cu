@@ -70,7 +70,7 @@ constexpr int kKOff = kQOff + 2 * kQBytes;
 constexpr int kVOff = kKOff + kStages * kKVBytes;
 constexpr int kOnesOff = kVOff + kStages * kKVBytes;
 constexpr int kBarOff = kOnesOff + kOnesBytes;
-constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 1 + 1 + 1 + 1;  // 18
+constexpr int kNumBars = 2 + 2 + 2 * kStages + 2 + 2 + 1 + 1 + 1;  // 19
 constexpr int kMiscOff = kBarOff + 24 * 8;
 constexpr int kUnitOff = kMiscOff + 128;  // misc: TMEM address, abort flag, unit count, 24 ints of scratch
 constexpr int kSmemBytes = kUnitOff + 2 * kMaxUnitsPerCta * 4;
@@ -360,8 +360,11 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
   // sum are up to date).  Tile jt is phase jt / kStages of pv_done[jt % kStages].
   uint64_t* pv_done = kv_full + kStages;
   uint64_t* s_ready = pv_done + kStages;  // [2]
+  // p_ready[b]: P of the tile in S buffer b is in tensor memory (phase jt / 2 for tile jt).
+  // Per buffer, so the issuing thread can never fall two phases behind: P(jt+2) needs
+  // S(jt+2), which is issued only after the wait for P(jt).
   uint64_t* p_ready = s_ready + 2;
-  uint64_t* o_free = p_ready + 1;  // the epilogue has read O out of tensor memory
+  uint64_t* o_free = p_ready + 2;  // the epilogue has read O out of tensor memory
   uint64_t* q_tmem = o_free + 1;   // this unit's Q is in tensor memory
   uint64_t* drain = q_tmem + 1;
   int* misc = reinterpret_cast<int*>(smem + kMiscOff);
@@ -382,7 +385,8 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
       mbar_init(&kv_full[i], 1);
       mbar_init(&pv_done[i], 1);
     }
-    mbar_init(p_ready, kRowWarps);
+    mbar_init(&p_ready[0], kRowWarps);
+    mbar_init(&p_ready[1], kRowWarps);
     mbar_init(o_free, kRowWarps);
     mbar_init(q_tmem, kRowWarps);
     mbar_init(drain, 1);
@@ -572,7 +576,8 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
             }
           }
           if (!ok) break;
-          if (!(ok = wait_or_abort(p_ready, static_cast<uint32_t>(jt & 1), &abort_flag, p.status)))
+          if (!(ok = wait_or_abort(&p_ready[jt & 1], static_cast<uint32_t>((jt >> 1) & 1),
+                                   &abort_flag, p.status)))
             break;
           if (j == 0 && kq > 0) {  // O is overwritten: the last unit's epilogue has read it
             if (!(ok = wait_or_abort(o_free, static_cast<uint32_t>((kq - 1) & 1), &abort_flag,
@@ -700,17 +705,18 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
           }
           fence_proxy_async_smem();
         }
-        if (jt > 0) {
-          // PV(jt-1) is done with O and its row sum before they are rescaled or P(jt) is
-          // published.  The barrier of its stage is at most one phase from the one waited
-          // for: PV(jt-2) has completed (before S(jt) did) and PV(jt+3) needs P(jt+3).
+        if (j > 0 && __any_sync(0xffffffffu, grow)) {
+          // O and its row sum are rescaled once PV(jt-1) is done with them.  Only a rescale
+          // waits for it: P(jt) itself overwrites its own S buffer, whose last reader PV(jt-2)
+          // completed before S(jt) did.  Skipping the wait on other tiles is safe because
+          // the barrier is per stage: its previous phase (PV(jt-5)) was observed by the
+          // producer before tile jt-1 was loaded, and its next one needs P(jt+3), so the
+          // parity wait below cannot alias a phase two away.
           ok = wait_or_abort(&pv_done[(jt - 1) % kStages],
                              static_cast<uint32_t>(((jt - 1) / kStages) & 1), &abort_flag, p.status);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           tc_fence_after_sync();
-        }
-        if (j > 0 && __any_sync(0xffffffffu, grow)) {
           uint32_t(&o)[32] = v[1];  // the raw scores there are spent
           const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
@@ -734,7 +740,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
         tmem_wait_st();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_ready);
+        if (lane == 0) mbar_arrive(&p_ready[jt & 1]);
       }
       if (!ok) break;
       // ---- epilogue: O / l of this unit, then release O to the next unit's first PV ----
