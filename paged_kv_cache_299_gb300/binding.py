@@ -328,8 +328,9 @@ def pa_varlen_workspace_size(num_seqs, num_query_tokens) -> int:
 def pa_attention_varlen(out, q, query_start_loc, max_query_len, key_cache, value_cache,
                         block_tables, context_lens, scale, workspace=None, device_status=None,
                         stream=None):
-    """One continuous-batching step's attention (decode rows and causal chunks mixed) in one
-    attention launch over a work-sorted item list; same results as pa_prefill_chunk."""
+    """One continuous-batching step's attention (decode rows and causal chunks mixed): decode
+    rows on the decode kernel, chunks on the tensor-core chunk kernel; chunk rows equal
+    pa_prefill_chunk's bit for bit, decode rows pa_decode's up to rounding."""
     _need(out, "out", torch.bfloat16, 3)
     _need(q, "q", torch.bfloat16, 3)
     _need(query_start_loc, "query_start_loc", torch.int32, 1)

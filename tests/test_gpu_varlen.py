@@ -1,7 +1,8 @@
 """Unified varlen launch ("vLLM", Continuous Batching: decode rows and prefill chunks of
 different sequences share one step): pa_attention_varlen over a mixed batch must equal the
-oracle's causal chunk attention for every row (a q_len = 1 sequence is a decode row), and
-be bit-identical to pa_prefill_chunk, whatever the order of the sequences."""
+oracle's causal chunk attention for every row (a q_len = 1 sequence is a decode row),
+whatever the order of the sequences; its chunk rows come from the tensor-core kernel and
+are bit-identical to pa_prefill_chunk, its decode rows from the decode kernel."""
 import numpy as np
 import pytest
 import torch
