@@ -123,6 +123,25 @@ pa_status pa_reshape_and_cache(const void* key, const void* value,
 size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_heads,
                                 int32_t max_context_len, int32_t partition_tokens);
 
+/* Launch flags of pa_decode and pa_decode_append.
+ * PA_LAUNCH_OVERLAP_PREVIOUS lets the launch begin while the kernel before it in the stream
+ * is still running (programmatic dependent launch), which hides the launch's start-up (the
+ * block-table prefix and the first K/V tiles in flight) behind that kernel's last
+ * CTAs; it carries on the launch-overhead removal of "vLLM" (blog.rlaisqls.com), section
+ * CUDA Graph.  Such a launch reads block_tables, context_lens and the first K/V tiles of
+ * both pools before that kernel has finished, and everything else (queries, new K/V rows,
+ * outputs, workspace, device_status) only after it has finished and its writes are
+ * visible.  So set it only when the kernel before it in the stream writes neither the
+ * block tables nor the context lengths nor the K/V pools this call reads; the decode
+ * kernels of consecutive layers of one step qualify (each layer has its own pools), a
+ * store into the same pools (pa_reshape_and_cache, pa_copy_blocks, a previous
+ * pa_decode_append on the same layer) does not.  The decode kernels of this library let a
+ * following launch that carries the flag start early; a launch without it waits for the
+ * previous kernel as usual.  Also valid inside CUDA graph capture.  Unknown bits are
+ * rejected (PA_ERR_INVALID_ARG). */
+#define PA_LAUNCH_DEFAULT 0u
+#define PA_LAUNCH_OVERLAP_PREVIOUS 1u
+
 /* Paged decode attention.  Defined by: "vLLM" (blog.rlaisqls.com), section Flash Attention
  * (S = Q K^T, P = softmax(S), O = P V, evaluated block by block with a running max and sum),
  * section PagedAttention (the K/V of a sequence are found through its block table), and
@@ -146,13 +165,15 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t 
  *                    in equal numbers per streaming warp)
  *   workspace        zero-initialised device buffer of >= pa_decode_workspace_size(...)
  *                    bytes (see pa_decode_workspace_size)
+ *   launch_flags     PA_LAUNCH_DEFAULT or PA_LAUNCH_OVERLAP_PREVIOUS (see there)
  * num_seqs == 0 is a no-op.  At most 4096 sequences per call. */
 pa_status pa_decode(void* out, const void* q, const void* key_cache, const void* value_cache,
                     pa_cache_desc cd, const int32_t* block_tables,
                     int32_t max_blocks_per_seq, const int32_t* context_lens,
                     int32_t num_seqs, int32_t num_q_heads, float scale,
                     int32_t max_context_len, int32_t partition_tokens, void* workspace,
-                    size_t workspace_bytes, int32_t* device_status, pa_stream_t stream);
+                    size_t workspace_bytes, uint32_t launch_flags, int32_t* device_status,
+                    pa_stream_t stream);
 
 /* Decode with the store of the new tokens fused in: for every sequence s, the token at
  * position context_lens[s] - 1 (key[s][h][:], value[s][h][:], bf16 [num_seqs][Hkv][D]) is
@@ -167,8 +188,8 @@ pa_status pa_decode_append(void* out, const void* q, const void* key, const void
                            const int32_t* block_tables, int32_t max_blocks_per_seq,
                            const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
                            float scale, int32_t max_context_len, int32_t partition_tokens,
-                           void* workspace, size_t workspace_bytes, int32_t* device_status,
-                           pa_stream_t stream);
+                           void* workspace, size_t workspace_bytes, uint32_t launch_flags,
+                           int32_t* device_status, pa_stream_t stream);
 
 /* Causal chunked-prefill attention over a paged prefix.  Defined by: "tiny-vllm (1)"
  * (geonuchoi.com), section 1 (decoder-only causal attention: position t attends positions

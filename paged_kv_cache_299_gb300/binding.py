@@ -40,6 +40,9 @@ PA_ERR_OUT_OF_BLOCKS = -7
 DEVFLAG_BAD_BLOCK, DEVFLAG_BAD_SLOT, DEVFLAG_BAD_CONTEXT, DEVFLAG_TIMEOUT = 1, 2, 4, 8
 # Size of the library-owned device scratch of pa_decode_static_scratch (bytes).
 PA_DECODE_STATIC_SCRATCH_BYTES = 8 << 20
+# Launch flags of pa_decode / pa_decode_append (include/pagedkv.h states the contract).
+PA_LAUNCH_DEFAULT = 0
+PA_LAUNCH_OVERLAP_PREVIOUS = 1
 
 # Every symbol include/pagedkv.h declares.
 EXPORTED = ("pa_compute_slot_mapping", "pa_reshape_and_cache", "pa_decode_workspace_size",
@@ -73,8 +76,9 @@ def load(path: str | None = None):
     lib.pa_reshape_and_cache.restype = st
     lib.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32]
     lib.pa_decode_workspace_size.restype = sz
+    u32 = ctypes.c_uint32
     lib.pa_decode.argtypes = [P, P, P, P, CacheDesc, P, i32, P, i32, i32, f32, i32, i32, P, sz,
-                              P, P]
+                              u32, P, P]
     lib.pa_decode.restype = st
     lib.pa_prefill_chunk.argtypes = [P, P, P, i32, i32, P, P, CacheDesc, P, i32, P, i32, i32,
                                      f32, P, P]
@@ -88,7 +92,7 @@ def load(path: str | None = None):
                                              i32, i32, P, P]
     lib.pa_decode_static_scratch.restype = st
     lib.pa_decode_append.argtypes = [P, P, P, P, P, P, CacheDesc, P, i32, P, i32, i32, f32, i32,
-                                     i32, P, sz, P, P]
+                                     i32, P, sz, u32, P, P]
     lib.pa_decode_append.restype = st
     lib.pa_copy_blocks.argtypes = [P, P, CacheDesc, P, i32, P, P]
     lib.pa_copy_blocks.restype = st
@@ -213,8 +217,9 @@ def pa_decode_workspace_size(num_seqs, num_kv_heads, num_q_heads, max_context_le
 
 def pa_decode(out, q, key_cache, value_cache, block_tables, context_lens, scale,
               max_context_len, partition_tokens=0, workspace=None, device_status=None,
-              stream=None):
-    """Paged decode attention; writes out [S, Hq, D] (bf16)."""
+              stream=None, launch_flags=PA_LAUNCH_DEFAULT):
+    """Paged decode attention; writes out [S, Hq, D] (bf16).  launch_flags: see
+    PA_LAUNCH_OVERLAP_PREVIOUS in include/pagedkv.h."""
     _need(out, "out", torch.bfloat16, 3)
     _need(q, "q", torch.bfloat16, 3)
     _need(key_cache, "key_cache", torch.bfloat16, 4)
@@ -234,16 +239,17 @@ def pa_decode(out, q, key_cache, value_cache, block_tables, context_lens, scale,
                           cache_desc(key_cache), _ptr(block_tables), block_tables.shape[1],
                           _ptr(context_lens), num_seqs, hq, float(scale), int(max_context_len),
                           int(partition_tokens), _ptr(workspace), workspace.numel(),
-                          _ptr(device_status), _stream(stream))
+                          int(launch_flags), _ptr(device_status), _stream(stream))
     _check(st, "pa_decode")
     return out
 
 
 def pa_decode_append(out, q, key, value, key_cache, value_cache, block_tables, context_lens,
                      scale, max_context_len, partition_tokens=0, workspace=None,
-                     device_status=None, stream=None):
+                     device_status=None, stream=None, launch_flags=PA_LAUNCH_DEFAULT):
     """Store each sequence's newest token (key/value [S, Hkv, D]) and run paged decode
-    attention, in one launch; bit-identical to pa_reshape_and_cache + pa_decode."""
+    attention, in one launch; bit-identical to pa_reshape_and_cache + pa_decode.
+    launch_flags: see PA_LAUNCH_OVERLAP_PREVIOUS in include/pagedkv.h."""
     _need(out, "out", torch.bfloat16, 3)
     _need(q, "q", torch.bfloat16, 3)
     _need(key, "key", torch.bfloat16, 3)
@@ -266,8 +272,8 @@ def pa_decode_append(out, q, key, value, key_cache, value_cache, block_tables, c
                                  _ptr(value_cache), cache_desc(key_cache), _ptr(block_tables),
                                  block_tables.shape[1], _ptr(context_lens), num_seqs, hq,
                                  float(scale), int(max_context_len), int(partition_tokens),
-                                 _ptr(workspace), workspace.numel(), _ptr(device_status),
-                                 _stream(stream))
+                                 _ptr(workspace), workspace.numel(), int(launch_flags),
+                                 _ptr(device_status), _stream(stream))
     _check(st, "pa_decode_append")
     return out
 

@@ -139,7 +139,8 @@ static pa_status decode_impl(void* out, const void* q, const void* k_new, const 
                     int32_t max_blocks_per_seq, const int32_t* context_lens,
                     int32_t num_seqs, int32_t num_q_heads, float scale,
                     int32_t max_context_len, int32_t partition_tokens, void* workspace,
-                    size_t workspace_bytes, int32_t* device_status, pa_stream_t stream) {
+                    size_t workspace_bytes, uint32_t launch_flags, int32_t* device_status,
+                    pa_stream_t stream) {
   pa_status st = check_desc(cd);
   if (st != PA_OK) return st;
   st = check_decode_sizes(num_seqs, cd.num_kv_heads, num_q_heads, max_context_len,
@@ -155,6 +156,8 @@ static pa_status decode_impl(void* out, const void* q, const void* k_new, const 
   if (!(scale > 0.f) || !isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale %g", scale);
   if ((k_new == nullptr) != (v_new == nullptr) || (k_new && (!aligned16(k_new) || !aligned16(v_new))))
     return fail(PA_ERR_INVALID_ARG, "k_new / v_new: both or neither, 16-byte aligned");
+  if (launch_flags & ~static_cast<uint32_t>(PA_LAUNCH_OVERLAP_PREVIOUS))
+    return fail(PA_ERR_INVALID_ARG, "unknown launch flags 0x%x", launch_flags);
   pkv::DecodePlan plan;
   cudaError_t e = pkv::plan_decode(num_seqs, cd.num_kv_heads, num_q_heads, max_context_len,
                                    partition_tokens, &plan);
@@ -179,6 +182,7 @@ static pa_status decode_impl(void* out, const void* q, const void* k_new, const 
   a.status = device_status;
   a.k_new = k_new;
   a.v_new = v_new;
+  a.overlap_previous = (launch_flags & PA_LAUNCH_OVERLAP_PREVIOUS) != 0;
   return from_cuda(pkv::launch_decode(a, plan, reinterpret_cast<cudaStream_t>(stream)),
                    "decode launch");
 }
@@ -188,11 +192,12 @@ pa_status pa_decode(void* out, const void* q, const void* key_cache, const void*
                     int32_t max_blocks_per_seq, const int32_t* context_lens,
                     int32_t num_seqs, int32_t num_q_heads, float scale,
                     int32_t max_context_len, int32_t partition_tokens, void* workspace,
-                    size_t workspace_bytes, int32_t* device_status, pa_stream_t stream) {
+                    size_t workspace_bytes, uint32_t launch_flags, int32_t* device_status,
+                    pa_stream_t stream) {
   return decode_impl(out, q, nullptr, nullptr, key_cache, value_cache, cd, block_tables,
                      max_blocks_per_seq, context_lens, num_seqs, num_q_heads, scale,
                      max_context_len, partition_tokens, workspace, workspace_bytes,
-                     device_status, stream);
+                     launch_flags, device_status, stream);
 }
 
 pa_status pa_decode_append(void* out, const void* q, const void* key, const void* value,
@@ -200,13 +205,13 @@ pa_status pa_decode_append(void* out, const void* q, const void* key, const void
                            const int32_t* block_tables, int32_t max_blocks_per_seq,
                            const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
                            float scale, int32_t max_context_len, int32_t partition_tokens,
-                           void* workspace, size_t workspace_bytes, int32_t* device_status,
-                           pa_stream_t stream) {
+                           void* workspace, size_t workspace_bytes, uint32_t launch_flags,
+                           int32_t* device_status, pa_stream_t stream) {
   if (num_seqs > 0 && (!key || !value)) return fail(PA_ERR_INVALID_ARG, "null key/value");
   return decode_impl(out, q, key, value, key_cache, value_cache, cd, block_tables,
                      max_blocks_per_seq, context_lens, num_seqs, num_q_heads, scale,
                      max_context_len, partition_tokens, workspace, workspace_bytes,
-                     device_status, stream);
+                     launch_flags, device_status, stream);
 }
 
 namespace {

@@ -459,6 +459,10 @@ template <int GROUP, bool kRows>
 __global__ void __launch_bounds__(kWarps * 32, 1)
 paged_decode_kernel(const KParams p) {
   constexpr int kThreads = kWarps * 32;
+  // A launch that follows in the stream with programmatic dependent launch enabled may
+  // start as soon as SMs free up; it waits for this grid before it reads what this grid
+  // writes (griddepcontrol.wait below).  No effect on launches without that attribute.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -555,24 +559,6 @@ paged_decode_kernel(const KParams p) {
   __syncthreads();
 
   const int64_t total = static_cast<int64_t>(seq_base[S]) * KV;
-  if (blockIdx.x == 0) {
-    for (int i = tid; i <= S; i += kThreads) p.ws_seq_base[i] = seq_base[i];
-    if (tid == 0) {
-      *p.ws_total = total;
-      if ((p.chunk > 0 && static_cast<int64_t>(p.grid) * p.chunk < total) ||
-          (p.tile_bound > 0 && total > p.tile_bound))
-        flag_error(p.status, PA_DEVFLAG_BAD_CONTEXT);  // contexts beyond max_context_len
-    }
-  }
-  if (p.fused_merge && blockIdx.x == 0 && !kRows) {
-    // empty contexts: zero rows (no tile writes them)
-    const int row_elems = p.num_q_heads * kHeadDim;
-    for (int s0 = 0; s0 < S; ++s0) {
-      if (seq_base[s0 + 1] != seq_base[s0]) continue;
-      __nv_bfloat16* out = p.out + static_cast<int64_t>(s0) * row_elems;
-      for (int e = tid; e < row_elems; e += kThreads) out[e] = __float2bfloat16_rn(0.f);
-    }
-  }
   // From here on every warp works alone: no block-wide synchronisation below.
   const int64_t total_warps = static_cast<int64_t>(gridDim.x) * kWarps;
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
@@ -643,6 +629,30 @@ paged_decode_kernel(const KParams p) {
     ++cur_i;
   };
   for (int i = 0; i < kStagesPerWarp; ++i) issue_one();
+
+  // Everything above reads only block_tables, context_lens (q_rows) and K/V tiles.  Under
+  // programmatic dependent launch the previous kernel in the stream may still be running
+  // here; wait for it (and its memory) before reading queries or new K/V rows and before
+  // writing outputs or the workspace.  Without that launch attribute this returns at once.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (blockIdx.x == 0 && warp == 0) {  // warp 0 of CTA 0 always runs (grid >= 1 run)
+    for (int i = lane; i <= S; i += 32) p.ws_seq_base[i] = seq_base[i];
+    if (lane == 0) {
+      *p.ws_total = total;
+      if ((p.chunk > 0 && static_cast<int64_t>(p.grid) * p.chunk < total) ||
+          (p.tile_bound > 0 && total > p.tile_bound))
+        flag_error(p.status, PA_DEVFLAG_BAD_CONTEXT);  // contexts beyond max_context_len
+    }
+    if (p.fused_merge && !kRows) {
+      // empty contexts: zero rows (no tile writes them)
+      const int row_elems = p.num_q_heads * kHeadDim;
+      for (int s0 = 0; s0 < S; ++s0) {
+        if (seq_base[s0 + 1] != seq_base[s0]) continue;
+        __nv_bfloat16* out = p.out + static_cast<int64_t>(s0) * row_elems;
+        for (int e = lane; e < row_elems; e += 32) out[e] = __float2bfloat16_rn(0.f);
+      }
+    }
+  }
 
   // ---- consume side: same runs, piece by piece ----
   int waited = 0;  // tiles whose data this warp has waited for (stage = waited % stages)
@@ -1029,11 +1039,21 @@ cudaError_t launch(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t str
   p.status = a.status;
   p.q_rows = a.q_rows;
   p.num_query_tokens = a.num_query_tokens;
-  if (a.q_rows != nullptr)
-    paged_decode_kernel<GROUP, true><<<plan.grid, kWarps * 32, plan.smem_bytes, stream>>>(p);
-  else
-    paged_decode_kernel<GROUP, false><<<plan.grid, kWarps * 32, plan.smem_bytes, stream>>>(p);
-  e = cudaGetLastError();
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.grid);
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.dynamicSmemBytes = plan.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = a.overlap_previous ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = a.q_rows != nullptr ? cudaLaunchKernelEx(&cfg, paged_decode_kernel<GROUP, true>, p)
+                            : cudaLaunchKernelEx(&cfg, paged_decode_kernel<GROUP, false>, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
+  }
   if (e != cudaSuccess || plan.fused_merge) return e;
   const dim3 mgrid(a.num_kv_heads, a.num_seqs);
   if (a.q_rows != nullptr)

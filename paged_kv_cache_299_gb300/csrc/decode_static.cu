@@ -134,5 +134,5 @@ extern "C" pa_status pa_decode_static_scratch(
   return pa_decode(out, q, key_cache, value_cache, cd, block_tables, max_blocks_per_seq,
                    context_lens, num_seqs, num_q_heads, scale, max_context_len,
                    partition_tokens, scratch, num_seqs > 0 ? kScratchBytes : 0,
-                   device_status, stream);
+                   PA_LAUNCH_DEFAULT, device_status, stream);
 }

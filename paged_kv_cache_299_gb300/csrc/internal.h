@@ -65,6 +65,10 @@ struct DecodeArgs {
   const int32_t* q_rows = nullptr;  // mixed batch: query/output row per sequence (prefix sums
                                     // of q_len); only q_len == 1 sequences are served
   int32_t num_query_tokens = 0;
+  // Programmatic dependent launch: the kernel may start before the previous kernel in the
+  // stream has finished; it reads block_tables, context_lens (and q_rows) and its first
+  // K/V tiles before waiting for that kernel, everything else after.
+  bool overlap_previous = false;
 };
 
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream);

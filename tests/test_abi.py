@@ -65,16 +65,20 @@ def test_host_rejects_bad_arguments_without_touching_the_device():
                                        None) == pa.PA_ERR_INVALID_ARG
     # decode: group of 3 unsupported, partition not a multiple of 16, too many sequences
     args = [fake, fake, fake, fake, _desc(), fake, 4, fake]
-    assert lib.pa_decode(*args, 2, 24, ctypes.c_float(0.125), 64, 0, fake, 1 << 20, None,
+    assert lib.pa_decode(*args, 2, 24, ctypes.c_float(0.125), 64, 0, fake, 1 << 20, 0, None,
                          None) == pa.PA_ERR_UNSUPPORTED
-    assert lib.pa_decode(*args, 2, 32, ctypes.c_float(0.125), 64, 24, fake, 1 << 20, None,
+    assert lib.pa_decode(*args, 2, 32, ctypes.c_float(0.125), 64, 24, fake, 1 << 20, 0, None,
                          None) == pa.PA_ERR_INVALID_ARG
-    assert lib.pa_decode(*args, 5000, 32, ctypes.c_float(0.125), 64, 0, fake, 1 << 20, None,
+    assert lib.pa_decode(*args, 5000, 32, ctypes.c_float(0.125), 64, 0, fake, 1 << 20, 0, None,
                          None) == pa.PA_ERR_UNSUPPORTED
-    assert lib.pa_decode(*args, 0, 32, ctypes.c_float(0.125), 64, 0, None, 0, None,
+    assert lib.pa_decode(*args, 0, 32, ctypes.c_float(0.125), 64, 0, None, 0, 0, None,
                          None) == pa.PA_OK
-    assert lib.pa_decode(*args, 2, 32, ctypes.c_float(-1.0), 64, 0, fake, 1 << 20, None,
+    assert lib.pa_decode(*args, 2, 32, ctypes.c_float(-1.0), 64, 0, fake, 1 << 20, 0, None,
                          None) == pa.PA_ERR_INVALID_ARG
+    # launch flags: unknown bits are rejected before any launch
+    assert lib.pa_decode(*args, 2, 32, ctypes.c_float(0.125), 64, 0, fake, 1 << 20, 2, None,
+                         None) == pa.PA_ERR_INVALID_ARG
+    assert b"launch flags" in lib.pa_last_error()
     # prefill needs group 4
     assert lib.pa_prefill_chunk(fake, fake, fake, 16, 8, fake, fake, _desc(), fake, 4, fake, 2,
                                 8, ctypes.c_float(0.125), None, None) == pa.PA_ERR_UNSUPPORTED
@@ -131,3 +135,11 @@ def test_static_scratch_size_matches_the_header():
     m = re.search(r"#define PA_DECODE_STATIC_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)", text)
     assert m, "PA_DECODE_STATIC_SCRATCH_BYTES not found in the header"
     assert int(m.group(1)) << int(m.group(2)) == pa.PA_DECODE_STATIC_SCRATCH_BYTES
+
+
+def test_launch_flags_match_the_header():
+    text = open(HEADER).read()
+    for name in ("PA_LAUNCH_DEFAULT", "PA_LAUNCH_OVERLAP_PREVIOUS"):
+        m = re.search(r"#define %s (\d+)u" % name, text)
+        assert m, name + " not found in the header"
+        assert int(m.group(1)) == getattr(pa, name)

@@ -1,0 +1,89 @@
+"""Decode launches that overlap the kernel before them (PA_LAUNCH_OVERLAP_PREVIOUS,
+programmatic dependent launch).  A decode step over several layers, each layer with its
+own pools and the launches after the first carrying the flag, must give the same bits as
+the same step without the flag, eagerly and replayed from a CUDA graph, and must agree
+with the oracle.  The layers share one workspace, so a launch that touched it before the
+previous layer had finished would show up as wrong rows."""
+import pytest
+import torch
+
+from paged_kv_cache_299_gb300 import binding as pa
+from paged_kv_cache_299_gb300 import graphs
+from paged_kv_cache_299_gb300 import workloads as wl
+from _gpu import GpuStep, host_vals, oracle_step
+from _util import ATOL_MAX, ATOL_MEAN, errors
+
+pytestmark = pytest.mark.gpu
+
+LAYERS = 4
+
+
+def _layers(w):
+    # history only: every run below appends the step's token itself (an idempotent store)
+    return [GpuStep(w, layer, store_new=False) for layer in range(LAYERS)]
+
+
+def _run(steps, outs, ws, partition_tokens, overlap):
+    w = steps[0].w
+    max_ctx = int(w.context_lens.max())
+    for i, st in enumerate(steps):
+        flags = pa.PA_LAUNCH_OVERLAP_PREVIOUS if overlap and i > 0 else pa.PA_LAUNCH_DEFAULT
+        pa.pa_decode_append(outs[i], st.vals["q_decode"], st.vals["new_k"], st.vals["new_v"],
+                            st.kc, st.vc, st.bt, st.ctx, w.scale, max_ctx, partition_tokens,
+                            workspace=ws, device_status=st.status, launch_flags=flags)
+
+
+@pytest.mark.parametrize("name,partition_tokens", [("batch64", 0), ("small_merge", 64),
+                                                   ("batch256", 0)])
+def test_overlapped_layers_match_serial_layers_and_oracle(name, partition_tokens):
+    w = {"batch64": lambda: wl.decode_batch64_uniform(),
+         "small_merge": lambda: wl.random_small(41, num_seqs=9, max_ctx=900),
+         "batch256": lambda: wl.decode_batch256_lognormal(layers=1)}[name]()
+    steps = _layers(w)
+    max_ctx = int(w.context_lens.max())
+    ws = torch.zeros(max(16, pa.pa_decode_workspace_size(w.num_seqs, 8, 32, max_ctx,
+                                                         partition_tokens)),
+                     dtype=torch.uint8, device="cuda")
+    serial = [torch.full_like(st.vals["q_decode"], float("nan")) for st in steps]
+    overlapped = [torch.full_like(st.vals["q_decode"], float("nan")) for st in steps]
+    _run(steps, serial, ws, partition_tokens, overlap=False)
+    for _ in range(3):  # repeated steps: the start-up of one layer meets the tail of another
+        _run(steps, overlapped, ws, partition_tokens, overlap=True)
+        torch.cuda.synchronize()
+        for a, b in zip(serial, overlapped):
+            assert torch.equal(a, b)
+    for st in steps:
+        assert st.check_status() == pa.PA_OK
+    for st, out in zip(steps, overlapped):
+        ref = oracle_step(w, host_vals(st.vals))["decode"]
+        mx, mean = errors(out.float().cpu().numpy(), ref)
+        assert mx <= ATOL_MAX and mean <= ATOL_MEAN, (name, mx, mean)
+
+
+def test_overlapped_layers_replay_from_a_graph():
+    w = wl.decode_batch64_uniform()
+    steps = _layers(w)
+    max_ctx = int(w.context_lens.max())
+    ws = torch.zeros(pa.pa_decode_workspace_size(w.num_seqs, 8, 32, max_ctx, 0),
+                     dtype=torch.uint8, device="cuda")
+    serial = [torch.empty_like(st.vals["q_decode"]) for st in steps]
+    replayed = [torch.full_like(st.vals["q_decode"], float("nan")) for st in steps]
+    _run(steps, serial, ws, 0, overlap=False)
+    graph = graphs.StepGraph(lambda: _run(steps, replayed, ws, 0, overlap=True))
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(serial, replayed):
+        assert torch.equal(a, b)
+
+
+def test_unknown_launch_flags_are_rejected():
+    w = wl.random_small(5, num_seqs=2, max_ctx=40)
+    st = GpuStep(w)
+    out = torch.full_like(st.vals["q_decode"], 7.0)
+    with pytest.raises(pa.PagedKVError) as e:
+        pa.pa_decode(out, st.vals["q_decode"], st.kc, st.vc, st.bt, st.ctx, w.scale,
+                     int(w.context_lens.max()), launch_flags=4)
+    assert e.value.status == pa.PA_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0)  # nothing ran
