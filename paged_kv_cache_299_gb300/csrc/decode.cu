@@ -14,18 +14,24 @@
 //     number of bytes whatever the length mix.  With partition_tokens the runs are at most
 //     that long, in equal numbers per warp.
 //   * Each warp streams its own run through a private 4-stage ring in shared memory: lane
-//     0 issues cp.async.bulk (TMA, non-tensor) copies of the K and V tile, completing on
-//     the stage's mbarrier, and refills a stage as soon as the warp has consumed it.  The
-//     block-table entries are fetched 32 at a time, one window ahead.  No producer warp,
-//     no release barriers, no block-wide synchronisation while streaming.
-//   * Lane 8 tg + dq owns 4 tokens of a tile (tg, tg + 4, tg + 8, tg + 12) and 8 of the
-//     64 dims; q for all GROUP heads stays in registers (pre-scaled by scale * log2 e).
-//     The 8-lane dot products are finished by a reduce-scatter that leaves each lane one
-//     head's score, whose online softmax (running max, running sum) it keeps; the
-//     reference max is raised only when a score exceeds it by more than 2^8.
-//   * When a piece ends, the warp's 4 token-group states are combined by shuffles and
-//     either the final bf16 rows are written (the whole segment in one piece) or an
-//     unnormalised (o, max, sum) partial.  The warp that publishes a segment's last piece
+//     0 issues two tensor-map TMA copies (one 16-row box of each pool, 128-byte swizzle)
+//     completing on the stage's mbarrier, and refills a stage as soon as the warp has
+//     consumed it.  The block-table entries are fetched 32 at a time, one window ahead.
+//     No producer warp, no release barriers, no block-wide synchronisation while
+//     streaming.
+//   * The tile arithmetic is a small dense contraction per warp: the GROUP query heads
+//     sharing a K/V head against 16 tokens, S = Q K^T ([GROUP x 64] x [64 x 16]) and
+//     O += P V ([GROUP x 16] x [16 x 64]).  It runs on the tensor cores as mma.sync
+//     m16n8k16 (bf16 in, fp32 accumulate) with the heads as MMA rows (rows past GROUP are
+//     zero), K and V fragments loaded by ldmatrix from the swizzled tiles without bank
+//     conflicts and P taken from the score accumulators: about 60 instructions per lane
+//     and tile, against some 300 for the same arithmetic on the CUDA cores, which left the
+//     streaming warps issue-bound.  The quad of lanes of head r keeps its online softmax
+//     (running max in log2 units, raised only when a score exceeds it by more than 2^8;
+//     running sum of P as rounded to bf16 for the product).
+//   * When a piece ends, the quad sums its shares of the running sum and either the final
+//     bf16 rows are written (the whole segment in one piece) or an unnormalised (o, max,
+//     sum) partial.  The warp that publishes a segment's last piece
 //     merges its partials (log-sum-exp weights) inside this kernel, with CTA-scope
 //     ordering when all the segment's pieces ran on its CTA; beyond 8192-token contexts
 //     or with fixed partitions merge_partials_kernel does it.
@@ -33,6 +39,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tcgen05.cuh"
 
 namespace pkv {
 
@@ -134,133 +141,123 @@ __device__ __forceinline__ Piece piece_at(const int32_t* base, int num_seqs, int
   return pc;
 }
 
-// Lane layout of a streaming warp: lane = 8 * tg + dq.  Token group tg (0..3) owns tokens
-// tg, tg + 4, tg + 8, tg + 12 of a 16-token tile (one per pass); dim slice dq (0..7) owns
-// dims 8*dq .. 8*dq + 7, one 16-byte chunk of each 128-byte row, so a quarter warp reads
-// one whole row per load and every K/V element is loaded and unpacked exactly once.
-constexpr int kPasses = 4;
-
-// Query head whose score lane `dq` holds after score_for_own_head: the reduce-scatter
-// leaves head (2 * (dq & 1) + ((dq >> 1) & 1)) for GROUP 4, (dq & 1) for GROUP 2, 0 for
-// GROUP 1 (lanes dq and dq ^ 4 hold the same head).  On the low two bits the map is its own
-// inverse, so it also names the lane (within the 8-lane group) that owns a head.
-template <int GROUP>
-__device__ __forceinline__ int own_head(int dq) {
-  if (GROUP == 4) return 2 * (dq & 1) + ((dq >> 1) & 1);
-  if (GROUP == 2) return dq & 1;
-  return 0;
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, int c0, int c1,
+                                                 uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
 }
 
-// Finish the 8-lane dot products of one token: a[h] is this lane's partial over its 8 dims.
-// Returns the full score of own_head(dq).
-template <int GROUP>
-__device__ __forceinline__ float score_for_own_head(const float (&a)[GROUP], int dq) {
-  float keep;
-  if (GROUP == 4) {
-    const bool b0 = dq & 1;
-    const float send0 = b0 ? a[0] : a[2];
-    const float send1 = b0 ? a[1] : a[3];
-    float keep0 = b0 ? a[2] : a[0];
-    float keep1 = b0 ? a[3] : a[1];
-    keep0 += __shfl_xor_sync(0xffffffffu, send0, 1);
-    keep1 += __shfl_xor_sync(0xffffffffu, send1, 1);
-    const bool b1 = dq & 2;
-    const float send = b1 ? keep0 : keep1;
-    keep = (b1 ? keep1 : keep0) + __shfl_xor_sync(0xffffffffu, send, 2);
-  } else if (GROUP == 2) {
-    const bool b0 = dq & 1;
-    keep = (b0 ? a[1] : a[0]) + __shfl_xor_sync(0xffffffffu, b0 ? a[0] : a[1], 1);
-    keep += __shfl_xor_sync(0xffffffffu, keep, 2);
-  } else {
-    keep = a[0] + __shfl_xor_sync(0xffffffffu, a[0], 1);
-    keep += __shfl_xor_sync(0xffffffffu, keep, 2);
+// Tiles arrive through tensor-map copies with the 128-byte swizzle: the 16-byte chunk c of
+// row t (token t, dims 8c .. 8c + 7) sits at t * 128 + ((c ^ (t & 7)) * 16) of its 2 KiB
+// stage half, so the eight rows an ldmatrix phase reads fall on eight distinct bank groups.
+__device__ __forceinline__ uint32_t swz(int t, int c) {
+  return static_cast<uint32_t>(t * kRowBytes + ((c ^ (t & 7)) << 4));
+}
+
+// Lane layout of a streaming warp for the tensor-core tile math (mma.sync m16n8k16, bf16
+// in, fp32 accumulate): r = lane / 4 is the MMA row (query head r of the group; rows past
+// the group and rows 8-15 are zero padding) and q = lane % 4.  S = Q K^T over one 16-token
+// tile is two n-tiles of 8 tokens and four k-steps of 16 dims; O += P V takes P straight
+// from the score accumulators (tokens 2q, 2q+1, 2q+8, 2q+9 of row r) and V through
+// transposing ldmatrix loads; the accumulators of n-tile j hold dims 8j + 2q, 8j + 2q + 1
+// of head r.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0,
+                                          uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// bf16 pair {lo = x, hi = y}
+__device__ __forceinline__ uint32_t pack_bf16x2(float x, float y) {
+  const __nv_bfloat162 b = __floats2bfloat162_rn(x, y);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// One 16-token tile pair held in shared memory (swizzled).  The quad of row r keeps the
+// online-softmax state of head r: m, the running reference maximum in log2 units (raised
+// only when a score exceeds it by more than 2^8; the same in the quad's four lanes), and l,
+// this lane's share of the running sum of the probabilities as rounded for the P V product.
+template <bool TAIL>
+__device__ __forceinline__ void attend_tile(uint32_t kt, uint32_t vt, int lane, int q,
+                                            int valid_tokens, float q_scale,
+                                            const uint32_t (&qa0)[4], const uint32_t (&qa2)[4],
+                                            float& m, float& l, float (&o)[8][4]) {
+  // K: matrix (n-tile j, chunk c) = tokens 8j .. 8j+7, dims 8c .. 8c+7; an x4 load of
+  // chunks 4h .. 4h+3 gives b0/b1 of k-steps 2h and 2h+1.
+  const int lrow = lane & 7, lmat = lane >> 3;
+  uint32_t k00[4], k01[4], k10[4], k11[4];
+  ldsm_x4(kt + swz(lrow, lmat), k00);          // n-tile 0, chunks 0..3
+  ldsm_x4(kt + swz(lrow, 4 + lmat), k01);      // n-tile 0, chunks 4..7
+  ldsm_x4(kt + swz(8 + lrow, lmat), k10);      // n-tile 1, chunks 0..3
+  ldsm_x4(kt + swz(8 + lrow, 4 + lmat), k11);  // n-tile 1, chunks 4..7
+  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+  mma_16816(s0, qa0[0], qa2[0], k00[0], k00[1]);
+  mma_16816(s1, qa0[0], qa2[0], k10[0], k10[1]);
+  mma_16816(s0, qa0[1], qa2[1], k00[2], k00[3]);
+  mma_16816(s1, qa0[1], qa2[1], k10[2], k10[3]);
+  mma_16816(s0, qa0[2], qa2[2], k01[0], k01[1]);
+  mma_16816(s1, qa0[2], qa2[2], k11[0], k11[1]);
+  mma_16816(s0, qa0[3], qa2[3], k01[2], k01[3]);
+  mma_16816(s1, qa0[3], qa2[3], k11[2], k11[3]);
+  // V: matrix (token half kb, n-tile j) = tokens 8kb .. 8kb+7, dims 8j .. 8j+7, loaded
+  // transposed: an x4 load gives b0/b1 of n-tiles j and j+1.  Issued before the softmax so
+  // that their latency overlaps it.
+  uint32_t v[4][4];
+#pragma unroll
+  for (int jp = 0; jp < 4; ++jp)
+    ldsm_x4_trans(vt + swz(8 * (lmat & 1) + lrow, 2 * jp + (lmat >> 1)), v[jp]);
+  float x[4] = {s0[0] * q_scale, s0[1] * q_scale, s1[0] * q_scale, s1[1] * q_scale};
+  uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+  if (TAIL) {
+    const int t0 = 2 * q;
+    if (t0 >= valid_tokens) x[0] = -INFINITY;
+    if (t0 + 1 >= valid_tokens) x[1] = -INFINITY;
+    if (t0 + 8 >= valid_tokens) x[2] = -INFINITY;
+    if (t0 + 9 >= valid_tokens) x[3] = -INFINITY;
+    // rows past the context may hold anything (NaN included): P is 0 there, V must be too
+    vm0 = (t0 < valid_tokens ? 0x0000ffffu : 0u) | (t0 + 1 < valid_tokens ? 0xffff0000u : 0u);
+    vm1 = (t0 + 8 < valid_tokens ? 0x0000ffffu : 0u) | (t0 + 9 < valid_tokens ? 0xffff0000u : 0u);
   }
-  return keep + __shfl_xor_sync(0xffffffffu, keep, 4);
-}
-
-// Value of `v` held by the owner lane of head h in this lane's 8-lane group.
-template <int GROUP>
-__device__ __forceinline__ float from_owner(float v, int lane, int h) {
-  if (GROUP == 1) return v;
-  return __shfl_sync(0xffffffffu, v, (lane & ~7) | own_head<GROUP>(h));
-}
-
-__device__ __forceinline__ void unpack4(uint4 a, float2 (&f)[4]) {
-  f[0] = bf16x2_to_float2(a.x);
-  f[1] = bf16x2_to_float2(a.y);
-  f[2] = bf16x2_to_float2(a.z);
-  f[3] = bf16x2_to_float2(a.w);
-}
-
-// One 16-token tile pair held in shared memory.  The lane keeps the online-softmax state
-// (m, l) of its own head; m is the running reference maximum in log2 units, raised only
-// when a score exceeds it by more than 2^8.  o covers every head of the group on the
-// lane's 8 dims.
-template <int GROUP, bool TAIL>
-__device__ __forceinline__ void attend_tile(const uint8_t* __restrict__ kt,
-                                            const uint8_t* __restrict__ vt, int lane, int tg,
-                                            int dq, int valid_tokens,
-                                            const float2 (&qf)[GROUP][4], float& m, float& l,
-                                            float2 (&o)[GROUP][4]) {
-  // all K loads of the tile first, so their latencies overlap
-  uint4 kr[kPasses];
-#pragma unroll
-  for (int j = 0; j < kPasses; ++j) kr[j] = lds128(kt + (tg + 4 * j) * kRowBytes + dq * 16);
-  float s[kPasses];
-#pragma unroll
-  for (int j = 0; j < kPasses; ++j) {
-    float2 kf[4];
-    unpack4(kr[j], kf);
-    float a[GROUP];
-#pragma unroll
-    for (int h = 0; h < GROUP; ++h) {
-      float2 acc = __fmul2_rn(qf[h][0], kf[0]);
-#pragma unroll
-      for (int i = 1; i < 4; ++i) acc = __ffma2_rn(qf[h][i], kf[i], acc);
-      a[h] = acc.x + acc.y;
-    }
-    s[j] = score_for_own_head<GROUP>(a, dq);
-    if (TAIL && tg + 4 * j >= valid_tokens) s[j] = -INFINITY;
-  }
-  uint4 vr[kPasses];  // V loads overlap the softmax below
-#pragma unroll
-  for (int j = 0; j < kPasses; ++j) vr[j] = lds128(vt + (tg + 4 * j) * kRowBytes + dq * 16);
-  const float mt = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
+  float mt = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+  mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+  mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
   const bool grow = mt - m > kRescaleThreshold;  // first tile: m = -inf
   if (__any_sync(0xffffffffu, grow)) {
     const float alpha = grow ? fast_exp2(m - mt) : 1.f;
-    if (grow) {
-      l *= alpha;
-      m = mt;
-    }
+    if (grow) m = mt;
+    l *= alpha;
 #pragma unroll
-    for (int h = 0; h < GROUP; ++h) {
-      const float ah = from_owner<GROUP>(alpha, lane, h);
-      const float2 aa = make_float2(ah, ah);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) o[h][i] = __fmul2_rn(o[h][i], aa);
+    for (int j = 0; j < 8; ++j) {
+      o[j][0] *= alpha;
+      o[j][1] *= alpha;
     }
   }
-  float pr[kPasses];
-#pragma unroll
-  for (int j = 0; j < kPasses; ++j) {
-    pr[j] = fast_exp2(s[j] - m);
-    if (TAIL && tg + 4 * j >= valid_tokens) pr[j] = 0.f;  // also covers m = -inf
+  const uint32_t pa0 = pack_bf16x2(fast_exp2(x[0] - m), fast_exp2(x[1] - m));
+  const uint32_t pa2 = pack_bf16x2(fast_exp2(x[2] - m), fast_exp2(x[3] - m));
+  {
+    const float2 f0 = bf16x2_to_float2(pa0), f2 = bf16x2_to_float2(pa2);
+    l += (f0.x + f0.y) + (f2.x + f2.y);
   }
-  l += (pr[0] + pr[1]) + (pr[2] + pr[3]);
 #pragma unroll
-  for (int j = 0; j < kPasses; ++j) {
-    uint4 va = vr[j];
-    if (TAIL && tg + 4 * j >= valid_tokens) va = make_uint4(0, 0, 0, 0);  // may hold NaN
-    float2 vf[4];
-    unpack4(va, vf);
-#pragma unroll
-    for (int h = 0; h < GROUP; ++h) {
-      const float ph = from_owner<GROUP>(pr[j], lane, h);
-      const float2 pp = make_float2(ph, ph);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) o[h][i] = __ffma2_rn(pp, vf[i], o[h][i]);
-    }
+  for (int jp = 0; jp < 4; ++jp) {
+    mma_16816(o[2 * jp], pa0, pa2, v[jp][0] & vm0, v[jp][1] & vm1);
+    mma_16816(o[2 * jp + 1], pa0, pa2, v[jp][2] & vm0, v[jp][3] & vm1);
   }
 }
 
@@ -457,13 +454,14 @@ __device__ void merge_segment_in_warp(const KParams& p, const SegmentPieces& sp,
 
 template <int GROUP, bool kRows>
 __global__ void __launch_bounds__(kWarps * 32, 1)
-paged_decode_kernel(const KParams p) {
+paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                    const __grid_constant__ CUtensorMap tmap_v, const KParams p) {
   constexpr int kThreads = kWarps * 32;
   // A launch that follows in the stream with programmatic dependent launch enabled may
   // start as soon as SMs free up; it waits for this grid before it reads what this grid
   // writes (griddepcontrol.wait below).  No effect on launches without that attribute.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem[];  // 128-byte swizzle atoms need 1 KiB
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -482,6 +480,10 @@ paged_decode_kernel(const KParams p) {
   // first run modulo kWarps (two such segments never share a first run)
   __shared__ int cta_seg_count[kWarps];
   if (tid < kWarps) cta_seg_count[tid] = 0;
+  if ((smem_addr(smem) & 1023u) != 0) {  // never issue swizzled copies to a misaligned ring
+    if (tid == 0 && blockIdx.x == 0) flag_error(p.status, PA_DEVFLAG_LAYOUT);
+    return;
+  }
 
   if (lane == 0) {
     for (int i = 0; i < kStagesPerWarp; ++i) mbar_init(&full_bar[i], 1);
@@ -565,8 +567,8 @@ paged_decode_kernel(const KParams p) {
   if (gw >= p.grid) return;
 
   const uint64_t policy = l2_evict_first_policy();
-  const int tg = lane >> 3;  // token group
-  const int dq = lane & 7;   // dim slice: dims 8*dq .. 8*dq+7
+  const int r = lane >> 2;  // MMA row: query head r of the group (padding past GROUP)
+  const int q = lane & 3;
 
   // ---- issue side: the warp's runs, walked one block-table window at a time ----
   int64_t wc_run = gw;
@@ -617,10 +619,10 @@ paged_decode_kernel(const KParams p) {
       stage_tile[st] = t;  // read back by the fused append
       if (t >= 0) {
         mbar_arrive_expect_tx(&full_bar[st], 2 * kTileBytes);
-        const size_t off = static_cast<size_t>(t) * kTileBytes;
         uint8_t* dst = ring + st * 2 * kTileBytes;
-        bulk_copy_g2s(dst, p.key_cache + off, kTileBytes, &full_bar[st], policy);
-        bulk_copy_g2s(dst + kTileBytes, p.value_cache + off, kTileBytes, &full_bar[st], policy);
+        // one 16-row box per pool: rows t*16 .. t*16+15 of the [rows][64] view, swizzled
+        tma_load_2d_hint(dst, &tmap_k, 0, t * kBlockSize, &full_bar[st], policy);
+        tma_load_2d_hint(dst + kTileBytes, &tmap_v, 0, t * kBlockSize, &full_bar[st], policy);
       } else {
         mbar_arrive(&full_bar[st]);  // invalid block: release the stage with stale data
       }
@@ -667,15 +669,16 @@ paged_decode_kernel(const KParams p) {
     const bool first_piece = y == start;
     const int ntiles = pc.b1 - pc.b0;
 
-    float2 qf[GROUP][4];
-#pragma unroll
-    for (int h = 0; h < GROUP; ++h) {
+    uint32_t qa0[4] = {0u, 0u, 0u, 0u}, qa2[4] = {0u, 0u, 0u, 0u};
+    if (r < GROUP) {
       const __nv_bfloat16* qrow =
-          p.q + (row_of<kRows>(p, pc.s) * p.num_q_heads + pc.g * GROUP + h) * kHeadDim;
-      float2 f[4];
-      unpack4(ldg_nc128(qrow + dq * 8), f);
+          p.q + (row_of<kRows>(p, pc.s) * p.num_q_heads + pc.g * GROUP + r) * kHeadDim;
+      const uint32_t* qw = reinterpret_cast<const uint32_t*>(qrow);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) qf[h][i] = make_float2(f[i].x * p.q_scale, f[i].y * p.q_scale);
+      for (int ks = 0; ks < 4; ++ks) {  // dims 16ks + 2q (+1) and 16ks + 8 + 2q (+1)
+        qa0[ks] = __ldg(qw + 8 * ks + q);
+        qa2[ks] = __ldg(qw + 8 * ks + 4 + q);
+      }
     }
     // Fused append: this piece holds the (sequence, kv head)'s last tile, whose row
     // (L - 1) % 16 is the new token.  Lanes 0-7 carry its K chunks, 8-15 its V chunks.
@@ -687,12 +690,9 @@ paged_decode_kernel(const KParams p) {
       new_row = ldg_nc128(src);
     }
     float m = -INFINITY, l = 0.f;
-    float2 o[GROUP][4];
+    float o[8][4];
 #pragma unroll
-    for (int h = 0; h < GROUP; ++h) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) o[h][i] = make_float2(0.f, 0.f);
-    }
+    for (int j = 0; j < 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
 
     for (int k = 0; k < ntiles && ok; ++k) {
       const int st = waited % kStagesPerWarp;
@@ -703,15 +703,16 @@ paged_decode_kernel(const KParams p) {
         break;
       }
       ++waited;
-      const uint8_t* kt = ring + st * 2 * kTileBytes;
-      const uint8_t* vt = kt + kTileBytes;
+      uint8_t* kt = ring + st * 2 * kTileBytes;
+      uint8_t* vt = kt + kTileBytes;
       const int valid = L - (pc.b0 + k) * kBlockSize;
       if (p.k_new != nullptr && pc.b0 + k == pc.nb - 1) {
         // the new token: into the tile before it is read, and into its slot in the pools
         if (append_here) {
-          const int off = ((L - 1) % kBlockSize) * kRowBytes + (lane & 7) * 16;
-          uint8_t* tile = const_cast<uint8_t*>(lane < 8 ? kt : vt);
-          *reinterpret_cast<uint4*>(tile + off) = new_row;
+          const int nrow = (L - 1) % kBlockSize;
+          const int off = nrow * kRowBytes + (lane & 7) * 16;  // place in the pools
+          uint8_t* tile = lane < 8 ? kt : vt;
+          *reinterpret_cast<uint4*>(tile + swz(nrow, lane & 7)) = new_row;  // swizzled stage
           const int32_t t = stage_tile[st];
           if (t >= 0) {
             uint8_t* pool = lane < 8 ? p.key_cache_w : p.value_cache_w;
@@ -727,9 +728,11 @@ paged_decode_kernel(const KParams p) {
         __syncwarp();
       }
       if (valid >= kBlockSize) {
-        attend_tile<GROUP, false>(kt, vt, lane, tg, dq, kBlockSize, qf, m, l, o);
+        attend_tile<false>(smem_addr(kt), smem_addr(vt), lane, q, kBlockSize, p.q_scale, qa0, qa2,
+                           m, l, o);
       } else {
-        attend_tile<GROUP, true>(kt, vt, lane, tg, dq, valid, qf, m, l, o);
+        attend_tile<true>(smem_addr(kt), smem_addr(vt), lane, q, valid, p.q_scale, qa0, qa2, m,
+                          l, o);
       }
       // Every lane's reads of this stage have completed (their values fed the arithmetic
       // above); the warp barrier orders them before lane 0 issues the refill into the same
@@ -738,54 +741,25 @@ paged_decode_kernel(const KParams p) {
       issue_one();
     }
 
-    // ---- combine the warp's 4 token-group states (lanes with the same dq own one head) ----
-    float mh = m;
-    mh = fmaxf(mh, __shfl_xor_sync(0xffffffffu, mh, 8));
-    mh = fmaxf(mh, __shfl_xor_sync(0xffffffffu, mh, 16));
-    const float f_own = m == -INFINITY ? 0.f : fast_exp2(m - mh);
-    float lsum = l * f_own;
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, 8);
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);
+    // ---- the quad of row r holds head r: sum its four shares of l ----
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    if (r < GROUP) {
+      if (whole) {
+        const float inv = 1.f / l;
+        const int64_t row = row_of<kRows>(p, pc.s) * p.num_q_heads + pc.g * GROUP + r;
+        uint32_t* dst = reinterpret_cast<uint32_t*>(p.out + row * kHeadDim);
 #pragma unroll
-    for (int h = 0; h < GROUP; ++h) {
-      const float fh = from_owner<GROUP>(f_own, lane, h);
-      const float2 ff = make_float2(fh, fh);
+        for (int j = 0; j < 8; ++j) dst[4 * j + q] = pack_bf16x2(o[j][0] * inv, o[j][1] * inv);
+      } else {
+        const int slot = first_piece ? 0 : 1;
+        float* dst = p.partials + ((run * 2 + slot) * GROUP + r) * kPartialFloats;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float2 v = __fmul2_rn(o[h][i], ff);
-        v.x += __shfl_xor_sync(0xffffffffu, v.x, 8);
-        v.y += __shfl_xor_sync(0xffffffffu, v.y, 8);
-        v.x += __shfl_xor_sync(0xffffffffu, v.x, 16);
-        v.y += __shfl_xor_sync(0xffffffffu, v.y, 16);
-        o[h][i] = v;
-      }
-    }
-    // token group 0 (lanes 0..7) now holds the sums of dims 8*dq .. 8*dq+7 of every head
-#pragma unroll
-    for (int h = 0; h < GROUP; ++h) {
-      const float hm = from_owner<GROUP>(mh, lane, h);
-      const float hl = from_owner<GROUP>(lsum, lane, h);
-      if (tg == 0) {
-        if (whole) {
-          const float inv = 1.f / hl;
-          const int64_t row = row_of<kRows>(p, pc.s) * p.num_q_heads + pc.g * GROUP + h;
-          uint32_t w[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(o[h][i].x * inv, o[h][i].y * inv);
-            w[i] = *reinterpret_cast<const uint32_t*>(&b2);
-          }
-          *reinterpret_cast<uint4*>(p.out + row * kHeadDim + dq * 8) =
-              make_uint4(w[0], w[1], w[2], w[3]);
-        } else {
-          const int slot = first_piece ? 0 : 1;
-          float* dst = p.partials + ((run * 2 + slot) * GROUP + h) * kPartialFloats;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) *reinterpret_cast<float2*>(dst + dq * 8 + 2 * i) = o[h][i];
-          if (dq == 0) {
-            dst[kHeadDim] = hm;
-            dst[kHeadDim + 1] = hl;
-          }
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<float2*>(dst + 8 * j + 2 * q) = make_float2(o[j][0], o[j][1]);
+        if (q == 0) {
+          dst[kHeadDim] = m;
+          dst[kHeadDim + 1] = l;
         }
       }
     }
@@ -1039,6 +1013,11 @@ cudaError_t launch(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t str
   p.status = a.status;
   p.q_rows = a.q_rows;
   p.num_query_tokens = a.num_query_tokens;
+  CUtensorMap tk, tv;
+  const uint64_t pool_rows = static_cast<uint64_t>(a.num_blocks) * a.num_kv_heads * kBlockSize;
+  if (pool_rows >= (1ull << 31) || !encode_pool_rows(&tk, a.key_cache, pool_rows, kBlockSize) ||
+      !encode_pool_rows(&tv, a.value_cache, pool_rows, kBlockSize))
+    return cudaErrorInvalidValue;
   {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.grid);
@@ -1050,8 +1029,8 @@ cudaError_t launch(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t str
     attr[0].val.programmaticStreamSerializationAllowed = a.overlap_previous ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = a.q_rows != nullptr ? cudaLaunchKernelEx(&cfg, paged_decode_kernel<GROUP, true>, p)
-                            : cudaLaunchKernelEx(&cfg, paged_decode_kernel<GROUP, false>, p);
+    e = a.q_rows != nullptr ? cudaLaunchKernelEx(&cfg, paged_decode_kernel<GROUP, true>, tk, tv, p)
+                            : cudaLaunchKernelEx(&cfg, paged_decode_kernel<GROUP, false>, tk, tv, p);
     if (e == cudaSuccess) e = cudaGetLastError();
   }
   if (e != cudaSuccess || plan.fused_merge) return e;

@@ -1,6 +1,7 @@
 // Host-side launchers shared between the C-ABI entry points (api.cu) and the kernel files.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -72,6 +73,10 @@ struct DecodeArgs {
 };
 
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream);
+
+// Tensor map of a [rows][64] bf16 array read in boxes of `box_rows` rows with the 128-byte
+// swizzle (the K/V pools, rows = blocks x kv heads x 16); false if the driver call fails.
+bool encode_pool_rows(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows);
 
 struct PrefillArgs {
   void* out;

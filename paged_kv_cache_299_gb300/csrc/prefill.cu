@@ -803,8 +803,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [rows][64] bf16 tensor read in boxes of `box_rows` rows (128-byte swizzle).
-bool encode_rows(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
+}  // namespace
+
+// [rows][64] bf16 tensor read in boxes of `box_rows` rows (128-byte swizzle); also the
+// decode kernel's view of the pools.
+bool encode_pool_rows(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), rows};
@@ -815,6 +818,8 @@ bool encode_rows(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
 
 // q as [tokens][heads][64]; one box = 32 tokens x 4 heads (the 128 MMA rows of a tile).
 bool encode_q(CUtensorMap* map, const void* base, uint64_t tokens, uint64_t heads) {
@@ -849,8 +854,8 @@ cudaError_t prepare(const PrefillArgs& a, CUtensorMap* tq, CUtensorMap* tk, CUte
   const uint64_t pool_rows = static_cast<uint64_t>(a.num_blocks) * a.num_kv_heads * kBlockSize;
   if (pool_rows >= (1ull << 31)) return cudaErrorInvalidValue;
   if (!encode_q(tq, a.q, static_cast<uint64_t>(a.num_query_tokens), a.num_q_heads) ||
-      !encode_rows(tk, a.key_cache, pool_rows, kBlockSize) ||
-      !encode_rows(tv, a.value_cache, pool_rows, kBlockSize))
+      !encode_pool_rows(tk, a.key_cache, pool_rows, kBlockSize) ||
+      !encode_pool_rows(tv, a.value_cache, pool_rows, kBlockSize))
     return cudaErrorInvalidValue;
   p->out = static_cast<__nv_bfloat16*>(a.out);
   p->query_start_loc = a.query_start_loc;
