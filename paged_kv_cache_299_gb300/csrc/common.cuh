@@ -83,17 +83,6 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return pol;
 }
 
-// Global -> shared copy of `bytes` (multiple of 16, both addresses 16-B aligned) that
-// completes `bytes` transactions on `bar`.
-__device__ __forceinline__ void bulk_copy_g2s(void* smem_dst, const void* gmem_src,
-                                              uint32_t bytes, uint64_t* bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
-      "[%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(smem_dst)),
-      "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
-      : "memory");
-}
-
 // Order this thread's (and, after a warp/block sync, its peers') generic-proxy shared-memory
 // accesses before later async-proxy operations (TMA copies, tensor-core reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -718,7 +718,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
             uint8_t* pool = lane < 8 ? p.key_cache_w : p.value_cache_w;
             *reinterpret_cast<uint4*>(pool + static_cast<size_t>(t) * kTileBytes + off) = new_row;
           }
-          // This stage is refilled by a bulk copy (async proxy) after the tile is consumed.
+          // This stage is refilled by a TMA copy (async proxy) after the tile is consumed.
           // A generic-proxy write followed by an async-proxy write to the same shared memory
           // is ordered only through a proxy fence: without it the new row could land after
           // the refill and corrupt the next tile.  (Plain reads need no fence: their values
