@@ -80,3 +80,35 @@ def test_traffic_figures_name_existing_kernels_and_sources():
             assert got == (fig["dram_bytes_per_launch"] if current else None)
             assert fig["dram_bytes_per_launch"] == fig["read"] + fig["write"]
     assert bench.ncu_traffic("no_such_kernel", "decode_b256") is None
+
+
+def test_decode_roofline_uses_the_timed_region_only_for_overlapped_layer_steps():
+    """A step made only of fused decode launches over several layers reports the timed
+    region's time per launch (the layers overlap), with one launch timed alone beside it;
+    every other step reports the launch timed alone."""
+    sys.path.insert(0, ROOT)
+    import types
+    import bench
+    from paged_kv_cache_299_gb300 import workloads as wl
+
+    w = wl.decode_batch256_lognormal(layers=16)
+    per_launch = w.decode_kv_bytes() / w.layers
+
+    def fake(**kw):
+        d = dict(w=w, fused_append=True, ws_merge_kernel=False, unified=False)
+        d.update(kw)
+        return types.SimpleNamespace(**d)
+
+    r = bench.decode_roofline(fake(), "decode_b256", 0.125, 6694.2, "measured", step_ms=1.6)
+    assert r["launch_ms"] == round(0.1, 5)
+    assert r["achieved"] == round(per_launch / 0.1e-3 / 1e9, 1)
+    assert r["isolated"]["launch_ms"] == 0.125
+    assert r["isolated"]["achieved"] == round(per_launch / 0.125e-3 / 1e9, 1)
+    assert r["frac"] == round(r["achieved"] / 6694.2, 4)
+    # a store launched separately, or a merge kernel in the step: the launch timed alone
+    for st in (fake(fused_append=False), fake(ws_merge_kernel=True)):
+        r = bench.decode_roofline(st, "decode_b256", 0.125, 6694.2, "measured", step_ms=1.6)
+        assert r["launch_ms"] == 0.125 and "isolated" not in r
+    w1 = wl.decode_batch64_uniform()  # one layer
+    r = bench.decode_roofline(fake(w=w1), "decode_b64", 0.04, 6694.2, "measured", step_ms=0.039)
+    assert r["launch_ms"] == 0.04 and "isolated" not in r
