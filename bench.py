@@ -380,8 +380,12 @@ class DeviceStep:
             if w.num_decode:
                 if dec_events is not None:
                     dec_events[li][0].record()
+                # after the chunk prefill, which writes only its own output rows, the
+                # decode's start-up may overlap the prefill's last CTAs
+                flags = pa.PA_LAUNCH_OVERLAP_PREVIOUS if w.num_prefill else pa.PA_LAUNCH_DEFAULT
                 pa.pa_decode(L["out_dec"], L["q_dec"], kc, vc, S["bt_dec"], S["ctx_dec"],
-                             w.scale, self.max_ctx_dec, w.partition_tokens, workspace=self.ws)
+                             w.scale, self.max_ctx_dec, w.partition_tokens, workspace=self.ws,
+                             launch_flags=flags)
                 if dec_events is not None:
                     dec_events[li][1].record()
 
@@ -575,7 +579,10 @@ def run_gpu(args, rank, world):
                               else "pa_compute_slot_mapping + pa_reshape_and_cache"),
                        **({"overlap": "layers after the first start under programmatic "
                                       "dependent launch (PA_LAUNCH_OVERLAP_PREVIOUS)"}
-                          if st.fused_append and w.layers > 1 else {}),
+                          if st.fused_append and w.layers > 1 else
+                          {"overlap": "the decode starts under programmatic dependent launch "
+                                      "behind the chunk prefill (PA_LAUNCH_OVERLAP_PREVIOUS)"}
+                          if w.num_prefill and w.num_decode and not st.unified else {}),
                        **({"attention": "pa_attention_varlen: decode rows on the decode "
                                         "kernel, chunks on the tensor-core kernel"}
                           if st.unified else {})),

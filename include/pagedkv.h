@@ -135,9 +135,9 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t 
  * block tables nor the context lengths nor the K/V pools this call reads; the decode
  * kernels of consecutive layers of one step qualify (each layer has its own pools), a
  * store into the same pools (pa_reshape_and_cache, pa_copy_blocks, a previous
- * pa_decode_append on the same layer) does not.  The decode kernels of this library let a
- * following launch that carries the flag start early; a launch without it waits for the
- * previous kernel as usual.  Also valid inside CUDA graph capture.  Unknown bits are
+ * pa_decode_append on the same layer) does not.  The decode and chunk-prefill kernels of
+ * this library (pa_prefill_chunk, pa_attention_varlen) let a following launch that carries
+ * the flag start early; a launch without it waits for the previous kernel as usual.  Also valid inside CUDA graph capture.  Unknown bits are
  * rejected (PA_ERR_INVALID_ARG). */
 #define PA_LAUNCH_DEFAULT 0u
 #define PA_LAUNCH_OVERLAP_PREVIOUS 1u

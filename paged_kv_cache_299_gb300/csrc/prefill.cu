@@ -341,10 +341,18 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  // A decode launch that follows with programmatic dependent launch may start its
+  // prologue as this grid's CTAs leave the SMs (it waits for this grid before touching what
+  // this grid writes).  When this grid itself was launched that way (the unified varlen
+  // launch, behind the decode of the same batch, whose outputs and inputs it does not
+  // touch), it waits for that grid only at its end, so that its completion still implies
+  // the previous grid's.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   extern __shared__ __align__(1024) uint8_t smem[];  // 128-byte swizzle atoms need 1 KiB
   if ((smem_addr(smem) & 1023u) != 0) {  // never issue swizzled copies to a misaligned tile
     if (tid == 0) flag_error(p.status, PA_DEVFLAG_LAYOUT);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     return;
   }
   uint8_t* sq = smem + kQOff;  // two Q buffers
@@ -788,6 +796,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
   }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -878,7 +887,8 @@ cudaError_t prepare(const PrefillArgs& a, CUtensorMap* tq, CUtensorMap* tk, CUte
 
 namespace {
 
-cudaError_t launch_prefill_kernel(const PrefillArgs& a, bool skip_single, cudaStream_t stream) {
+cudaError_t launch_prefill_kernel(const PrefillArgs& a, bool skip_single, cudaStream_t stream,
+                                  bool overlap_previous = false) {
   CUtensorMap tq, tk, tv;
   PParams p;
   cudaError_t e = prepare(a, &tq, &tk, &tv, &p);
@@ -892,7 +902,18 @@ cudaError_t launch_prefill_kernel(const PrefillArgs& a, bool skip_single, cudaSt
   const int64_t units_upper = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads * p.q_tiles;
   const int64_t grid = units_upper < 2LL * sms ? units_upper : 2LL * sms;
   if (grid < 1) return cudaSuccess;
-  paged_prefill_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = overlap_previous ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, paged_prefill_kernel, tq, tk, tv, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -965,7 +986,9 @@ cudaError_t launch_varlen(const PrefillArgs& a, void* workspace, cudaStream_t st
   // Chunks (q_len > 1) on the tensor-core kernel; none can exist when the host bound of
   // q_len is 1 (a decode-only batch), and then nothing more is launched.
   if (a.max_query_len <= 1) return cudaSuccess;
-  return launch_prefill_kernel(a, true, stream);
+  // The chunk launch reads nothing the decode launch writes and writes other rows, so it
+  // may start as the decode's CTAs leave (it waits for the decode grid before it ends).
+  return launch_prefill_kernel(a, true, stream, /*overlap_previous=*/true);
 }
 
 }  // namespace pkv

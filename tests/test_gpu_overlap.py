@@ -3,7 +3,9 @@ programmatic dependent launch).  A decode step over several layers, each layer w
 own pools and the launches after the first carrying the flag, must give the same bits as
 the same step without the flag, eagerly and replayed from a CUDA graph, and must agree
 with the oracle.  The layers share one workspace, so a launch that touched it before the
-previous layer had finished would show up as wrong rows."""
+previous layer had finished would show up as wrong rows.  The mixed step's decode behind a
+chunk prefill is checked the same way.  (The unified varlen launch starts its chunk kernel
+behind its decode kernel in the same manner; its tests are in test_gpu_varlen.py.)"""
 import pytest
 import torch
 
@@ -87,3 +89,39 @@ def test_unknown_launch_flags_are_rejected():
     assert e.value.status == pa.PA_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert torch.all(out == 7.0)  # nothing ran
+
+
+def test_decode_behind_a_chunk_prefill_overlaps_it():
+    """The mixed step: chunk prefill, then the decode of the one-token sequences with the
+    flag (the prefill writes only its own output rows).  Both outputs match the serial
+    launches bit for bit, and the decode rows match the oracle."""
+    w = wl.mixed_prefill_decode()
+    st = GpuStep(w)  # history and this step's tokens stored
+    P = w.num_prefill
+    qsl = torch.from_numpy(w.prefill_query_start_loc.astype("int32")).cuda()
+    max_q = int(w.new_lens[:P].max())
+    bt_p, ctx_p = st.bt[:P].contiguous(), st.ctx[:P].contiguous()
+    bt_d, ctx_d = st.bt[P:].contiguous(), st.ctx[P:].contiguous()
+    max_ctx = int(w.decode_context_lens.max())
+    ws = torch.zeros(pa.pa_decode_workspace_size(w.num_decode, 8, 32, max_ctx, 0),
+                     dtype=torch.uint8, device="cuda")
+
+    def run(flags, out_p, out_d):
+        pa.pa_prefill_chunk(out_p, st.vals["q_prefill"], qsl, max_q, st.kc, st.vc, bt_p, ctx_p,
+                            w.scale, device_status=st.status)
+        pa.pa_decode(out_d, st.vals["q_decode"], st.kc, st.vc, bt_d, ctx_d, w.scale, max_ctx,
+                     workspace=ws, device_status=st.status, launch_flags=flags)
+
+    serial_p = torch.empty_like(st.vals["q_prefill"])
+    serial_d = torch.empty_like(st.vals["q_decode"])
+    run(pa.PA_LAUNCH_DEFAULT, serial_p, serial_d)
+    over_p = torch.full_like(serial_p, float("nan"))
+    over_d = torch.full_like(serial_d, float("nan"))
+    for _ in range(3):
+        run(pa.PA_LAUNCH_OVERLAP_PREVIOUS, over_p, over_d)
+    torch.cuda.synchronize()
+    assert st.check_status() == pa.PA_OK
+    assert torch.equal(serial_p, over_p) and torch.equal(serial_d, over_d)
+    ref = oracle_step(w, host_vals(st.vals))["decode"]
+    mx, mean = errors(over_d.float().cpu().numpy(), ref)
+    assert mx <= ATOL_MAX and mean <= ATOL_MEAN, (mx, mean)
