@@ -68,7 +68,11 @@ typedef enum pa_status {
 #define PA_DEVFLAG_LAYOUT 0x10     /* shared memory not aligned as the kernel requires
                                       (work skipped; reported as PA_ERR_DEVICE_INDEX) */
 
-/* Geometry of one layer's pair of cache pools; validated on every call. */
+/* Geometry of one layer's pair of cache pools; validated on every call.  The attention
+ * calls (pa_decode, pa_decode_append, pa_prefill_chunk, pa_attention_varlen) also need
+ * num_blocks x num_kv_heads x 16 < 2^31 (each pool under 256 GiB): their kernels address
+ * the pools as rows of 64 head dims with 32-bit coordinates; larger geometries return
+ * PA_ERR_UNSUPPORTED. */
 typedef struct pa_cache_desc {
   int32_t num_blocks;   /* physical blocks in each pool */
   int32_t num_kv_heads; /* Hkv (8 for Llama-3.2-1B) */

@@ -46,6 +46,20 @@ pa_status check_desc(const pa_cache_desc& cd) {
   return PA_OK;
 }
 
+// The attention kernels read the pools through tensor maps over [blocks x heads x 16][64]
+// rows with 32-bit row coordinates: fewer than 2^31 rows (each pool under 256 GiB).
+pa_status check_attention_pools(const pa_cache_desc& cd) {
+  pa_status st = check_desc(cd);
+  if (st != PA_OK) return st;
+  const int64_t rows = static_cast<int64_t>(cd.num_blocks) * cd.num_kv_heads * cd.block_size;
+  if (rows >= (int64_t{1} << 31))
+    return fail(PA_ERR_UNSUPPORTED,
+                "cache desc: %d blocks x %d kv heads x 16 rows = %lld rows per pool (the "
+                "attention kernels take fewer than 2^31)",
+                cd.num_blocks, cd.num_kv_heads, static_cast<long long>(rows));
+  return PA_OK;
+}
+
 }  // namespace
 
 namespace pkv {
@@ -141,7 +155,7 @@ static pa_status decode_impl(void* out, const void* q, const void* k_new, const 
                     int32_t max_context_len, int32_t partition_tokens, void* workspace,
                     size_t workspace_bytes, uint32_t launch_flags, int32_t* device_status,
                     pa_stream_t stream) {
-  pa_status st = check_desc(cd);
+  pa_status st = check_attention_pools(cd);
   if (st != PA_OK) return st;
   st = check_decode_sizes(num_seqs, cd.num_kv_heads, num_q_heads, max_context_len,
                           partition_tokens);
@@ -225,7 +239,7 @@ pa_status chunk_args(void* out, const void* q, const int32_t* query_start_loc,
                      int32_t num_q_heads, float scale, int32_t* device_status,
                      pkv::PrefillArgs* a, bool* skip) {
   *skip = false;
-  pa_status st = check_desc(cd);
+  pa_status st = check_attention_pools(cd);
   if (st != PA_OK) return st;
   if (num_seqs < 0 || max_query_len < 0 || num_query_tokens < 0 || max_blocks_per_seq <= 0)
     return fail(PA_ERR_INVALID_ARG,

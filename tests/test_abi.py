@@ -75,6 +75,12 @@ def test_host_rejects_bad_arguments_without_touching_the_device():
                          None) == pa.PA_OK
     assert lib.pa_decode(*args, 2, 32, ctypes.c_float(-1.0), 64, 0, fake, 1 << 20, 0, None,
                          None) == pa.PA_ERR_INVALID_ARG
+    # pools beyond 2^31 rows of 64 head dims are refused by the attention calls
+    big = pa.CacheDesc(1 << 24, 8, 64, 16)  # 2^24 blocks x 8 heads x 16 rows = 2^31 rows
+    assert lib.pa_decode(fake, fake, fake, fake, big, fake, 4, fake, 2, 32,
+                         ctypes.c_float(0.125), 64, 0, fake, 1 << 20, 0, None,
+                         None) == pa.PA_ERR_UNSUPPORTED
+    assert b"2^31" in lib.pa_last_error()
     # launch flags: unknown bits are rejected before any launch
     assert lib.pa_decode(*args, 2, 32, ctypes.c_float(0.125), 64, 0, fake, 1 << 20, 2, None,
                          None) == pa.PA_ERR_INVALID_ARG
