@@ -227,6 +227,17 @@ def test_group_sizes_one_and_two():
         assert mx <= ATOL_MAX and mean <= ATOL_MEAN
 
 
+@pytest.mark.parametrize("hq", [8, 16])
+@pytest.mark.parametrize("partition_tokens", [0, 64])
+def test_group_sizes_one_and_two_batched(hq, partition_tokens):
+    """Group sizes 1 (8 query heads) and 2 (16) over a ragged batch of 12 sequences: the
+    tensor-core tile arithmetic with 1 or 2 live MMA rows, runs split across sequences and
+    merged in the attention kernel (balanced) or by the merge kernel (64-token partitions);
+    pools bit-exact and outputs against the oracle."""
+    w = wl.random_small(300 + hq + partition_tokens, num_seqs=12, max_ctx=900, num_q_heads=hq)
+    full_check(w, partition_tokens=partition_tokens)
+
+
 @pytest.mark.parametrize("partition_tokens", [0, 16, 512])
 def test_group_sizes_one_and_two_long_context(partition_tokens):
     """Group sizes 1 and 2 over a 1500-token context: split segments merged in the attention
