@@ -17,6 +17,7 @@ of the same workload: the slow baseline arm, not a target.
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -147,21 +148,33 @@ def describe(w) -> dict:
 # clocks sampled during the timed region
 # ----------------------------------------------------------------------------------------
 class ClockSampler:
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampling every 20 ms, started ahead of the region it measures (the tool
+    needs a moment to start); mark() brackets the region, and stop() keeps the samples whose
+    timestamps fall inside it."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    TIME_FORMAT = "%Y/%m/%d %H:%M:%S.%f"
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
         self.file = None
+        self.t0 = None
+        self.t1 = None
+
+    def mark_start(self):
+        self.t0 = datetime.datetime.now()
+
+    def mark_end(self):
+        self.t1 = datetime.datetime.now()
 
     def start(self):
         try:
             self.file = tempfile.TemporaryFile(mode="w+")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=self.file, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -175,24 +188,34 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.file.seek(0)
-        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            r = [x.strip() for x in r]
-            if len(r) < 9:
+        return self.summarise(self.file.read(), self.t0, self.t1)
+
+    @classmethod
+    def summarise(cls, text: str, t0=None, t1=None) -> dict:
+        """Median SM clock, maximum clock and the throttle reasons seen, over the samples
+        between t0 and t1 (all samples when no bound is set or none falls inside)."""
+        rows = []
+        for line in text.strip().splitlines():
+            r = [x.strip() for x in line.split(",")]
+            if len(r) < 10:
                 continue
             try:
-                sm.append(float(r[1]))
-                smax.append(float(r[2]))
+                ts = datetime.datetime.strptime(r[0], cls.TIME_FORMAT)
+                rows.append((ts, float(r[2]), float(r[3]), r[6:10]))
             except ValueError:
                 continue
-            for name, val in zip(names, r[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
+        inside = [x for x in rows
+                  if (t0 is None or x[0] >= t0) and (t1 is None or x[0] <= t1)]
+        window = "the marked region"
+        if not inside:
+            inside, window = rows, "the whole sampling (no sample inside the marked region)"
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = {name for _, _, _, vals in inside
+                   for name, val in zip(names, vals) if val.lower() == "active"}
+        sm = [x[1] for x in inside]
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "sm_max_mhz": max(x[2] for x in inside) if inside else None,
+                "samples": len(sm), "reasons": sorted(reasons), "samples_from": window}
 
 
 # ----------------------------------------------------------------------------------------
@@ -436,6 +459,8 @@ def time_steps(st, dev, K: int, warmup: int, flush_l2, use_graph: bool, barrier=
     if use_graph:
         from paged_kv_cache_299_gb300 import graphs
         graph = graphs.StepGraph(st.step)
+    if sampler is not None:
+        sampler.mark_start()
     t_wall = time.perf_counter()
     for k in range(K):
         if flush_l2 is not None:
@@ -554,6 +579,8 @@ def run_gpu(args, rank, world):
     if not args.no_e2e:
         e2e = run_e2e(st, max(3, min(K, 50)), dev, graph, flush_l2)
         e2e["step_ms"] = max_over_ranks(e2e["step_ms"], dev)
+    torch.cuda.synchronize(dev)
+    sampler.mark_end()
     t["clocks"] = dict(sampler.stop(), window="from the timed steps to the end of the "
                                               "end-to-end loop")
 
@@ -627,6 +654,7 @@ def run_secondary(args, dev, local: int, peak: float, peak_src: str) -> dict:
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.2)
+    sampler.mark_start()
     for key, K in SECONDARY:
         if key == args.workload:
             continue
@@ -654,6 +682,7 @@ def run_secondary(args, dev, local: int, peak: float, peak_src: str) -> dict:
         torch.cuda.empty_cache()
     out["reshape_and_cache"] = measure_store(dev, peak, peak_src)
     out["copy_blocks"] = measure_copy_blocks(dev, peak, peak_src)
+    sampler.mark_end()
     out["clocks"] = sampler.stop()
     return out
 

@@ -112,3 +112,26 @@ def test_decode_roofline_uses_the_timed_region_only_for_overlapped_layer_steps()
     w1 = wl.decode_batch64_uniform()  # one layer
     r = bench.decode_roofline(fake(w=w1), "decode_b64", 0.04, 6694.2, "measured", step_ms=0.039)
     assert r["launch_ms"] == 0.04 and "isolated" not in r
+
+
+def test_clock_summary_keeps_the_samples_of_the_marked_region():
+    """nvidia-smi rows (timestamp first) outside the marked region are left out of the
+    clock summary; a region without samples falls back to every sample, and says so."""
+    sys.path.insert(0, ROOT)
+    import datetime
+    import bench
+    rows = [
+        "2026/12/03 10:00:00.000, 0, 1200, 2070, 300.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/03 10:00:00.500, 0, 2070, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Active",
+        "2026/12/03 10:00:00.520, 0, 2070, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/03 10:00:01.000, 0, 1000, 2070, 200.0, 0x0, Active, Not Active, Not Active, Not Active",
+    ]
+    text = "\n".join(rows)
+    t = lambda x: datetime.datetime.strptime("2026/12/03 " + x, "%Y/%m/%d %H:%M:%S.%f")
+    got = bench.ClockSampler.summarise(text, t("10:00:00.400"), t("10:00:00.600"))
+    assert got["samples"] == 2 and got["sm_mhz"] == 2070 and got["sm_max_mhz"] == 2070
+    assert got["reasons"] == ["sw_power_cap"] and got["samples_from"] == "the marked region"
+    everything = bench.ClockSampler.summarise(text, t("10:00:02.000"), t("10:00:03.000"))
+    assert everything["samples"] == 4 and "hw_slowdown" in everything["reasons"]
+    assert everything["samples_from"].startswith("the whole sampling")
+    assert bench.ClockSampler.summarise("")["samples"] == 0
