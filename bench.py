@@ -645,7 +645,8 @@ def run_gpu(args, rank, world):
 # The other workloads, measured in the same invocation with the same method (graph-replayed
 # step, eager per-kernel events, in-run stream read of one decode launch's bytes), and a
 # standalone KV store: (bench name, timed steps).
-SECONDARY = (("decode_b64", 100), ("long_context_b4", 30), ("mixed_step", 30))
+SECONDARY = (("single_seq_300", 200), ("decode_b64", 100), ("long_context_b4", 30),
+             ("mixed_step", 30))
 
 
 def run_secondary(args, dev, local: int, peak: float, peak_src: str) -> dict:
@@ -664,6 +665,7 @@ def run_secondary(args, dev, local: int, peak: float, peak_src: str) -> dict:
         flush_l2 = make_flush(dev, kv, "write-read")
         t = time_steps(st, dev, K, 3, flush_l2, True)
         d = {"kv_read_bytes_per_step": kv, "steps": K, "ms_per_step": round(t["step_ms"], 5),
+             "us_per_step": round(t["step_ms"] * 1e3, 2),
              "step_gbs": round(kv / (t["step_ms"] * 1e-3) / 1e9, 1),
              "step_pct_of_8tbs": round(100 * kv / (t["step_ms"] * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 2),
              "l2": "flushed between steps" if flush_l2 else "inputs larger than L2",
