@@ -141,8 +141,8 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t 
  * store into the same pools (pa_reshape_and_cache, pa_copy_blocks, a previous
  * pa_decode_append on the same layer) does not.  The decode and chunk-prefill kernels of
  * this library (pa_prefill_chunk, pa_attention_varlen) let a following launch that carries
- * the flag start early; a launch without it waits for the previous kernel as usual.  Also valid inside CUDA graph capture.  Unknown bits are
- * rejected (PA_ERR_INVALID_ARG). */
+ * the flag start early; a launch without it waits for the previous kernel as usual.  Also
+ * valid inside CUDA graph capture.  Unknown bits are rejected (PA_ERR_INVALID_ARG). */
 #define PA_LAUNCH_DEFAULT 0u
 #define PA_LAUNCH_OVERLAP_PREVIOUS 1u
 
