@@ -3,9 +3,11 @@
 
 One step = one pass of the whole path over one batch: slot mapping of the step's new
 tokens, then for every layer the KV store of the new tokens and paged attention (decode,
-plus causal chunked prefill where the workload has chunks).  The default workload is
-decode batch 256 with lognormal contexts (median 1024, sigma 0.8, clipped to [1, 8192])
-and 16 layers of KV pools resident; other workloads are reachable with --workload.
+plus causal chunked prefill where the workload has chunks).  When every sequence adds one
+token, the store rides in the decode launch (pa_decode_append), and the layers after the
+first start under PA_LAUNCH_OVERLAP_PREVIOUS.  The default workload is decode batch 256
+with lognormal contexts (median 1024, sigma 0.8, clipped to [1, 8192]) and 16 layers of
+KV pools resident; other workloads are reachable with --workload.
 
 Prints ONE JSON line (rank 0).  ``value`` is KV-read GB/s: the live K+V bytes the decode
 attention must read in a step (sum of context lengths x 2048 B x layers), divided by the
