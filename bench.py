@@ -646,9 +646,15 @@ def run_gpu(args, rank, world):
 
 # The other workloads, measured in the same invocation with the same method (graph-replayed
 # step, eager per-kernel events, in-run stream read of one decode launch's bytes), and a
-# standalone KV store: (bench name, timed steps).
-SECONDARY = (("single_seq_300", 200), ("decode_b64", 100), ("long_context_b4", 30),
-             ("mixed_step", 30))
+# standalone KV store: (name, workload, timed steps, layers or None for the workload's own).
+# The batch-64 decode is measured twice: one layer with L2 flushed before every step (one
+# launch alone), and back to back over 16 layers, each with its own pool (2.2 GB per step,
+# no flush), the later layers overlapping the earlier ones as in the default step.
+SECONDARY = (("single_seq_300", "single_seq_300", 200, None),
+             ("decode_b64", "decode_b64", 100, None),
+             ("decode_b64_16layers", "decode_b64", 50, 16),
+             ("long_context_b4", "long_context_b4", 30, None),
+             ("mixed_step", "mixed_step", 30, None))
 
 
 def run_secondary(args, dev, local: int, peak: float, peak_src: str) -> dict:
@@ -658,10 +664,10 @@ def run_secondary(args, dev, local: int, peak: float, peak_src: str) -> dict:
     sampler.start()
     time.sleep(0.2)
     sampler.mark_start()
-    for key, K in SECONDARY:
-        if key == args.workload:
+    for name, key, K, layers in SECONDARY:
+        if key == args.workload and layers is None:
             continue
-        w = workload(key)
+        w = workload(key, layers)
         st = DeviceStep(w, dev, fused_append=True, mixed="split")
         kv = w.decode_kv_bytes()
         flush_l2 = make_flush(dev, kv, "write-read")
@@ -673,15 +679,19 @@ def run_secondary(args, dev, local: int, peak: float, peak_src: str) -> dict:
              "l2": "flushed between steps" if flush_l2 else "inputs larger than L2",
              "store": ("fused into decode (pa_decode_append)" if st.fused_append
                        else "pa_compute_slot_mapping + pa_reshape_and_cache")}
+        if layers is not None:
+            d["layers"] = int(w.layers)
         if t["dec_ms"]:
             d["roofline"] = decode_roofline(st, key, t["dec_ms"], peak, peak_src,
                                             step_ms=t["step_ms"])
-            sr = measure_stream_read(dev, kv // w.layers, flush_l2, 20)
+            # one launch's bytes, flushed before each read when they fit in 4x L2
+            sr = measure_stream_read(dev, kv // w.layers,
+                                     make_flush(dev, kv // w.layers, "write-read"), 20)
             d["roofline"]["stream_read"] = dict(
                 sr, decode_frac_of_stream=round(d["roofline"]["achieved"] / sr["achieved"], 4))
         if t["pre_ms"]:
             d["prefill_roofline"] = prefill_roofline(st, t["pre_ms"])
-        out[key] = d
+        out[name] = d
         del st, t
         torch.cuda.empty_cache()
     out["reshape_and_cache"] = measure_store(dev, peak, peak_src)
