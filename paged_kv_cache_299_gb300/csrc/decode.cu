@@ -272,7 +272,8 @@ constexpr size_t decode_smem_fixed() {
 // Block-table window: lane j holds the tile (phys_block * Hkv + kv_head) of the j-th of
 // `n` consecutive tiles of one run, or -1 for an invalid block id.
 struct Window {
-  int32_t tile;
+  int32_t tile;  // raw block id until resolved (see resolve_window), then the tile or -1
+  int32_t g;
   int n;
 };
 
@@ -583,10 +584,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
       }
     }
     Window w;
-    w.tile = -1;
+    w.tile = 0;
+    w.g = 0;
     const int64_t left = wc_stop - wc_y;
     w.n = wc_run < p.grid ? static_cast<int>(left < kWindow ? left : kWindow) : 0;
-    bool bad = false;
     if (lane < w.n) {
       const int64_t y = wc_y + lane;
       const int s = find_seq(seq_base, S, y, KV);
@@ -594,16 +595,22 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
       const int off = static_cast<int>(y - static_cast<int64_t>(seq_base[s]) * KV);
       const int g = off / nb;
       const int b = off - g * nb;
-      const int32_t phys = __ldg(p.block_tables + static_cast<int64_t>(s) * p.max_blocks_per_seq + b);
-      bad = phys < 0 || phys >= p.num_blocks;
-      w.tile = bad ? -1 : phys * KV + g;
+      w.tile = __ldg(p.block_tables + static_cast<int64_t>(s) * p.max_blocks_per_seq + b);
+      w.g = g;
     }
-    if (__any_sync(0xffffffffu, bad) && lane == 0) flag_error(p.status, PA_DEVFLAG_BAD_BLOCK);
     wc_y += w.n;
     return w;
   };
+  // The loaded block ids are checked and turned into tiles only when the window is first
+  // used, so that the loads of the next window stay in flight meanwhile.
+  auto resolve_window = [&](Window& w) {
+    const bool bad = lane < w.n && (w.tile < 0 || w.tile >= p.num_blocks);
+    w.tile = lane < w.n && !bad ? w.tile * KV + w.g : -1;
+    if (__any_sync(0xffffffffu, bad) && lane == 0) flag_error(p.status, PA_DEVFLAG_BAD_BLOCK);
+  };
   Window cur = next_window();
   Window nxt = next_window();
+  resolve_window(cur);
   int cur_i = 0;
   int issued = 0;
   auto issue_one = [&]() {
@@ -611,6 +618,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
       cur = nxt;
       cur_i = 0;
       if (cur.n == 0) return;  // nothing left to issue
+      resolve_window(cur);
       nxt = next_window();
     }
     const int32_t t = __shfl_sync(0xffffffffu, cur.tile, cur_i);
