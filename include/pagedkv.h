@@ -251,8 +251,8 @@ pa_status pa_attention_varlen(void* out, const void* q, const int32_t* query_sta
                               size_t workspace_bytes, int32_t* device_status,
                               pa_stream_t stream);
 
-/* Paged decode attention that needs no workspace from the caller.  The paper has no
- * counterpart for this call.  It exists for callers that cannot allocate device memory
+/* Paged decode attention that needs no workspace from the caller.  The vLLM and
+ * tiny-vllm pages describe no counterpart for this call.  It exists for callers that cannot allocate device memory
  * themselves: code embedded in a host program that owns every device allocation (its
  * memory pool is not reachable from here), or code that must not call cudaMalloc at run
  * time because that call can stall the whole device.  It computes exactly what pa_decode
