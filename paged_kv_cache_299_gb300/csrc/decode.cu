@@ -57,6 +57,7 @@ constexpr int kFusedMergeMaxContext = 8192;
 constexpr int kMaxSeqs = 4096;
 constexpr int kMergeThreads = 512;
 constexpr int kMergeUnroll = 4;  // partials whose loads one warp has in flight at once
+constexpr int kMergeSplitPieces = 16;  // segments with this many pieces merge per query head
 
 struct KParams {
   __nv_bfloat16* out;
@@ -819,29 +820,37 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
 }
 
 // Combines the partials of every (sequence, kv head) whose tiles were split across CTAs,
-// and writes zero rows for empty contexts.  One CTA per (kv head, sequence).
-template <int GROUP, bool kRows>
+// and writes zero rows for empty contexts.  One CTA per (sequence, kv head, HPC of the
+// head's GROUP query heads): HPC = GROUP when segments have few pieces, 1 when they have
+// many (long contexts), so that GROUP times as many CTAs share the loads.  Each warp folds
+// its partials into a running (maximum, sum, o) per query head, rescaling by the
+// log-sum-exp weights as the maximum grows, with U partials' loads in flight per round;
+// the warps' states are then combined the same way.
+template <int GROUP, int HPC, bool kRows>
 __global__ void __launch_bounds__(kMergeThreads)
 merge_partials_kernel(const KParams p) {
   constexpr int kWarps = kMergeThreads / 32;
-  __shared__ float red_m[kWarps][GROUP];
-  __shared__ float red_l[kWarps][GROUP];
-  __shared__ float red_o[kWarps][GROUP][kHeadDim];
-  __shared__ float s_M[GROUP];
-  const int g = blockIdx.x;
+  constexpr int kSplit = GROUP / HPC;
+  constexpr int U = HPC == 1 ? 2 * kMergeUnroll : kMergeUnroll;
+  __shared__ float red_m[kWarps][HPC];
+  __shared__ float red_l[kWarps][HPC];
+  __shared__ float red_o[kWarps][HPC][kHeadDim];
+  const int g = blockIdx.x / kSplit;
+  const int h0 = (blockIdx.x % kSplit) * HPC;
   const int s = blockIdx.y;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int KV = p.num_kv_heads;
-  __nv_bfloat16* out = p.out + (row_of<kRows>(p, s) * p.num_q_heads + g * GROUP) * kHeadDim;
+  __nv_bfloat16* out =
+      p.out + (row_of<kRows>(p, s) * p.num_q_heads + g * GROUP + h0) * kHeadDim;
   const int32_t base = p.ws_seq_base[s];
   const int nb = p.ws_seq_base[s + 1] - base;
   if (nb == 0) {
     // an empty context gives a zero row; in a mixed batch nb == 0 means the sequence is not
     // a decode row (or was flagged), and its row is left alone
     if (!kRows)
-      for (int e = tid; e < GROUP * kHeadDim; e += kMergeThreads) out[e] = __float2bfloat16_rn(0.f);
+      for (int e = tid; e < HPC * kHeadDim; e += kMergeThreads) out[e] = __float2bfloat16_rn(0.f);
     return;
   }
   const int64_t total = *p.ws_total;
@@ -860,7 +869,7 @@ merge_partials_kernel(const KParams p) {
   auto record = [&](int k, int h) -> const float* {
     const int64_t c = c_first + k;
     const int slot = k == 0 ? first_slot : 0;
-    return p.partials + ((c * 2 + slot) * GROUP + h) * kPartialFloats;
+    return p.partials + ((c * 2 + slot) * GROUP + h0 + h) * kPartialFloats;
   };
   // With at least one tile per run (the usual case) no run is empty and the test is skipped.
   const bool maybe_empty = total < p.grid;
@@ -870,46 +879,25 @@ merge_partials_kernel(const KParams p) {
     return run_start(c, total, p.grid, p.chunk) == run_start(c + 1, total, p.grid, p.chunk);
   };
 
-  float mloc[GROUP];
+  float M[HPC], L[HPC];
+  float2 A[HPC];
 #pragma unroll
-  for (int h = 0; h < GROUP; ++h) mloc[h] = -INFINITY;
-  for (int k = tid; k < n; k += kMergeThreads) {
-    if (empty_run(k)) continue;
-#pragma unroll
-    for (int h = 0; h < GROUP; ++h) mloc[h] = fmaxf(mloc[h], record(k, h)[kHeadDim]);
+  for (int h = 0; h < HPC; ++h) {
+    M[h] = -INFINITY;
+    L[h] = 0.f;
+    A[h] = make_float2(0.f, 0.f);
   }
+  // Each warp takes U partials per round and issues all their loads before combining them,
+  // so a round costs one memory latency.
+  for (int k0 = warp * U; k0 < n; k0 += kWarps * U) {
+    float mk[U][HPC], lk[U][HPC];
+    float2 vk[U][HPC];
 #pragma unroll
-  for (int h = 0; h < GROUP; ++h) {
-    for (int off = 16; off > 0; off >>= 1)
-      mloc[h] = fmaxf(mloc[h], __shfl_xor_sync(0xffffffffu, mloc[h], off));
-    if (lane == 0) red_m[warp][h] = mloc[h];
-  }
-  __syncthreads();
-  if (tid < GROUP) {
-    float v = red_m[0][tid];
-    for (int w = 1; w < kWarps; ++w) v = fmaxf(v, red_m[w][tid]);
-    s_M[tid] = v;
-  }
-  __syncthreads();
-
-  float2 acc[GROUP];
-  float lacc[GROUP];
-#pragma unroll
-  for (int h = 0; h < GROUP; ++h) {
-    acc[h] = make_float2(0.f, 0.f);
-    lacc[h] = 0.f;
-  }
-  // Each warp takes kMergeUnroll partials per round and issues all their loads before
-  // combining them, so a round costs one memory latency.
-  for (int k0 = warp * kMergeUnroll; k0 < n; k0 += kWarps * kMergeUnroll) {
-    float mk[kMergeUnroll][GROUP], lk[kMergeUnroll][GROUP];
-    float2 vk[kMergeUnroll][GROUP];
-#pragma unroll
-    for (int u = 0; u < kMergeUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int k = k0 + u;
       const bool use = k < n && !empty_run(k);
 #pragma unroll
-      for (int h = 0; h < GROUP; ++h) {
+      for (int h = 0; h < HPC; ++h) {
         if (use) {
           const float* r = record(k, h);
           mk[u][h] = r[kHeadDim];
@@ -923,30 +911,47 @@ merge_partials_kernel(const KParams p) {
       }
     }
 #pragma unroll
-    for (int u = 0; u < kMergeUnroll; ++u) {
+    for (int h = 0; h < HPC; ++h) {
+      float mu = mk[0][h];
 #pragma unroll
-      for (int h = 0; h < GROUP; ++h) {
-        const float wgt = fast_exp2(mk[u][h] - s_M[h]);  // 0 for unused slots (-inf)
-        lacc[h] += wgt * lk[u][h];
-        acc[h].x += wgt * vk[u][h].x;
-        acc[h].y += wgt * vk[u][h].y;
+      for (int u = 1; u < U; ++u) mu = fmaxf(mu, mk[u][h]);
+      const float nm = fmaxf(M[h], mu);
+      if (nm == -INFINITY) continue;  // nothing of this head loaded yet
+      const float keep = M[h] == -INFINITY ? 0.f : fast_exp2(M[h] - nm);
+      L[h] *= keep;
+      A[h].x *= keep;
+      A[h].y *= keep;
+      M[h] = nm;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const float wgt = mk[u][h] == -INFINITY ? 0.f : fast_exp2(mk[u][h] - nm);
+        L[h] += wgt * lk[u][h];
+        A[h].x += wgt * vk[u][h].x;
+        A[h].y += wgt * vk[u][h].y;
       }
     }
   }
 #pragma unroll
-  for (int h = 0; h < GROUP; ++h) {
-    red_o[warp][h][2 * lane] = acc[h].x;
-    red_o[warp][h][2 * lane + 1] = acc[h].y;
-    if (lane == 0) red_l[warp][h] = lacc[h];
+  for (int h = 0; h < HPC; ++h) {
+    red_o[warp][h][2 * lane] = A[h].x;
+    red_o[warp][h][2 * lane + 1] = A[h].y;
+    if (lane == 0) {
+      red_m[warp][h] = M[h];
+      red_l[warp][h] = L[h];
+    }
   }
   __syncthreads();
-  for (int e = tid; e < GROUP * kHeadDim; e += kMergeThreads) {
+  for (int e = tid; e < HPC * kHeadDim; e += kMergeThreads) {
     const int h = e / kHeadDim;
     const int d = e % kHeadDim;
+    float gm = -INFINITY;
+    for (int w = 0; w < kWarps; ++w) gm = fmaxf(gm, red_m[w][h]);
     float o = 0.f, lsum = 0.f;
     for (int w = 0; w < kWarps; ++w) {
-      o += red_o[w][h][d];
-      lsum += red_l[w][h];
+      if (red_m[w][h] == -INFINITY) continue;  // a warp without partials
+      const float wgt = fast_exp2(red_m[w][h] - gm);
+      o += wgt * red_o[w][h][d];
+      lsum += wgt * red_l[w][h];
     }
     out[e] = __float2bfloat16_rn(o / lsum);
   }
@@ -1042,11 +1047,19 @@ cudaError_t launch(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t str
     if (e == cudaSuccess) e = cudaGetLastError();
   }
   if (e != cudaSuccess || plan.fused_merge) return e;
-  const dim3 mgrid(a.num_kv_heads, a.num_seqs);
-  if (a.q_rows != nullptr)
-    merge_partials_kernel<GROUP, true><<<mgrid, kMergeThreads, 0, stream>>>(p);
-  else
-    merge_partials_kernel<GROUP, false><<<mgrid, kMergeThreads, 0, stream>>>(p);
+  if (plan.merge_split_heads && GROUP > 1) {  // one CTA per query head
+    const dim3 mgrid(a.num_kv_heads * GROUP, a.num_seqs);
+    if (a.q_rows != nullptr)
+      merge_partials_kernel<GROUP, 1, true><<<mgrid, kMergeThreads, 0, stream>>>(p);
+    else
+      merge_partials_kernel<GROUP, 1, false><<<mgrid, kMergeThreads, 0, stream>>>(p);
+  } else {  // one CTA per kv head
+    const dim3 mgrid(a.num_kv_heads, a.num_seqs);
+    if (a.q_rows != nullptr)
+      merge_partials_kernel<GROUP, GROUP, true><<<mgrid, kMergeThreads, 0, stream>>>(p);
+    else
+      merge_partials_kernel<GROUP, GROUP, false><<<mgrid, kMergeThreads, 0, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 
@@ -1098,6 +1111,12 @@ cudaError_t plan_decode(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_he
   const int64_t ctas = (runs + kWarps - 1) / kWarps;
   plan->grid = static_cast<int>(ctas < resident ? ctas : resident);
   plan->fused_merge = partition_tokens == 0 && max_context_len <= kFusedMergeMaxContext;
+  // Pieces per (sequence, kv head) segment at the longest context: with many, the merge
+  // kernel spreads each segment's query heads over separate CTAs.
+  const int64_t seg_pieces =
+      partition_tokens > 0 ? (max_context_len + partition_tokens - 1) / partition_tokens
+                           : runs / (static_cast<int64_t>(num_seqs) * num_kv_heads) + 2;
+  plan->merge_split_heads = !plan->fused_merge && seg_pieces >= kMergeSplitPieces;
   plan->ws_count_offset = (16 + sizeof(int32_t) * (num_seqs + 1) + 255) / 256 * 256;
   plan->ws_meta_bytes = plan->ws_count_offset +
                         (sizeof(int32_t) * num_seqs * num_kv_heads + 255) / 256 * 256;

@@ -37,6 +37,7 @@ struct DecodePlan {
   int64_t tile_bound; // > 0: host upper bound of the tile count, checked on the device
   size_t smem_bytes;  // dynamic shared memory of the attention kernel
   bool fused_merge;          // split segments merged inside the attention kernel
+  bool merge_split_heads;    // otherwise: the merge kernel takes one CTA per query head
   size_t ws_count_offset;    // offset of the per-segment piece counters (must start zeroed)
   size_t ws_meta_bytes;      // offset of the partials inside the workspace
   size_t workspace_bytes;    // total workspace
