@@ -47,9 +47,10 @@ def parse_args():
     ap.add_argument("--workload", default="decode_b256",
                     choices=["single_seq_300", "decode_b64", "decode_b256", "long_context_b4",
                              "mixed_step"])
-    ap.add_argument("--mixed", choices=["split", "unified"], default="split",
-                    help="steps with prefill chunks and decode rows: pa_prefill_chunk + "
-                         "pa_decode, or one pa_attention_varlen over all sequences")
+    ap.add_argument("--mixed", choices=["split", "unified", "concurrent"], default="split",
+                    help="steps with prefill chunks and decode rows: pa_prefill_chunk then "
+                         "pa_decode; one pa_attention_varlen over all sequences; or the "
+                         "decode on part of the SMs with the chunk prefill beside it")
     ap.add_argument("--append", choices=["fused", "separate"], default="fused",
                     help="decode-only steps: store the new tokens inside the decode launch "
                          "(pa_decode_append) or with pa_reshape_and_cache first")
@@ -122,6 +123,27 @@ def measured_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+# The decode beside the chunk prefill (PA_LAUNCH_MAX_SMS): the decode's share of the SMs is
+# chosen so that both end together, from per-SM rates measured on a GB300 (decode with one
+# CTA per SM: about 64 GB/s of K/V per SM, 6.2 TB/s at most in all; chunk prefill: about
+# 3.75 TFLOP/s of causal-useful work per SM at two CTAs per SM).
+DECODE_GBS_PER_SM = 64.0
+DECODE_GBS_MAX = 6200.0
+PREFILL_TFLOPS_PER_SM = 3.75
+
+
+def concurrent_decode_sms(decode_bytes: float, prefill_flops: float, sms: int) -> int:
+    """SMs for the decode when it runs beside the chunk prefill on the others."""
+    best = None
+    for d in range(1, sms):
+        t_dec = decode_bytes / (min(d * DECODE_GBS_PER_SM, DECODE_GBS_MAX) * 1e9)
+        t_pre = prefill_flops / ((sms - d) * PREFILL_TFLOPS_PER_SM * 1e12)
+        t = max(t_dec, t_pre)
+        if best is None or t < best[0]:
+            best = (t, d)
+    return best[1]
 
 
 def workload(key: str, layers=None, seed_offset=0):
@@ -278,6 +300,8 @@ class DeviceStep:
         # unified: one varlen call serves the chunks (first) and the decode rows of a step
         self.unified = bool(mixed == "unified" and w.num_prefill and w.num_decode
                             and self.one_token_each is False)
+        # concurrent: the decode on decode_sms SMs, the chunk prefill beside it on the rest
+        self.concurrent = bool(mixed == "concurrent" and w.num_prefill and w.num_decode)
         self.all_qsl = i32(np.concatenate([w.prefill_query_start_loc[: w.num_prefill + 1]
                                            if w.num_prefill else [0],
                                            self.n_pre_rows + np.arange(1, w.num_decode + 1)]))
@@ -315,6 +339,10 @@ class DeviceStep:
             need = pa.pa_decode_workspace_size(w.num_decode, w.num_kv_heads, w.num_q_heads,
                                                self.max_ctx_dec, w.partition_tokens)
             self.ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
+        if self.concurrent:
+            self.sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            self.decode_sms = concurrent_decode_sms(w.decode_kv_bytes() / w.layers,
+                                                    self.prefill_flops() / w.layers, self.sms)
         assert pa.pa_check_device_status(self.status) == pa.PA_OK
 
     def _carve_set(self) -> dict:
@@ -395,6 +423,17 @@ class DeviceStep:
                 if dec_events is not None:
                     dec_events[li][1].record()
                 continue
+            if self.concurrent:
+                # the decode on decode_sms SMs, then the chunk prefill starting at once on
+                # the other SMs (it writes and reads nothing the decode touches)
+                pa.pa_decode(L["out_dec"], L["q_dec"], kc, vc, S["bt_dec"], S["ctx_dec"],
+                             w.scale, self.max_ctx_dec, w.partition_tokens, workspace=self.ws,
+                             launch_flags=pa.PA_LAUNCH_MAX_SMS(self.decode_sms))
+                pa.pa_prefill_chunk(L["out_pre"], L["q_pre"], self.pre_qsl, self.max_q_pre,
+                                    kc, vc, S["bt_pre"], S["ctx_pre"], w.scale,
+                                    launch_flags=pa.PA_LAUNCH_OVERLAP_PREVIOUS |
+                                    pa.PA_LAUNCH_MAX_SMS(self.sms - self.decode_sms))
+                continue
             if w.num_prefill:
                 if pre_events is not None:
                     pre_events[li][0].record()
@@ -448,9 +487,11 @@ def time_steps(st, dev, K: int, warmup: int, flush_l2, use_graph: bool, barrier=
     barrier()
     n_kernel = min(K, 20) if use_graph else K
     mk = lambda: [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-    dec_ev = [[mk() for _ in range(w.layers)] for _ in range(K)]
+    # (a concurrent step's kernels overlap: no per-kernel events)
+    dec_ev = [[mk() for _ in range(w.layers)] for _ in range(K)] \
+        if w.num_decode and not st.concurrent else None
     pre_ev = [[mk() for _ in range(w.layers)] for _ in range(K)] \
-        if w.num_prefill and not st.unified else None
+        if w.num_prefill and not st.unified and not st.concurrent else None
     step_ev = [mk() for _ in range(K)]
     if sampler is not None:
         sampler.start()
@@ -471,20 +512,20 @@ def time_steps(st, dev, K: int, warmup: int, flush_l2, use_graph: bool, barrier=
         if graph is not None:
             graph.replay()
         else:
-            st.step(dec_ev[k] if w.num_decode else None, pre_ev[k] if pre_ev else None)
+            st.step(dec_ev[k] if dec_ev else None, pre_ev[k] if pre_ev else None)
         step_ev[k][1].record()
     torch.cuda.synchronize(dev)
-    if graph is not None:  # per-kernel timing: an eager pass right after, same workload
+    if graph is not None and dec_ev:  # per-kernel timing: an eager pass right after
         for k in range(n_kernel):
             if flush_l2 is not None:
                 flush_l2(k)
-            st.step(dec_ev[k] if w.num_decode else None, pre_ev[k] if pre_ev else None)
+            st.step(dec_ev[k] if dec_ev else None, pre_ev[k] if pre_ev else None)
         torch.cuda.synchronize(dev)
     barrier()
     wall = time.perf_counter() - t_wall
     res = {"step_ms": sum(a.elapsed_time(b) for a, b in step_ev) / K, "wall": wall,
            "graph": graph, "clocks": None, "dec_ms": None, "pre_ms": None}
-    if w.num_decode:
+    if dec_ev:
         res["dec_ms"] = sum(a.elapsed_time(b) for row in dec_ev[:n_kernel] for a, b in row) / (
             n_kernel * w.layers)
     if pre_ev:
@@ -609,6 +650,11 @@ def run_gpu(args, rank, world):
                        **({"overlap": "layers after the first start under programmatic "
                                       "dependent launch (PA_LAUNCH_OVERLAP_PREVIOUS)"}
                           if st.fused_append and w.layers > 1 else
+                          {"overlap": f"the decode on {st.decode_sms} SMs "
+                                      "(PA_LAUNCH_MAX_SMS), the chunk prefill beside it on "
+                                      f"the other {st.sms - st.decode_sms} "
+                                      "(PA_LAUNCH_OVERLAP_PREVIOUS)"}
+                          if st.concurrent else
                           {"overlap": "the decode starts under programmatic dependent launch "
                                       "behind the chunk prefill (PA_LAUNCH_OVERLAP_PREVIOUS)"}
                           if w.num_prefill and w.num_decode and not st.unified else {}),
@@ -649,12 +695,15 @@ def run_gpu(args, rank, world):
 # standalone KV store: (name, workload, timed steps, layers or None for the workload's own).
 # The batch-64 decode is measured twice: one layer with L2 flushed before every step (one
 # launch alone), and back to back over 16 layers, each with its own pool (2.2 GB per step,
-# no flush), the later layers overlapping the earlier ones as in the default step.
-SECONDARY = (("single_seq_300", "single_seq_300", 200, None),
-             ("decode_b64", "decode_b64", 100, None),
-             ("decode_b64_16layers", "decode_b64", 50, 16),
-             ("long_context_b4", "long_context_b4", 30, None),
-             ("mixed_step", "mixed_step", 30, None))
+# no flush), the later layers overlapping the earlier ones as in the default step.  The
+# mixed step is measured twice too: chunk prefill then decode (each kernel on every SM,
+# timed one by one), and the decode on part of the SMs with the chunk prefill beside it.
+SECONDARY = (("single_seq_300", "single_seq_300", 200, None, "split"),
+             ("decode_b64", "decode_b64", 100, None, "split"),
+             ("decode_b64_16layers", "decode_b64", 50, 16, "split"),
+             ("long_context_b4", "long_context_b4", 30, None, "split"),
+             ("mixed_step", "mixed_step", 30, None, "split"),
+             ("mixed_step_concurrent", "mixed_step", 30, None, "concurrent"))
 
 
 def run_secondary(args, dev, local: int, peak: float, peak_src: str) -> dict:
@@ -664,11 +713,11 @@ def run_secondary(args, dev, local: int, peak: float, peak_src: str) -> dict:
     sampler.start()
     time.sleep(0.2)
     sampler.mark_start()
-    for name, key, K, layers in SECONDARY:
-        if key == args.workload and layers is None:
+    for name, key, K, layers, mixed in SECONDARY:
+        if key == args.workload and layers is None and mixed == args.mixed:
             continue
         w = workload(key, layers)
-        st = DeviceStep(w, dev, fused_append=True, mixed="split")
+        st = DeviceStep(w, dev, fused_append=True, mixed=mixed)
         kv = w.decode_kv_bytes()
         flush_l2 = make_flush(dev, kv, "write-read")
         t = time_steps(st, dev, K, 3, flush_l2, True)
@@ -681,6 +730,13 @@ def run_secondary(args, dev, local: int, peak: float, peak_src: str) -> dict:
                        else "pa_compute_slot_mapping + pa_reshape_and_cache")}
         if layers is not None:
             d["layers"] = int(w.layers)
+        if st.concurrent:
+            d["schedule"] = (f"decode on {st.decode_sms} SMs (PA_LAUNCH_MAX_SMS), chunk prefill "
+                             f"beside it on the other {st.sms - st.decode_sms} "
+                             "(PA_LAUNCH_OVERLAP_PREVIOUS); the kernels overlap, so no "
+                             "per-kernel times")
+            d["prefill_tflops_over_step"] = round(
+                st.prefill_flops() / (t["step_ms"] * 1e-3) / 1e12, 1)
         if t["dec_ms"]:
             d["roofline"] = decode_roofline(st, key, t["dec_ms"], peak, peak_src,
                                             step_ms=t["step_ms"])

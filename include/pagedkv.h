@@ -142,9 +142,17 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t 
  * pa_decode_append on the same layer) does not.  The decode and chunk-prefill kernels of
  * this library (pa_prefill_chunk, pa_attention_varlen) let a following launch that carries
  * the flag start early; a launch without it waits for the previous kernel as usual.  Also
- * valid inside CUDA graph capture.  Unknown bits are rejected (PA_ERR_INVALID_ARG). */
+ * valid inside CUDA graph capture.
+ * PA_LAUNCH_MAX_SMS(n), n in 1 .. 65535, ORed into the flags, spreads the persistent grid
+ * over at most n SMs (one decode CTA or two chunk-prefill CTAs per SM) instead of all of
+ * them, so that a kernel launched next with PA_LAUNCH_OVERLAP_PREVIOUS runs on the other
+ * SMs at the same time: a memory-bound decode beside a tensor-core chunk prefill, as in a
+ * continuous-batching step ("vLLM", section Continuous Batching).  The work is the same;
+ * only where and when it runs changes.  Other unknown bits are rejected
+ * (PA_ERR_INVALID_ARG). */
 #define PA_LAUNCH_DEFAULT 0u
 #define PA_LAUNCH_OVERLAP_PREVIOUS 1u
+#define PA_LAUNCH_MAX_SMS(n) ((uint32_t)(n) << 16)
 
 /* Paged decode attention.  Defined by: "vLLM" (blog.rlaisqls.com), section Flash Attention
  * (S = Q K^T, P = softmax(S), O = P V, evaluated block by block with a running max and sum),
@@ -169,7 +177,8 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t 
  *                    in equal numbers per streaming warp)
  *   workspace        zero-initialised device buffer of >= pa_decode_workspace_size(...)
  *                    bytes (see pa_decode_workspace_size)
- *   launch_flags     PA_LAUNCH_DEFAULT or PA_LAUNCH_OVERLAP_PREVIOUS (see there)
+ *   launch_flags     PA_LAUNCH_DEFAULT, PA_LAUNCH_OVERLAP_PREVIOUS and/or
+ *                    PA_LAUNCH_MAX_SMS(n) (see there)
  * num_seqs == 0 is a no-op.  At most 4096 sequences per call. */
 pa_status pa_decode(void* out, const void* q, const void* key_cache, const void* value_cache,
                     pa_cache_desc cd, const int32_t* block_tables,
@@ -216,6 +225,21 @@ pa_status pa_prefill_chunk(void* out, const void* q, const int32_t* query_start_
                            const int32_t* context_lens, int32_t num_seqs,
                            int32_t num_q_heads, float scale, int32_t* device_status,
                            pa_stream_t stream);
+
+/* pa_prefill_chunk with launch flags (see PA_LAUNCH_OVERLAP_PREVIOUS and
+ * PA_LAUNCH_MAX_SMS).  With PA_LAUNCH_OVERLAP_PREVIOUS the chunk kernel may run from its
+ * first instruction while the previous kernel in the stream is still running (it waits for
+ * that kernel only before it ends, so its completion still implies the previous kernel's):
+ * set it only when that kernel writes nothing this call reads or writes (a decode of other
+ * sequences without the fused store qualifies).  Results are bit-identical to
+ * pa_prefill_chunk whatever the flags. */
+pa_status pa_prefill_chunk_ex(void* out, const void* q, const int32_t* query_start_loc,
+                              int32_t num_query_tokens, int32_t max_query_len,
+                              const void* key_cache, const void* value_cache, pa_cache_desc cd,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* context_lens, int32_t num_seqs,
+                              int32_t num_q_heads, float scale, uint32_t launch_flags,
+                              int32_t* device_status, pa_stream_t stream);
 
 /* Bytes of device workspace pa_attention_varlen needs on the current device for a batch of
  * num_seqs sequences carrying num_query_tokens query rows, for any head count and context

@@ -44,6 +44,13 @@ PA_DECODE_STATIC_SCRATCH_BYTES = 8 << 20
 PA_LAUNCH_DEFAULT = 0
 PA_LAUNCH_OVERLAP_PREVIOUS = 1
 
+
+def PA_LAUNCH_MAX_SMS(n: int) -> int:
+    """Launch-flag bits confining a persistent grid to at most n SMs (1 .. 65535)."""
+    if not 1 <= int(n) <= 0xFFFF:
+        raise ValueError(f"PA_LAUNCH_MAX_SMS: n = {n} outside 1 .. 65535")
+    return int(n) << 16
+
 # Every symbol include/pagedkv.h declares.
 EXPORTED = ("pa_compute_slot_mapping", "pa_reshape_and_cache", "pa_decode_workspace_size",
             "pa_decode", "pa_prefill_chunk", "pa_check_device_status", "pa_status_string",
@@ -51,7 +58,8 @@ EXPORTED = ("pa_compute_slot_mapping", "pa_reshape_and_cache", "pa_decode_worksp
             "pa_bm_destroy", "pa_bm_num_free_blocks", "pa_bm_ref_count", "pa_bm_add_sequence",
             "pa_bm_fork", "pa_bm_append_tokens", "pa_bm_free_sequence", "pa_bm_num_tokens",
             "pa_bm_block_table", "pa_decode_append", "pa_selftest_wait_timeout",
-            "pa_varlen_workspace_size", "pa_attention_varlen", "pa_stream_read")
+            "pa_varlen_workspace_size", "pa_attention_varlen", "pa_stream_read",
+            "pa_prefill_chunk_ex")
 
 
 def library_path() -> str:
@@ -83,6 +91,9 @@ def load(path: str | None = None):
     lib.pa_prefill_chunk.argtypes = [P, P, P, i32, i32, P, P, CacheDesc, P, i32, P, i32, i32,
                                      f32, P, P]
     lib.pa_prefill_chunk.restype = st
+    lib.pa_prefill_chunk_ex.argtypes = [P, P, P, i32, i32, P, P, CacheDesc, P, i32, P, i32, i32,
+                                        f32, u32, P, P]
+    lib.pa_prefill_chunk_ex.restype = st
     lib.pa_varlen_workspace_size.argtypes = [i32, i32]
     lib.pa_varlen_workspace_size.restype = sz
     lib.pa_attention_varlen.argtypes = [P, P, P, i32, i32, P, P, CacheDesc, P, i32, P, i32,
@@ -304,8 +315,11 @@ def pa_decode_static_scratch(out, q, key_cache, value_cache, block_tables, conte
 
 
 def pa_prefill_chunk(out, q, query_start_loc, max_query_len, key_cache, value_cache,
-                     block_tables, context_lens, scale, device_status=None, stream=None):
-    """Causal chunked-prefill attention; writes out [Tq, Hq, D] (bf16)."""
+                     block_tables, context_lens, scale, device_status=None, stream=None,
+                     launch_flags=PA_LAUNCH_DEFAULT):
+    """Causal chunked-prefill attention; writes out [Tq, Hq, D] (bf16).  launch_flags (see
+    PA_LAUNCH_OVERLAP_PREVIOUS and PA_LAUNCH_MAX_SMS in include/pagedkv.h) go through
+    pa_prefill_chunk_ex."""
     _need(out, "out", torch.bfloat16, 3)
     _need(q, "q", torch.bfloat16, 3)
     _need(query_start_loc, "query_start_loc", torch.int32, 1)
@@ -317,13 +331,16 @@ def pa_prefill_chunk(out, q, query_start_loc, max_query_len, key_cache, value_ca
     if out.shape != q.shape or query_start_loc.shape[0] != num_seqs + 1 or \
             block_tables.shape[0] != num_seqs:
         raise ValueError("prefill argument shapes disagree")
-    st = load().pa_prefill_chunk(_ptr(out), _ptr(q), _ptr(query_start_loc), q.shape[0],
-                                 int(max_query_len),
-                                 _ptr(key_cache), _ptr(value_cache), cache_desc(key_cache),
-                                 _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
-                                 num_seqs, q.shape[1], float(scale), _ptr(device_status),
-                                 _stream(stream))
-    _check(st, "pa_prefill_chunk")
+    args = (_ptr(out), _ptr(q), _ptr(query_start_loc), q.shape[0], int(max_query_len),
+            _ptr(key_cache), _ptr(value_cache), cache_desc(key_cache), _ptr(block_tables),
+            block_tables.shape[1], _ptr(context_lens), num_seqs, q.shape[1], float(scale))
+    if launch_flags == PA_LAUNCH_DEFAULT:
+        st = load().pa_prefill_chunk(*args, _ptr(device_status), _stream(stream))
+        _check(st, "pa_prefill_chunk")
+    else:
+        st = load().pa_prefill_chunk_ex(*args, int(launch_flags), _ptr(device_status),
+                                        _stream(stream))
+        _check(st, "pa_prefill_chunk_ex")
     return out
 
 

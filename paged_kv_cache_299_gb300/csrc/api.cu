@@ -13,6 +13,9 @@ int decode_max_seqs();
 
 namespace {
 
+// the launch-flag bits the attention calls accept (the SM budget takes bits 16-31)
+constexpr uint32_t kKnownLaunchFlags = PA_LAUNCH_OVERLAP_PREVIOUS | 0xFFFF0000u;
+
 thread_local char g_last_error[256] = "";
 
 pa_status fail(pa_status st, const char* fmt, ...) {
@@ -170,11 +173,11 @@ static pa_status decode_impl(void* out, const void* q, const void* k_new, const 
   if (!(scale > 0.f) || !isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale %g", scale);
   if ((k_new == nullptr) != (v_new == nullptr) || (k_new && (!aligned16(k_new) || !aligned16(v_new))))
     return fail(PA_ERR_INVALID_ARG, "k_new / v_new: both or neither, 16-byte aligned");
-  if (launch_flags & ~static_cast<uint32_t>(PA_LAUNCH_OVERLAP_PREVIOUS))
+  if (launch_flags & ~kKnownLaunchFlags)
     return fail(PA_ERR_INVALID_ARG, "unknown launch flags 0x%x", launch_flags);
   pkv::DecodePlan plan;
   cudaError_t e = pkv::plan_decode(num_seqs, cd.num_kv_heads, num_q_heads, max_context_len,
-                                   partition_tokens, &plan);
+                                   partition_tokens, &plan, static_cast<int32_t>(launch_flags >> 16));
   if (e != cudaSuccess) return from_cuda(e, "decode plan");
   if (!workspace || workspace_bytes < plan.workspace_bytes || !aligned16(workspace))
     return fail(PA_ERR_WORKSPACE, "workspace %zu bytes at %p, need %zu (16-byte aligned)",
@@ -282,6 +285,28 @@ pa_status chunk_args(void* out, const void* q, const int32_t* query_start_loc,
 
 }  // namespace
 
+pa_status pa_prefill_chunk_ex(void* out, const void* q, const int32_t* query_start_loc,
+                              int32_t num_query_tokens, int32_t max_query_len,
+                              const void* key_cache, const void* value_cache, pa_cache_desc cd,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* context_lens, int32_t num_seqs,
+                              int32_t num_q_heads, float scale, uint32_t launch_flags,
+                              int32_t* device_status, pa_stream_t stream) {
+  pkv::PrefillArgs a;
+  bool skip;
+  pa_status st = chunk_args(out, q, query_start_loc, num_query_tokens, max_query_len, key_cache,
+                            value_cache, cd, block_tables, max_blocks_per_seq, context_lens,
+                            num_seqs, num_q_heads, scale, device_status, &a, &skip);
+  if (st != PA_OK) return st;
+  if (launch_flags & ~kKnownLaunchFlags)
+    return fail(PA_ERR_INVALID_ARG, "unknown launch flags 0x%x", launch_flags);
+  if (skip) return ok();
+  return from_cuda(pkv::launch_prefill(a, reinterpret_cast<cudaStream_t>(stream),
+                                       (launch_flags & PA_LAUNCH_OVERLAP_PREVIOUS) != 0,
+                                       static_cast<int32_t>(launch_flags >> 16)),
+                   "prefill launch");
+}
+
 pa_status pa_prefill_chunk(void* out, const void* q, const int32_t* query_start_loc,
                            int32_t num_query_tokens, int32_t max_query_len,
                            const void* key_cache,
@@ -290,14 +315,10 @@ pa_status pa_prefill_chunk(void* out, const void* q, const int32_t* query_start_
                            const int32_t* context_lens, int32_t num_seqs,
                            int32_t num_q_heads, float scale, int32_t* device_status,
                            pa_stream_t stream) {
-  pkv::PrefillArgs a;
-  bool skip;
-  pa_status st = chunk_args(out, q, query_start_loc, num_query_tokens, max_query_len, key_cache,
-                            value_cache, cd, block_tables, max_blocks_per_seq, context_lens,
-                            num_seqs, num_q_heads, scale, device_status, &a, &skip);
-  if (st != PA_OK || skip) return st == PA_OK ? ok() : st;
-  return from_cuda(pkv::launch_prefill(a, reinterpret_cast<cudaStream_t>(stream)),
-                   "prefill launch");
+  return pa_prefill_chunk_ex(out, q, query_start_loc, num_query_tokens, max_query_len,
+                             key_cache, value_cache, cd, block_tables, max_blocks_per_seq,
+                             context_lens, num_seqs, num_q_heads, scale, PA_LAUNCH_DEFAULT,
+                             device_status, stream);
 }
 
 size_t pa_varlen_workspace_size(int32_t num_seqs, int32_t num_query_tokens) {

@@ -1066,7 +1066,8 @@ cudaError_t launch(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t str
 }  // namespace
 
 cudaError_t plan_decode(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_heads,
-                        int32_t max_context_len, int32_t partition_tokens, DecodePlan* plan) {
+                        int32_t max_context_len, int32_t partition_tokens, DecodePlan* plan,
+                        int32_t max_sms) {
   const int group = num_q_heads / num_kv_heads;
   plan->group = group;
   int ctas_per_sm = 0;
@@ -1086,7 +1087,9 @@ cudaError_t plan_decode(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_he
   if (ctas_per_sm < 1) return cudaErrorInvalidConfiguration;
   const int64_t blocks_max = (static_cast<int64_t>(max_context_len) + kBlockSize - 1) / kBlockSize;
   const int64_t tiles_upper = static_cast<int64_t>(num_seqs) * num_kv_heads * blocks_max;
-  const int64_t resident = static_cast<int64_t>(sms) * ctas_per_sm;
+  // max_sms > 0: the persistent grid spreads over at most that many SMs
+  const int64_t resident =
+      static_cast<int64_t>(max_sms > 0 && max_sms < sms ? max_sms : sms) * ctas_per_sm;
   int64_t runs;
   plan->tile_bound = 0;
   if (partition_tokens > 0) {

@@ -44,8 +44,11 @@ struct DecodePlan {
 };
 
 // Returns cudaSuccess and fills `plan`, or an error (e.g. no device).
+// max_sms > 0 confines the persistent grid to that many SMs (the rest stay free for a
+// kernel launched beside it).
 cudaError_t plan_decode(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_heads,
-                        int32_t max_context_len, int32_t partition_tokens, DecodePlan* plan);
+                        int32_t max_context_len, int32_t partition_tokens, DecodePlan* plan,
+                        int32_t max_sms = 0);
 
 struct DecodeArgs {
   void* out;
@@ -98,7 +101,11 @@ struct PrefillArgs {
   int32_t* status;
 };
 
-cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+// overlap_previous: programmatic dependent launch behind the previous kernel in the stream
+// (the kernel waits for it only at its end); max_sms > 0: at most two CTAs on each of that
+// many SMs.
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream, bool overlap_previous = false,
+                           int32_t max_sms = 0);
 
 // Unified varlen launch: the decode kernel serves the one-row sequences in place (the
 // workspace is its workspace), the chunk kernel the others.  Sizes on the current device:

@@ -888,7 +888,7 @@ cudaError_t prepare(const PrefillArgs& a, CUtensorMap* tq, CUtensorMap* tk, CUte
 namespace {
 
 cudaError_t launch_prefill_kernel(const PrefillArgs& a, bool skip_single, cudaStream_t stream,
-                                  bool overlap_previous = false) {
+                                  bool overlap_previous = false, int32_t max_sms = 0) {
   CUtensorMap tq, tk, tv;
   PParams p;
   cudaError_t e = prepare(a, &tq, &tk, &tv, &p);
@@ -898,6 +898,7 @@ cudaError_t launch_prefill_kernel(const PrefillArgs& a, bool skip_single, cudaSt
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return e;
+  if (max_sms > 0 && max_sms < sms) sms = max_sms;
   // persistent: two CTAs per SM, never more CTAs than work units can exist
   const int64_t units_upper = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads * p.q_tiles;
   const int64_t grid = units_upper < 2LL * sms ? units_upper : 2LL * sms;
@@ -928,8 +929,9 @@ cudaError_t varlen_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t n
 
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
-  return launch_prefill_kernel(a, false, stream);
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream, bool overlap_previous,
+                           int32_t max_sms) {
+  return launch_prefill_kernel(a, false, stream, overlap_previous, max_sms);
 }
 
 bool varlen_routes_decode_rows(int32_t num_seqs) { return num_seqs <= decode_max_seqs(); }

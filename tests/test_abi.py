@@ -81,10 +81,20 @@ def test_host_rejects_bad_arguments_without_touching_the_device():
                          ctypes.c_float(0.125), 64, 0, fake, 1 << 20, 0, None,
                          None) == pa.PA_ERR_UNSUPPORTED
     assert b"2^31" in lib.pa_last_error()
-    # launch flags: unknown bits are rejected before any launch
-    assert lib.pa_decode(*args, 2, 32, ctypes.c_float(0.125), 64, 0, fake, 1 << 20, 2, None,
-                         None) == pa.PA_ERR_INVALID_ARG
-    assert b"launch flags" in lib.pa_last_error()
+    # launch flags: unknown bits are rejected before any launch, with or without an SM budget
+    # (bits 16-31), and by the chunk call too
+    for flags in (2, 4 | pa.PA_LAUNCH_MAX_SMS(8), 0x8000):
+        assert lib.pa_decode(*args, 2, 32, ctypes.c_float(0.125), 64, 0, fake, 1 << 20, flags,
+                             None, None) == pa.PA_ERR_INVALID_ARG
+        assert b"launch flags" in lib.pa_last_error()
+        assert lib.pa_prefill_chunk_ex(fake, fake, fake, 16, 8, fake, fake, _desc(), fake, 4,
+                                       fake, 2, 32, ctypes.c_float(0.125), flags, None,
+                                       None) == pa.PA_ERR_INVALID_ARG
+        assert b"launch flags" in lib.pa_last_error()
+    # the chunk call's own checks come first, as in pa_prefill_chunk
+    assert lib.pa_prefill_chunk_ex(fake, fake, fake, 16, 8, fake, fake, _desc(), fake, 4, fake,
+                                   2, 8, ctypes.c_float(0.125), 0, None,
+                                   None) == pa.PA_ERR_UNSUPPORTED
     # prefill needs group 4
     assert lib.pa_prefill_chunk(fake, fake, fake, 16, 8, fake, fake, _desc(), fake, 4, fake, 2,
                                 8, ctypes.c_float(0.125), None, None) == pa.PA_ERR_UNSUPPORTED
@@ -149,3 +159,9 @@ def test_launch_flags_match_the_header():
         m = re.search(r"#define %s (\d+)u" % name, text)
         assert m, name + " not found in the header"
         assert int(m.group(1)) == getattr(pa, name)
+    m = re.search(r"#define PA_LAUNCH_MAX_SMS\(n\) \(\(uint32_t\)\(n\) << (\d+)\)", text)
+    assert m, "PA_LAUNCH_MAX_SMS not found in the header"
+    assert pa.PA_LAUNCH_MAX_SMS(88) == 88 << int(m.group(1))
+    for bad in (0, 1 << 16):
+        with pytest.raises(ValueError):
+            pa.PA_LAUNCH_MAX_SMS(bad)

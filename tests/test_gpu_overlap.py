@@ -125,3 +125,57 @@ def test_decode_behind_a_chunk_prefill_overlaps_it():
     ref = oracle_step(w, host_vals(st.vals))["decode"]
     mx, mean = errors(over_d.float().cpu().numpy(), ref)
     assert mx <= ATOL_MAX and mean <= ATOL_MEAN, (mx, mean)
+
+
+@pytest.mark.parametrize("decode_share", [1, 40, "half", "all_but_one"])
+def test_decode_beside_a_chunk_prefill_on_separate_sms(decode_share):
+    """The mixed step with the decode confined to part of the SMs (PA_LAUNCH_MAX_SMS) and the
+    chunk prefill launched right behind it on the other SMs (PA_LAUNCH_OVERLAP_PREVIOUS |
+    PA_LAUNCH_MAX_SMS), so that both run at the same time: the chunk rows are bit-identical
+    to the serial launches (a unit's arithmetic does not depend on the grid), the decode
+    rows match the oracle (with fewer warps the split points move, so their rounding may
+    differ from the serial decode's), eagerly and replayed from a CUDA graph."""
+    w = wl.mixed_prefill_decode()
+    st = GpuStep(w)
+    P = w.num_prefill
+    qsl = torch.from_numpy(w.prefill_query_start_loc.astype("int32")).cuda()
+    max_q = int(w.new_lens[:P].max())
+    bt_p, ctx_p = st.bt[:P].contiguous(), st.ctx[:P].contiguous()
+    bt_d, ctx_d = st.bt[P:].contiguous(), st.ctx[P:].contiguous()
+    max_ctx = int(w.decode_context_lens.max())
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    d = {1: 1, 40: 40, "half": sms // 2, "all_but_one": sms - 1}[decode_share]
+    ws = torch.zeros(pa.pa_decode_workspace_size(w.num_decode, 8, 32, max_ctx, 0),
+                     dtype=torch.uint8, device="cuda")
+    serial_p = torch.empty_like(st.vals["q_prefill"])
+    serial_d = torch.empty_like(st.vals["q_decode"])
+    pa.pa_prefill_chunk(serial_p, st.vals["q_prefill"], qsl, max_q, st.kc, st.vc, bt_p, ctx_p,
+                        w.scale, device_status=st.status)
+    pa.pa_decode(serial_d, st.vals["q_decode"], st.kc, st.vc, bt_d, ctx_d, w.scale, max_ctx,
+                 workspace=ws, device_status=st.status)
+
+    def run(out_p, out_d):
+        pa.pa_decode(out_d, st.vals["q_decode"], st.kc, st.vc, bt_d, ctx_d, w.scale, max_ctx,
+                     workspace=ws, device_status=st.status, launch_flags=pa.PA_LAUNCH_MAX_SMS(d))
+        pa.pa_prefill_chunk(out_p, st.vals["q_prefill"], qsl, max_q, st.kc, st.vc, bt_p, ctx_p,
+                            w.scale, device_status=st.status,
+                            launch_flags=pa.PA_LAUNCH_OVERLAP_PREVIOUS | pa.PA_LAUNCH_MAX_SMS(sms - d))
+
+    conc_p = torch.full_like(serial_p, float("nan"))
+    conc_d = torch.full_like(serial_d, float("nan"))
+    for _ in range(2):
+        run(conc_p, conc_d)
+    torch.cuda.synchronize()
+    assert st.check_status() == pa.PA_OK
+    assert torch.equal(serial_p, conc_p)
+    ref = oracle_step(w, host_vals(st.vals))["decode"]
+    mx, mean = errors(conc_d.float().cpu().numpy(), ref)
+    assert mx <= ATOL_MAX and mean <= ATOL_MEAN, (d, mx, mean)
+    graph_p = torch.full_like(serial_p, float("nan"))
+    graph_d = torch.full_like(serial_d, float("nan"))
+    graph = graphs.StepGraph(lambda: run(graph_p, graph_d))
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert st.check_status() == pa.PA_OK
+    assert torch.equal(graph_p, serial_p) and torch.equal(graph_d, conc_d)
