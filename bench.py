@@ -542,6 +542,20 @@ def decode_roofline(st, workload_key: str, dec_ms: float, peak: float, peak_src:
     between two events of its own would not show what the step sustains.  That isolated
     figure (an eager pass right after the timed region) is reported beside it."""
     w = st.w
+    if st.concurrent:
+        # the decode and the chunk prefill overlap: the step's time per layer bounds the
+        # decode's own duration from above (a conservative figure)
+        per_launch = w.decode_kv_bytes() / w.layers
+        launch_ms = step_ms / w.layers
+        achieved = per_launch / (launch_ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": ncu_traffic("paged_decode_kernel", workload_key),
+                "kernel": f"pa_decode on {st.decode_sms} SMs beside the chunk prefill",
+                "peak_source": f"{peak_src} hbm_gbs", "launch_ms": round(launch_ms, 5),
+                "algorithmic_bytes_per_launch": int(per_launch),
+                "timing": "timed region / layers: the decode runs beside the chunk prefill, "
+                          "so the step's time per layer stands for its duration"}
     if st.unified:
         # the varlen launch reads the K/V of every sequence of the step at least once
         per_launch = float(np.sum(w.context_lens)) * w.num_kv_heads * w.head_dim * 2 * 2
@@ -667,7 +681,7 @@ def run_gpu(args, rank, world):
         "wall_s_timed": round(t["wall"], 3),
         "clocks": t["clocks"],
     }
-    if t["dec_ms"]:
+    if t["dec_ms"] or st.concurrent:
         res["roofline"] = decode_roofline(st, args.workload, t["dec_ms"], peak, peak_src,
                                           step_ms=t["step_ms"])
     if stream_ref and "roofline" in res:
