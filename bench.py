@@ -542,7 +542,7 @@ def decode_roofline(st, workload_key: str, dec_ms: float, peak: float, peak_src:
     between two events of its own would not show what the step sustains.  That isolated
     figure (an eager pass right after the timed region) is reported beside it."""
     w = st.w
-    if st.concurrent:
+    if getattr(st, "concurrent", False):
         # the decode and the chunk prefill overlap: the step's time per layer bounds the
         # decode's own duration from above (a conservative figure)
         per_launch = w.decode_kv_bytes() / w.layers
