@@ -135,3 +135,15 @@ def test_clock_summary_keeps_the_samples_of_the_marked_region():
     assert everything["samples"] == 4 and "hw_slowdown" in everything["reasons"]
     assert everything["samples_from"].startswith("the whole sampling")
     assert bench.ClockSampler.summarise("")["samples"] == 0
+
+
+def test_concurrent_split_balances_the_two_kernels():
+    """The decode's SM share beside a chunk prefill: both modelled kernels end together,
+    more prefill work leaves fewer SMs to the decode, and the share stays within 1 .. SMs-1."""
+    import bench
+    d = bench.concurrent_decode_sms(1056923648, 45134905344, 152)  # the mixed step
+    assert 80 <= d <= 96
+    assert bench.concurrent_decode_sms(1056923648, 4 * 45134905344, 152) < d
+    assert bench.concurrent_decode_sms(4 * 1056923648, 45134905344, 152) > d
+    assert bench.concurrent_decode_sms(1.0, 1e15, 152) == 1
+    assert bench.concurrent_decode_sms(1e15, 1.0, 152) == 151
