@@ -146,4 +146,6 @@ def test_concurrent_split_balances_the_two_kernels():
     assert bench.concurrent_decode_sms(1056923648, 4 * 45134905344, 152) < d
     assert bench.concurrent_decode_sms(4 * 1056923648, 45134905344, 152) > d
     assert bench.concurrent_decode_sms(1.0, 1e15, 152) == 1
-    assert bench.concurrent_decode_sms(1e15, 1.0, 152) == 151
+    # a decode-only load takes the SMs it can use: past DECODE_GBS_MAX more SMs add nothing
+    cap = int(bench.DECODE_GBS_MAX / bench.DECODE_GBS_PER_SM)
+    assert cap <= bench.concurrent_decode_sms(1e15, 1.0, 152) <= cap + 1
