@@ -127,9 +127,9 @@ def measured_peaks():
 
 # The decode beside the chunk prefill (PA_LAUNCH_MAX_SMS): the decode's share of the SMs is
 # chosen so that both end together, from per-SM rates measured on a GB300 (decode with one
-# CTA per SM: about 64 GB/s of K/V per SM, 6.2 TB/s at most in all; chunk prefill: about
-# 3.75 TFLOP/s of causal-useful work per SM at two CTAs per SM).
-DECODE_GBS_PER_SM = 64.0
+# CTA per SM beside the prefill: about 61 GB/s of K/V per SM, 6.2 TB/s at most in all;
+# chunk prefill: about 3.75 TFLOP/s of causal-useful work per SM at two CTAs per SM).
+DECODE_GBS_PER_SM = 61.0
 DECODE_GBS_MAX = 6200.0
 PREFILL_TFLOPS_PER_SM = 3.75
 
