@@ -339,7 +339,8 @@ class DeviceStep:
             need = pa.pa_decode_workspace_size(w.num_decode, w.num_kv_heads, w.num_q_heads,
                                                self.max_ctx_dec, w.partition_tokens)
             self.ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
-        if self.concurrent:
+        if self.concurrent or self.unified:
+            # (the unified call takes the same split: decode rows on decode_sms SMs)
             self.sms = torch.cuda.get_device_properties(dev).multi_processor_count
             self.decode_sms = concurrent_decode_sms(w.decode_kv_bytes() / w.layers,
                                                     self.prefill_flops() / w.layers, self.sms)
@@ -419,7 +420,8 @@ class DeviceStep:
                     dec_events[li][0].record()
                 pa.pa_attention_varlen(L["out_all"], L["q_all"], self.all_qsl,
                                        max(self.max_q_pre, 1), kc, vc, S["bt"], S["ctx"],
-                                       w.scale, workspace=self.ws_var)
+                                       w.scale, workspace=self.ws_var,
+                                       launch_flags=pa.PA_LAUNCH_MAX_SMS(self.decode_sms))
                 if dec_events is not None:
                     dec_events[li][1].record()
                 continue
@@ -669,6 +671,10 @@ def run_gpu(args, rank, world):
                                       f"the other {st.sms - st.decode_sms} "
                                       "(PA_LAUNCH_OVERLAP_PREVIOUS)"}
                           if st.concurrent else
+                          {"overlap": f"one varlen call: decode rows on {st.decode_sms} SMs, "
+                                      f"the chunks beside them on the other "
+                                      f"{st.sms - st.decode_sms}"}
+                          if st.unified else
                           {"overlap": "the decode starts under programmatic dependent launch "
                                       "behind the chunk prefill (PA_LAUNCH_OVERLAP_PREVIOUS)"}
                           if w.num_prefill and w.num_decode and not st.unified else {}),

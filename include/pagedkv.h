@@ -275,6 +275,20 @@ pa_status pa_attention_varlen(void* out, const void* q, const int32_t* query_sta
                               size_t workspace_bytes, int32_t* device_status,
                               pa_stream_t stream);
 
+/* pa_attention_varlen with launch flags.  PA_LAUNCH_MAX_SMS(n) (the only flag it takes)
+ * puts the decode rows on n SMs and the chunks on the other SMs at the same time, instead
+ * of each kernel on every SM one after the other (see PA_LAUNCH_MAX_SMS); n at or above
+ * the SM count gives the default schedule.  Chunk rows are bit-identical either way;
+ * decode rows may differ in their last bits (the split points of long contexts move). */
+pa_status pa_attention_varlen_ex(void* out, const void* q, const int32_t* query_start_loc,
+                                 int32_t num_query_tokens, int32_t max_query_len,
+                                 const void* key_cache, const void* value_cache,
+                                 pa_cache_desc cd, const int32_t* block_tables,
+                                 int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                 int32_t num_seqs, int32_t num_q_heads, float scale,
+                                 void* workspace, size_t workspace_bytes, uint32_t launch_flags,
+                                 int32_t* device_status, pa_stream_t stream);
+
 /* Paged decode attention that needs no workspace from the caller.  The vLLM and
  * tiny-vllm pages describe no counterpart for this call.  It exists for callers that cannot allocate device memory
  * themselves: code embedded in a host program that owns every device allocation (its

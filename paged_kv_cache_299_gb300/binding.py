@@ -59,7 +59,7 @@ EXPORTED = ("pa_compute_slot_mapping", "pa_reshape_and_cache", "pa_decode_worksp
             "pa_bm_fork", "pa_bm_append_tokens", "pa_bm_free_sequence", "pa_bm_num_tokens",
             "pa_bm_block_table", "pa_decode_append", "pa_selftest_wait_timeout",
             "pa_varlen_workspace_size", "pa_attention_varlen", "pa_stream_read",
-            "pa_prefill_chunk_ex")
+            "pa_prefill_chunk_ex", "pa_attention_varlen_ex")
 
 
 def library_path() -> str:
@@ -99,6 +99,9 @@ def load(path: str | None = None):
     lib.pa_attention_varlen.argtypes = [P, P, P, i32, i32, P, P, CacheDesc, P, i32, P, i32,
                                         i32, f32, P, sz, P, P]
     lib.pa_attention_varlen.restype = st
+    lib.pa_attention_varlen_ex.argtypes = [P, P, P, i32, i32, P, P, CacheDesc, P, i32, P, i32,
+                                           i32, f32, P, sz, u32, P, P]
+    lib.pa_attention_varlen_ex.restype = st
     lib.pa_decode_static_scratch.argtypes = [P, P, P, P, CacheDesc, P, i32, P, i32, i32, f32,
                                              i32, i32, P, P]
     lib.pa_decode_static_scratch.restype = st
@@ -350,10 +353,12 @@ def pa_varlen_workspace_size(num_seqs, num_query_tokens) -> int:
 
 def pa_attention_varlen(out, q, query_start_loc, max_query_len, key_cache, value_cache,
                         block_tables, context_lens, scale, workspace=None, device_status=None,
-                        stream=None):
+                        stream=None, launch_flags=PA_LAUNCH_DEFAULT):
     """One continuous-batching step's attention (decode rows and causal chunks mixed): decode
     rows on the decode kernel, chunks on the tensor-core chunk kernel; chunk rows equal
-    pa_prefill_chunk's bit for bit, decode rows pa_decode's up to rounding."""
+    pa_prefill_chunk's bit for bit, decode rows pa_decode's up to rounding.  launch_flags:
+    PA_LAUNCH_MAX_SMS(n) runs the decode rows on n SMs beside the chunks (through
+    pa_attention_varlen_ex)."""
     _need(out, "out", torch.bfloat16, 3)
     _need(q, "q", torch.bfloat16, 3)
     _need(query_start_loc, "query_start_loc", torch.int32, 1)
@@ -368,14 +373,17 @@ def pa_attention_varlen(out, q, query_start_loc, max_query_len, key_cache, value
     if workspace is None:
         workspace = torch.empty(max(16, pa_varlen_workspace_size(num_seqs, q.shape[0])),
                                 dtype=torch.uint8, device=q.device)
-    st = load().pa_attention_varlen(_ptr(out), _ptr(q), _ptr(query_start_loc), q.shape[0],
-                                    int(max_query_len), _ptr(key_cache), _ptr(value_cache),
-                                    cache_desc(key_cache), _ptr(block_tables),
-                                    block_tables.shape[1], _ptr(context_lens), num_seqs,
-                                    q.shape[1], float(scale), _ptr(workspace),
-                                    workspace.numel() * workspace.element_size(),
-                                    _ptr(device_status), _stream(stream))
-    _check(st, "pa_attention_varlen")
+    args = (_ptr(out), _ptr(q), _ptr(query_start_loc), q.shape[0], int(max_query_len),
+            _ptr(key_cache), _ptr(value_cache), cache_desc(key_cache), _ptr(block_tables),
+            block_tables.shape[1], _ptr(context_lens), num_seqs, q.shape[1], float(scale),
+            _ptr(workspace), workspace.numel() * workspace.element_size())
+    if launch_flags == PA_LAUNCH_DEFAULT:
+        st = load().pa_attention_varlen(*args, _ptr(device_status), _stream(stream))
+        _check(st, "pa_attention_varlen")
+    else:
+        st = load().pa_attention_varlen_ex(*args, int(launch_flags), _ptr(device_status),
+                                           _stream(stream))
+        _check(st, "pa_attention_varlen_ex")
     return out
 
 

@@ -327,6 +327,35 @@ size_t pa_varlen_workspace_size(int32_t num_seqs, int32_t num_query_tokens) {
   return pkv::varlen_workspace_size(num_seqs, num_query_tokens);
 }
 
+pa_status pa_attention_varlen_ex(void* out, const void* q, const int32_t* query_start_loc,
+                                 int32_t num_query_tokens, int32_t max_query_len,
+                                 const void* key_cache, const void* value_cache,
+                                 pa_cache_desc cd, const int32_t* block_tables,
+                                 int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                 int32_t num_seqs, int32_t num_q_heads, float scale,
+                                 void* workspace, size_t workspace_bytes, uint32_t launch_flags,
+                                 int32_t* device_status, pa_stream_t stream) {
+  pkv::PrefillArgs a;
+  bool skip;
+  pa_status st = chunk_args(out, q, query_start_loc, num_query_tokens, max_query_len, key_cache,
+                            value_cache, cd, block_tables, max_blocks_per_seq, context_lens,
+                            num_seqs, num_q_heads, scale, device_status, &a, &skip);
+  if (st != PA_OK) return st;
+  if (launch_flags & ~0xFFFF0000u)  // only the decode rows' SM budget
+    return fail(PA_ERR_INVALID_ARG, "unknown launch flags 0x%x", launch_flags);
+  if (skip) return ok();
+  if (!workspace || !aligned16(workspace))
+    return fail(PA_ERR_WORKSPACE, "varlen workspace at %p (needs a 16-byte aligned buffer)",
+                workspace);
+  const size_t need = pkv::varlen_workspace_need(a);
+  if (need == 0) return fail(PA_ERR_CUDA, "varlen: decode plan failed (no device?)");
+  if (workspace_bytes < need)
+    return fail(PA_ERR_WORKSPACE, "varlen workspace %zu bytes, need %zu", workspace_bytes, need);
+  return from_cuda(pkv::launch_varlen(a, workspace, reinterpret_cast<cudaStream_t>(stream),
+                                      static_cast<int32_t>(launch_flags >> 16)),
+                   "varlen launch");
+}
+
 pa_status pa_attention_varlen(void* out, const void* q, const int32_t* query_start_loc,
                               int32_t num_query_tokens, int32_t max_query_len,
                               const void* key_cache, const void* value_cache, pa_cache_desc cd,
@@ -335,21 +364,10 @@ pa_status pa_attention_varlen(void* out, const void* q, const int32_t* query_sta
                               int32_t num_q_heads, float scale, void* workspace,
                               size_t workspace_bytes, int32_t* device_status,
                               pa_stream_t stream) {
-  pkv::PrefillArgs a;
-  bool skip;
-  pa_status st = chunk_args(out, q, query_start_loc, num_query_tokens, max_query_len, key_cache,
-                            value_cache, cd, block_tables, max_blocks_per_seq, context_lens,
-                            num_seqs, num_q_heads, scale, device_status, &a, &skip);
-  if (st != PA_OK || skip) return st == PA_OK ? ok() : st;
-  if (!workspace || !aligned16(workspace))
-    return fail(PA_ERR_WORKSPACE, "varlen workspace at %p (needs a 16-byte aligned buffer)",
-                workspace);
-  const size_t need = pkv::varlen_workspace_need(a);
-  if (need == 0) return fail(PA_ERR_CUDA, "varlen: decode plan failed (no device?)");
-  if (workspace_bytes < need)
-    return fail(PA_ERR_WORKSPACE, "varlen workspace %zu bytes, need %zu", workspace_bytes, need);
-  return from_cuda(pkv::launch_varlen(a, workspace, reinterpret_cast<cudaStream_t>(stream)),
-                   "varlen launch");
+  return pa_attention_varlen_ex(out, q, query_start_loc, num_query_tokens, max_query_len,
+                                key_cache, value_cache, cd, block_tables, max_blocks_per_seq,
+                                context_lens, num_seqs, num_q_heads, scale, workspace,
+                                workspace_bytes, PA_LAUNCH_DEFAULT, device_status, stream);
 }
 
 pa_status pa_copy_blocks(void* key_cache, void* value_cache, pa_cache_desc cd,

@@ -114,6 +114,9 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream, bool overl
 int decode_max_seqs();
 size_t varlen_workspace_size(int32_t num_seqs, int32_t num_query_tokens);
 size_t varlen_workspace_need(const PrefillArgs& a);
-cudaError_t launch_varlen(const PrefillArgs& a, void* workspace, cudaStream_t stream);
+// decode_sms in 1 .. SMs-1: the decode rows on that many SMs and the chunks on the others,
+// at the same time; 0: each kernel on every SM, one after the other.
+cudaError_t launch_varlen(const PrefillArgs& a, void* workspace, cudaStream_t stream,
+                          int32_t decode_sms = 0);
 
 }  // namespace pkv

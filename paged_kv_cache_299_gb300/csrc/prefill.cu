@@ -921,10 +921,12 @@ cudaError_t launch_prefill_kernel(const PrefillArgs& a, bool skip_single, cudaSt
 // Decode plan of a mixed batch's one-row sequences: a balanced split over the device, every
 // context bounded by its block-table row.
 cudaError_t varlen_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_heads,
-                               int32_t max_blocks_per_seq, DecodePlan* plan) {
+                               int32_t max_blocks_per_seq, DecodePlan* plan,
+                               int32_t max_sms = 0) {
   const int64_t max_ctx = static_cast<int64_t>(max_blocks_per_seq) * kBlockSize;
   return plan_decode(num_seqs, num_kv_heads, num_q_heads,
-                     static_cast<int32_t>(max_ctx < 0x7fffffff ? max_ctx : 0x7fffffff), 0, plan);
+                     static_cast<int32_t>(max_ctx < 0x7fffffff ? max_ctx : 0x7fffffff), 0, plan,
+                     max_sms);
 }
 
 }  // namespace
@@ -954,14 +956,22 @@ size_t varlen_workspace_size(int32_t num_seqs, int32_t num_query_tokens) {
   return plan.workspace_bytes;
 }
 
-cudaError_t launch_varlen(const PrefillArgs& a, void* workspace, cudaStream_t stream) {
+cudaError_t launch_varlen(const PrefillArgs& a, void* workspace, cudaStream_t stream,
+                          int32_t decode_sms) {
   if (!varlen_routes_decode_rows(a.num_seqs))  // every row on the tensor-core kernel
     return launch_prefill_kernel(a, false, stream);
+  // decode_sms in 1 .. SMs-1: the decode rows on that many SMs, the chunks beside them on
+  // the others at the same time
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const bool split = decode_sms > 0 && decode_sms < sms;
   // Decode rows (q_len 1) on the CUDA-core decode kernel, reading and writing their rows in
   // place; its workspace counters start at zero (cleared on the stream, nothing allocated).
   DecodePlan plan;
-  cudaError_t e = varlen_decode_plan(a.num_seqs, a.num_kv_heads, a.num_q_heads,
-                                     a.max_blocks_per_seq, &plan);
+  e = varlen_decode_plan(a.num_seqs, a.num_kv_heads, a.num_q_heads, a.max_blocks_per_seq, &plan,
+                         split ? decode_sms : 0);
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(static_cast<uint8_t*>(workspace) + plan.ws_count_offset, 0,
                       plan.ws_meta_bytes - plan.ws_count_offset, stream);
@@ -989,8 +999,10 @@ cudaError_t launch_varlen(const PrefillArgs& a, void* workspace, cudaStream_t st
   // q_len is 1 (a decode-only batch), and then nothing more is launched.
   if (a.max_query_len <= 1) return cudaSuccess;
   // The chunk launch reads nothing the decode launch writes and writes other rows, so it
-  // may start as the decode's CTAs leave (it waits for the decode grid before it ends).
-  return launch_prefill_kernel(a, true, stream, /*overlap_previous=*/true);
+  // may start as the decode's CTAs leave, or at once on the SMs the decode leaves free (it
+  // waits for the decode grid before it ends).
+  return launch_prefill_kernel(a, true, stream, /*overlap_previous=*/true,
+                               split ? sms - decode_sms : 0);
 }
 
 }  // namespace pkv

@@ -102,6 +102,43 @@ def test_mixed_step_matches_chunk_and_decode_kernels_and_oracle():
     check(out, np.concatenate([ref_pre, ref_dec]), "mixed step, every row")
 
 
+def test_mixed_step_with_the_decode_rows_beside_the_chunks():
+    """The same mixed step with PA_LAUNCH_MAX_SMS: the decode rows on part of the SMs, the
+    chunks on the others at the same time.  Chunk rows stay bit-identical to
+    pa_prefill_chunk, decode rows match the oracle, and unknown flags are refused."""
+    w = wl.mixed_prefill_decode()
+    step = GpuStep(w)
+    nd = w.num_decode
+    qsl_pre = w.prefill_query_start_loc
+    tp = int(qsl_pre[-1])
+    qsl = np.concatenate([qsl_pre, tp + np.arange(1, nd + 1)]).astype(np.int32)
+    q = torch.cat([step.vals["q_prefill"], step.vals["q_decode"]]).contiguous()
+    ws = torch.empty(pa.pa_varlen_workspace_size(w.num_seqs, q.shape[0]), dtype=torch.uint8,
+                     device="cuda")
+    same = torch.empty_like(q)
+    pa.pa_prefill_chunk(same, q, i32(qsl), 512, step.kc, step.vc, step.bt, step.ctx, w.scale)
+    hv = host_vals(step.vals)
+    kc, vc = oracle_pools(w, hv)
+    ref_dec = oracle_decode_rows(wl.bf16_bits(hv["q_decode"]), kc, vc, w.decode_block_tables,
+                                 w.decode_context_lens, w.scale)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for d in (2, sms // 2 + 14, sms + 10):  # the last one: the default schedule
+        out = torch.full_like(q, float("nan"))
+        for _ in range(2):
+            pa.pa_attention_varlen(out, q, i32(qsl), 512, step.kc, step.vc, step.bt, step.ctx,
+                                   w.scale, workspace=ws, device_status=step.status,
+                                   launch_flags=pa.PA_LAUNCH_MAX_SMS(d))
+        torch.cuda.synchronize()
+        assert step.check_status() == pa.PA_OK
+        assert torch.equal(out[:tp], same[:tp]), d
+        check(out[tp:], ref_dec, f"decode rows on {d} SMs")
+    with pytest.raises(pa.PagedKVError) as e:
+        pa.pa_attention_varlen(out, q, i32(qsl), 512, step.kc, step.vc, step.bt, step.ctx,
+                               w.scale, workspace=ws,
+                               launch_flags=pa.PA_LAUNCH_OVERLAP_PREVIOUS)
+    assert e.value.status == pa.PA_ERR_INVALID_ARG
+
+
 def test_empty_sequences_and_one_long_chunk():
     """q_len 0 sequences contribute nothing; a 700-row chunk (22 tiles) among decode rows."""
     hist = [40, 0, 300, 25, 1000, 7]
