@@ -148,7 +148,8 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_kv_heads, int32_t 
  * them, so that a kernel launched next with PA_LAUNCH_OVERLAP_PREVIOUS runs on the other
  * SMs at the same time: a memory-bound decode beside a tensor-core chunk prefill, as in a
  * continuous-batching step ("vLLM", section Continuous Batching).  The work is the same;
- * only where and when it runs changes.  Other unknown bits are rejected
+ * only where and when it runs changes, and the workspace of pa_decode_workspace_size()
+ * suffices under any budget.  Other unknown bits are rejected
  * (PA_ERR_INVALID_ARG). */
 #define PA_LAUNCH_DEFAULT 0u
 #define PA_LAUNCH_OVERLAP_PREVIOUS 1u

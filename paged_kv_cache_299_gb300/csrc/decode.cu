@@ -1097,9 +1097,16 @@ cudaError_t plan_decode(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_he
     // can take in equal numbers (a multiple of the warp count once there are more runs than
     // warps), split evenly over the real tile count: no warp ends a whole run after the rest.
     const int64_t max_tiles = partition_tokens / kBlockSize;
-    runs = (tiles_upper + max_tiles - 1) / max_tiles;
-    const int64_t warps = resident * kWarps;
-    if (runs > warps) runs = (runs + warps - 1) / warps * warps;
+    const int64_t least = (tiles_upper + max_tiles - 1) / max_tiles;
+    auto even = [least](int64_t warps) {
+      return least > warps ? (least + warps - 1) / warps * warps : least;
+    };
+    runs = even(resident * kWarps);
+    // Under an SM budget, never more runs (partials) than on the whole device, so the
+    // workspace the size query returns (which knows no budget) always suffices; the warps
+    // then take one run more or less each.
+    const int64_t runs_full = even(static_cast<int64_t>(sms) * ctas_per_sm * kWarps);
+    if (runs > runs_full) runs = runs_full;
     plan->chunk = 0;
     plan->tile_bound = tiles_upper;
   } else {

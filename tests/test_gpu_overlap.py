@@ -179,3 +179,30 @@ def test_decode_beside_a_chunk_prefill_on_separate_sms(decode_share):
     torch.cuda.synchronize()
     assert st.check_status() == pa.PA_OK
     assert torch.equal(graph_p, serial_p) and torch.equal(graph_d, conc_d)
+
+
+@pytest.mark.parametrize("decode_sms", [1, 50, 100])
+def test_fixed_partitions_under_an_sm_budget_fit_the_size_query(decode_sms):
+    """Fixed 512-token partitions of 64000 tokens give 1000 runs.  Under an SM budget with
+    fewer warps than runs, rounding the runs up to a multiple of the budget's warp count
+    would need more partials than the size query (which knows no budget) provides; the plan
+    keeps the whole device's run count instead.  The call succeeds in exactly that
+    workspace, reuses it, and matches the oracle."""
+    w = wl.make_workload("budget", [15999, 15999, 14000, 9000], [1, 1, 1, 1], seed=31,
+                         pool_slack=0.05)
+    step = GpuStep(w)
+    mx = int(w.context_lens.max())
+    need = pa.pa_decode_workspace_size(4, 8, 32, mx, 512)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(2):
+        out = torch.empty_like(step.vals["q_decode"])
+        pa.pa_decode(out, step.vals["q_decode"], step.kc, step.vc, step.bt, step.ctx, w.scale,
+                     mx, 512, workspace=ws, device_status=step.status,
+                     launch_flags=pa.PA_LAUNCH_MAX_SMS(decode_sms))
+        outs.append(out)
+    assert step.check_status() == pa.PA_OK
+    assert torch.equal(outs[0], outs[1])
+    ref = oracle_step(w, host_vals(step.vals))["decode"]
+    mxe, mean = errors(outs[0].float().cpu().numpy(), ref)
+    assert mxe <= ATOL_MAX and mean <= ATOL_MEAN, (decode_sms, mxe, mean)
