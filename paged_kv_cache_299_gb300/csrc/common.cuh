@@ -120,6 +120,15 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// Hint: bring `bytes` (a multiple of 16) from a 16-byte-aligned global address into L2 with
+// one bulk request under an L2 cache policy; nothing lands in shared memory and nothing
+// signals completion.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes, uint64_t policy) {
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(p),
+               "r"(bytes), "l"(policy)
+               : "memory");
+}
+
 __device__ __forceinline__ uint4 lds128(const void* p) {
   return *reinterpret_cast<const uint4*>(p);
 }

@@ -18,7 +18,8 @@
 //     completing on the stage's mbarrier, and refills a stage as soon as the warp has
 //     consumed it.  The block-table entries are fetched 32 at a time, one window ahead.
 //     No producer warp, no release barriers, no block-wide synchronisation while
-//     streaming.
+//     streaming.  Before waiting for the previous grid (programmatic dependent launch),
+//     a warp with a long run also asks L2 for its next 8 tiles.
 //   * The tile arithmetic is a small dense contraction per warp: the GROUP query heads
 //     sharing a K/V head against 16 tokens, S = Q K^T ([GROUP x 64] x [64 x 16]) and
 //     O += P V ([GROUP x 16] x [16 x 64]).  It runs on the tensor cores as mma.sync
@@ -51,6 +52,11 @@ constexpr int kWindow = 32;         // block-table entries fetched per window
 constexpr int kPartialFloats = kHeadDim + 2;  // o[64], max (log2 units), sum
 constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale when max grows > 2^8
 constexpr int kMinTilesPerRun = 2;
+// Before its dependency wait a warp asks L2 for up to this many tiles past its ring (from
+// its first block-table window), when the warps average at least kPrefetchMinTilesPerWarp
+// tiles each and the launch has every SM to itself.
+constexpr int kPrefetchTiles = 8;
+constexpr int kPrefetchMinTilesPerWarp = 48;
 // Longest context whose split segments are merged inside the attention kernel; longer ones
 // (many pieces per segment) go to the parallel merge kernel.
 constexpr int kFusedMergeMaxContext = 8192;
@@ -82,6 +88,7 @@ struct KParams {
   int32_t* seg_count;   // [num_seqs * Hkv] pieces published per split segment (fused merge);
                         // zero between calls: the merging warp resets its counter
   int32_t fused_merge;  // 1: the last warp to finish a split segment merges it in place
+  int32_t prefetch_tiles;  // tiles past the ring a warp may ask L2 for before its wait
   const uint8_t* k_new;  // optional [num_seqs][Hkv][64] bf16: token at position L-1 to store
   const uint8_t* v_new;  //   (fused append: stored to its slot and used in attention)
   uint8_t* key_cache_w;    // writable views of the pools (fused append)
@@ -640,6 +647,18 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
     ++cur_i;
   };
   for (int i = 0; i < kStagesPerWarp; ++i) issue_one();
+  // The next tiles of the first window, past the ring, are requested into L2 now: under
+  // programmatic dependent launch the wait below lasts until the previous grid's slowest
+  // CTAs end, and with long runs per warp the extra requests keep DRAM busy meanwhile
+  // (and at the start of a launch).  Lane i holds entry i of the window; entries before
+  // cur_i are in the ring already.
+  const int64_t busy_warps = p.grid < total_warps ? p.grid : total_warps;
+  if (p.prefetch_tiles > 0 && total >= kPrefetchMinTilesPerWarp * busy_warps &&
+      lane >= cur_i && lane < cur.n && lane < cur_i + p.prefetch_tiles && cur.tile >= 0) {
+    const int64_t off = static_cast<int64_t>(cur.tile) * kTileBytes;
+    bulk_prefetch_l2(p.key_cache + off, kTileBytes, policy);  // evict-first, as the loads
+    bulk_prefetch_l2(p.value_cache + off, kTileBytes, policy);
+  }
 
   // Everything above reads only block_tables, context_lens (q_rows) and K/V tiles.  Under
   // programmatic dependent launch the previous kernel in the stream may still be running
@@ -1019,6 +1038,7 @@ cudaError_t launch(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t str
   p.seg_count = reinterpret_cast<int32_t*>(ws + plan.ws_count_offset);
   p.partials = reinterpret_cast<float*>(ws + plan.ws_meta_bytes);
   p.fused_merge = plan.fused_merge ? 1 : 0;
+  p.prefetch_tiles = plan.prefetch_tiles;
   p.k_new = static_cast<const uint8_t*>(a.k_new);
   p.v_new = static_cast<const uint8_t*>(a.v_new);
   p.key_cache_w = static_cast<uint8_t*>(const_cast<void*>(a.key_cache));
@@ -1127,6 +1147,8 @@ cudaError_t plan_decode(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_he
       partition_tokens > 0 ? (max_context_len + partition_tokens - 1) / partition_tokens
                            : runs / (static_cast<int64_t>(num_seqs) * num_kv_heads) + 2;
   plan->merge_split_heads = !plan->fused_merge && seg_pieces >= kMergeSplitPieces;
+  // Under an SM budget another kernel shares DRAM and L2 with this one: no extra requests.
+  plan->prefetch_tiles = max_sms > 0 && max_sms < sms ? 0 : kPrefetchTiles;
   plan->ws_count_offset = (16 + sizeof(int32_t) * (num_seqs + 1) + 255) / 256 * 256;
   plan->ws_meta_bytes = plan->ws_count_offset +
                         (sizeof(int32_t) * num_seqs * num_kv_heads + 255) / 256 * 256;
