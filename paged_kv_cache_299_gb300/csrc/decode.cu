@@ -52,6 +52,7 @@ constexpr int kWindow = 32;         // block-table entries fetched per window
 constexpr int kPartialFloats = kHeadDim + 2;  // o[64], max (log2 units), sum
 constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale when max grows > 2^8
 constexpr int kMinTilesPerRun = 2;
+constexpr int kOneSeqMaxTilesPerWarp = 4;  // a single sequence up to this: one CTA per head
 // Before its dependency wait a warp asks L2 for up to this many tiles past its ring (from
 // its first block-table window), when the warps average at least kPrefetchMinTilesPerWarp
 // tiles each and the launch has every SM to itself.
@@ -1134,6 +1135,13 @@ cudaError_t plan_decode(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_he
     runs = resident * kWarps;
     const int64_t by_size = (tiles_upper + kMinTilesPerRun - 1) / kMinTilesPerRun;
     if (by_size < runs) runs = by_size;
+    // One short sequence: one CTA per K/V head.  Its tiles (num_kv_heads segments of equal
+    // length) split into num_kv_heads * kWarps equal runs put every segment's pieces on
+    // one CTA, so they publish and merge with CTA-scope ordering instead of device-scope
+    // fences.
+    if (num_seqs == 1 && num_kv_heads <= resident &&
+        tiles_upper <= static_cast<int64_t>(kOneSeqMaxTilesPerWarp) * num_kv_heads * kWarps)
+      runs = static_cast<int64_t>(num_kv_heads) * kWarps;
   }
   if (runs < 1) runs = 1;
   if (runs > 0x7fffffff) return cudaErrorInvalidValue;
