@@ -19,7 +19,7 @@
 //     consumed it.  The block-table entries are fetched 32 at a time, one window ahead.
 //     No producer warp, no release barriers, no block-wide synchronisation while
 //     streaming.  Before waiting for the previous grid (programmatic dependent launch),
-//     a warp with a long run also asks L2 for its next 8 tiles.
+//     a warp with a long run also asks L2 for its next 8 tiles (2 for shorter runs).
 //   * The tile arithmetic is a small dense contraction per warp: the GROUP query heads
 //     sharing a K/V head against 16 tokens, S = Q K^T ([GROUP x 64] x [64 x 16]) and
 //     O += P V ([GROUP x 16] x [16 x 64]).  It runs on the tensor cores as mma.sync
@@ -53,11 +53,14 @@ constexpr int kPartialFloats = kHeadDim + 2;  // o[64], max (log2 units), sum
 constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale when max grows > 2^8
 constexpr int kMinTilesPerRun = 2;
 constexpr int kOneSeqMaxTilesPerWarp = 4;  // a single sequence up to this: one CTA per head
-// Before its dependency wait a warp asks L2 for up to this many tiles past its ring (from
-// its first block-table window), when the warps average at least kPrefetchMinTilesPerWarp
-// tiles each and the launch has every SM to itself.
+// Before its dependency wait a warp asks L2 for up to kPrefetchTiles tiles past its ring
+// (from its first block-table window) when the warps average at least
+// kPrefetchMinTilesPerWarp tiles each, kPrefetchTilesShort when they average at least
+// kPrefetchShortMinTilesPerWarp, and none when the launch shares the GPU (an SM budget).
 constexpr int kPrefetchTiles = 8;
 constexpr int kPrefetchMinTilesPerWarp = 48;
+constexpr int kPrefetchTilesShort = 2;
+constexpr int kPrefetchShortMinTilesPerWarp = 12;
 // Longest context whose split segments are merged inside the attention kernel; longer ones
 // (many pieces per segment) go to the parallel merge kernel.
 constexpr int kFusedMergeMaxContext = 8192;
@@ -89,7 +92,7 @@ struct KParams {
   int32_t* seg_count;   // [num_seqs * Hkv] pieces published per split segment (fused merge);
                         // zero between calls: the merging warp resets its counter
   int32_t fused_merge;  // 1: the last warp to finish a split segment merges it in place
-  int32_t prefetch_tiles;  // tiles past the ring a warp may ask L2 for before its wait
+  int32_t prefetch_ok;  // 1: a warp may ask L2 for tiles past its ring before its wait
   const uint8_t* k_new;  // optional [num_seqs][Hkv][64] bf16: token at position L-1 to store
   const uint8_t* v_new;  //   (fused append: stored to its slot and used in attention)
   uint8_t* key_cache_w;    // writable views of the pools (fused append)
@@ -654,8 +657,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   // (and at the start of a launch).  Lane i holds entry i of the window; entries before
   // cur_i are in the ring already.
   const int64_t busy_warps = p.grid < total_warps ? p.grid : total_warps;
-  if (p.prefetch_tiles > 0 && total >= kPrefetchMinTilesPerWarp * busy_warps &&
-      lane >= cur_i && lane < cur.n && lane < cur_i + p.prefetch_tiles && cur.tile >= 0) {
+  const int pf = !p.prefetch_ok                                        ? 0
+                 : total >= kPrefetchMinTilesPerWarp * busy_warps      ? kPrefetchTiles
+                 : total >= kPrefetchShortMinTilesPerWarp * busy_warps ? kPrefetchTilesShort
+                                                                       : 0;
+  if (pf > 0 && lane >= cur_i && lane < cur.n && lane < cur_i + pf && cur.tile >= 0) {
     const int64_t off = static_cast<int64_t>(cur.tile) * kTileBytes;
     bulk_prefetch_l2(p.key_cache + off, kTileBytes, policy);  // evict-first, as the loads
     bulk_prefetch_l2(p.value_cache + off, kTileBytes, policy);
@@ -1039,7 +1045,7 @@ cudaError_t launch(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t str
   p.seg_count = reinterpret_cast<int32_t*>(ws + plan.ws_count_offset);
   p.partials = reinterpret_cast<float*>(ws + plan.ws_meta_bytes);
   p.fused_merge = plan.fused_merge ? 1 : 0;
-  p.prefetch_tiles = plan.prefetch_tiles;
+  p.prefetch_ok = plan.prefetch_ok ? 1 : 0;
   p.k_new = static_cast<const uint8_t*>(a.k_new);
   p.v_new = static_cast<const uint8_t*>(a.v_new);
   p.key_cache_w = static_cast<uint8_t*>(const_cast<void*>(a.key_cache));
@@ -1156,7 +1162,7 @@ cudaError_t plan_decode(int32_t num_seqs, int32_t num_kv_heads, int32_t num_q_he
                            : runs / (static_cast<int64_t>(num_seqs) * num_kv_heads) + 2;
   plan->merge_split_heads = !plan->fused_merge && seg_pieces >= kMergeSplitPieces;
   // Under an SM budget another kernel shares DRAM and L2 with this one: no extra requests.
-  plan->prefetch_tiles = max_sms > 0 && max_sms < sms ? 0 : kPrefetchTiles;
+  plan->prefetch_ok = !(max_sms > 0 && max_sms < sms);
   plan->ws_count_offset = (16 + sizeof(int32_t) * (num_seqs + 1) + 255) / 256 * 256;
   plan->ws_meta_bytes = plan->ws_count_offset +
                         (sizeof(int32_t) * num_seqs * num_kv_heads + 255) / 256 * 256;

@@ -38,7 +38,7 @@ struct DecodePlan {
   size_t smem_bytes;  // dynamic shared memory of the attention kernel
   bool fused_merge;          // split segments merged inside the attention kernel
   bool merge_split_heads;    // otherwise: the merge kernel takes one CTA per query head
-  int prefetch_tiles;        // tiles past the ring a warp may ask L2 for before its wait
+  bool prefetch_ok;          // warps may ask L2 for tiles past their ring before the wait
   size_t ws_count_offset;    // offset of the per-segment piece counters (must start zeroed)
   size_t ws_meta_bytes;      // offset of the partials inside the workspace
   size_t workspace_bytes;    // total workspace

@@ -56,6 +56,30 @@ def test_config1_single_sequence():
     full_check(wl.single_sequence_300())
 
 
+@pytest.mark.parametrize("L", [1, 17, 300, 768, 769])
+def test_single_sequence_one_cta_per_head(L):
+    """One sequence of up to 768 tokens (4 tiles per warp) runs one CTA per K/V head, all
+    of a head's pieces merged inside its CTA.  At and around that bound, and with a host
+    bound of the context above the real one (768: the same plan; 2048: the general one),
+    the decode matches the oracle and a reused workspace gives the same bits."""
+    w = wl.make_workload(f"one{L}", [L - 1], [1], seed=50 + L, pool_slack=0.5)
+    step, _, ref = full_check(w)
+    for max_ctx in sorted({L, 768, 2048}):
+        if max_ctx < L:
+            continue
+        ws = torch.zeros(pa.pa_decode_workspace_size(1, 8, 32, max_ctx, 0), dtype=torch.uint8,
+                         device="cuda")
+        outs = []
+        for _ in range(2):
+            out = torch.empty_like(step.vals["q_decode"])
+            pa.pa_decode(out, step.vals["q_decode"], step.kc, step.vc, step.bt, step.ctx,
+                         w.scale, max_ctx, workspace=ws, device_status=step.status)
+            outs.append(out)
+        assert step.check_status() == pa.PA_OK
+        assert torch.equal(outs[0], outs[1])
+        assert_close(outs[0], ref["decode"], f"one sequence of {L} tokens, bound {max_ctx}")
+
+
 def test_config2_decode_batch64():
     full_check(wl.decode_batch64_uniform())
 
